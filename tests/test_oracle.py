@@ -1,0 +1,500 @@
+"""Pins of the fp64 oracle to what the GrowPage paper and mathematics fix.
+
+Every check here is independent of the oracle's own code path: hand-derived
+golden values (tests/golden/*.json), closed forms, invariants, brute force on
+tiny inputs, and special cases that reduce to a library routine.  The last
+group plants plausible mistakes in the oracle (on the CPU) and checks that a
+pin catches each one.
+"""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from oracle import growpage as og
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# Eq. 2: p-coverage demand
+# ---------------------------------------------------------------------------
+
+def check_dp_golden(dp=og.coverage_demand):
+    for case in _golden("coverage_demand.json")["cases"]:
+        if "a_uniform" in case:
+            n = case["a_uniform"]
+            a = np.full(n, 1.0 / n)
+        else:
+            a = np.array(case["a"], dtype=np.float64)
+        got = dp(a, case["p"])
+        assert got == case["expect"], (case, got)
+
+
+def test_dp_golden():
+    check_dp_golden()
+
+
+@pytest.mark.parametrize("n", [3, 7, 100, 1000, 4093])
+def test_dp_uniform_closed_form(n):
+    # uniform weights: sum of k weights is k/n, so D_p = ceil(p n) when p n is
+    # not an integer (Eq. 2)
+    rng = np.random.default_rng(n)
+    for p in rng.uniform(0.01, 0.999, size=20):
+        if abs(p * n - round(p * n)) < 1e-6:
+            continue
+        assert og.coverage_demand(np.full(n, 1.0 / n), p) == math.ceil(p * n)
+
+
+def test_dp_one_hot_and_monotone():
+    rng = np.random.default_rng(1)
+    for n in (1, 2, 17, 300):
+        e = np.zeros(n)
+        e[rng.integers(n)] = 1.0
+        assert og.coverage_demand(e, 0.99) == 1
+    for _ in range(50):
+        n = int(rng.integers(1, 400))
+        a = rng.gamma(0.3, size=n)
+        a /= a.sum()
+        ps = np.sort(rng.uniform(0, 1, size=30))
+        ds = [og.coverage_demand(a, p) for p in ps]
+        assert all(x <= y for x, y in zip(ds, ds[1:]))     # monotone in p
+        assert all(1 <= x <= n for x in ds)
+
+
+def test_dp_bruteforce_small():
+    # D_p is the size of the smallest subset whose mass reaches p (the largest
+    # mass of a k-subset is that of the top-k weights): enumerate subsets.
+    rng = np.random.default_rng(2)
+    for _ in range(200):
+        n = int(rng.integers(1, 9))
+        a = rng.dirichlet(np.full(n, 0.5))
+        p = float(rng.uniform(0.05, 0.999))
+        best = None
+        for k in range(1, n + 1):
+            if max(sum(a[list(s)]) for s in itertools.combinations(range(n), k)) >= p:
+                best = k
+                break
+        assert og.coverage_demand(a, p) == best
+
+
+# ---------------------------------------------------------------------------
+# Eqs. 3-5, Theorem 3.1 (brute force over all subsets, N <= 12)
+# ---------------------------------------------------------------------------
+
+def check_theorem31(dp=og.coverage_demand, seed=3, trials=40):
+    rng = np.random.default_rng(seed)
+    for t in range(trials):
+        n = int(rng.integers(1, 13))
+        if t % 3 == 0:
+            a = rng.dirichlet(np.full(n, 0.2))          # concentrated
+        elif t % 3 == 1:
+            a = rng.dirichlet(np.full(n, 5.0))          # diffuse
+        else:
+            a = np.sort(rng.dirichlet(np.ones(n)))[::-1]
+        vmax = float(rng.uniform(0.5, 3.0))
+        delta = float(rng.uniform(0.01, 2 * vmax - 0.01))
+        cap = og.worst_case_capacity(a, delta, vmax)
+        assert cap == dp(a, 1.0 - delta / (2.0 * vmax)), (a, delta, vmax)
+
+
+def test_theorem31_bruteforce():
+    check_theorem31()
+
+
+def test_theorem31_golden():
+    for case in _golden("theorem31.json")["cases"]:
+        a = np.array(case["a"])
+        if "expect_capacity" in case:
+            got = og.worst_case_capacity(a, case["delta"], case["vmax"])
+            assert got == case["expect_capacity"]
+            assert og.coverage_demand(a, 1 - case["delta"] / (2 * case["vmax"])) == got
+        else:
+            got = og.worst_case_error(a, case["subset"], case["vmax"])
+            assert got == pytest.approx(case["expect_error"], abs=1e-15)
+
+
+def test_eq5_tight_construction_and_bound():
+    # App. C: with v_i = -Vmax u on S and +Vmax u off S the error equals
+    # 2 Vmax (1 - m(S)); no admissible v exceeds it.
+    rng = np.random.default_rng(4)
+    for _ in range(60):
+        n = int(rng.integers(2, 10))
+        d = int(rng.integers(1, 6))
+        a = rng.dirichlet(np.ones(n))
+        vmax = float(rng.uniform(0.1, 4))
+        k = int(rng.integers(1, n))
+        sub = sorted(rng.choice(n, size=k, replace=False).tolist())
+        u = rng.normal(size=d)
+        u /= np.linalg.norm(u)
+        v = np.array([(-vmax if i in sub else vmax) * u for i in range(n)])
+        err = np.linalg.norm(og.attention_output(a, v) -
+                             og.renormalised_output(a, v, sub))
+        bound = og.worst_case_error(a, sub, vmax)
+        assert err == pytest.approx(bound, rel=1e-12, abs=1e-14)
+        for _ in range(20):
+            w = rng.normal(size=(n, d))
+            w *= (vmax * rng.uniform(0, 1, size=(n, 1))) / np.linalg.norm(w, axis=1, keepdims=True)
+            e2 = np.linalg.norm(og.attention_output(a, w) - og.renormalised_output(a, w, sub))
+            assert e2 <= bound * (1 + 1e-12) + 1e-14
+
+
+# ---------------------------------------------------------------------------
+# Eq. 6 and App. E.1: EMA
+# ---------------------------------------------------------------------------
+
+def check_ema_golden(update=og.ema_update):
+    g = _golden("ema.json")
+    d = 3
+    s = l = None
+    seq = [np.zeros(d), np.ones(d)] + [np.zeros(d)] * 4
+    hist_s, hist_l = {}, {}
+    for t, q in enumerate(seq):
+        s, l = update(s, l, q, t == 0, g["beta_s"], g["beta_l"])
+        hist_s[t], hist_l[t] = s[0], l[0]
+    for t, v in g["short_after_steps"].items():
+        assert hist_s[int(t)] == pytest.approx(v, rel=1e-12)
+    for t, v in g["long_after_steps"].items():
+        assert hist_l[int(t)] == pytest.approx(v, rel=1e-12)
+
+
+def test_ema_impulse_golden():
+    check_ema_golden()
+
+
+def test_ema_constant_fixed_point_and_beta0():
+    rng = np.random.default_rng(5)
+    q = rng.normal(size=(2, 4, 8))
+    s, l = og.ema_update(None, None, q, True, 0.9, 0.999)   # init (App. E.1)
+    assert np.array_equal(s, q) and np.array_equal(l, q)
+    for _ in range(100):
+        s, l = og.ema_update(s, l, q, False, 0.9, 0.999)
+    assert np.allclose(s, q, rtol=1e-13) and np.allclose(l, q, rtol=1e-13)
+    # beta_S = 0 reduces the short summary to the current query (Sec. 5.3)
+    q2 = rng.normal(size=q.shape)
+    s2, _ = og.ema_update(s, l, q2, False, 0.0, 0.999)
+    assert np.array_equal(s2, q2)
+    # the init overwrites stale state without clearing
+    s3, l3 = og.ema_update(s2 * 7, l * 3, q, True, 0.9, 0.999)
+    assert np.array_equal(s3, q) and np.array_equal(l3, q)
+
+
+def test_ema_matches_geometric_sum():
+    # closed form of the recursion: qbar_T = beta^T q_0 + sum_t (1-beta) beta^(T-t) q_t
+    rng = np.random.default_rng(6)
+    qs = rng.normal(size=(30, 5))
+    for beta in (0.9, 0.999, 0.5):
+        s = None
+        for t, q in enumerate(qs):
+            s, _ = og.ema_update(s, s, q, t == 0, beta, beta)
+        T = len(qs) - 1
+        ref = beta ** T * qs[0] + sum((1 - beta) * beta ** (T - t) * qs[t] for t in range(1, T + 1))
+        assert np.allclose(s, ref, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Eq. 12 calibration and RoPE
+# ---------------------------------------------------------------------------
+
+def test_calibration_restores_rms():
+    rng = np.random.default_rng(7)
+    q = rng.normal(size=(3, 4, 16)) * rng.uniform(0.1, 5, size=(3, 4, 1))
+    qbar = rng.normal(size=(3, 4, 16)) * 0.01
+    qt = og.calibrate(qbar, q)
+    assert np.allclose(og.rms(qt), og.rms(q), rtol=1e-13)
+    # direction unchanged, positive scale
+    cos = np.sum(qt * qbar, -1) / (np.linalg.norm(qt, axis=-1) * np.linalg.norm(qbar, axis=-1))
+    assert np.allclose(cos, 1.0, rtol=1e-13)
+    assert np.array_equal(og.calibrate(np.zeros((2, 8)), rng.normal(size=(2, 8))), np.zeros((2, 8)))
+
+
+def test_rope_rotation_properties():
+    rng = np.random.default_rng(8)
+    for d in (2, 8, 64, 128):
+        x = rng.normal(size=(5, d))
+        y = rng.normal(size=(5, d))
+        theta = 1e4
+        assert np.array_equal(og.rope(x, 0, theta), x)                 # identity at 0
+        for pos in (1, 17, 1000, 32768):
+            rx = og.rope(x, pos, theta)
+            assert np.allclose(np.linalg.norm(rx, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-12)
+            assert np.allclose(og.rope(rx, -pos, theta), x, atol=1e-9)     # inverse
+            # relative position: R_m x . R_n y = x . R_{n-m} y
+            m, n = pos, pos + 37
+            lhs = np.sum(og.rope(x, m, theta) * og.rope(y, n, theta), -1)
+            rhs = np.sum(x * og.rope(y, n - m, theta), -1)
+            assert np.allclose(lhs, rhs, rtol=1e-9, atol=1e-9)
+    # d = 2: a plain rotation by pos radians (theta^0 = 1)
+    x = np.array([1.0, 0.0])
+    assert np.allclose(og.rope(x, 1, 1e4), [math.cos(1.0), math.sin(1.0)], atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# scores, softmax, GQA mean
+# ---------------------------------------------------------------------------
+
+def test_logits_against_loops_and_softmax_against_scipy():
+    rng = np.random.default_rng(9)
+    q = rng.normal(size=(3, 8))
+    k = rng.normal(size=(11, 8))
+    z = og.logits(q, k)
+    for r in range(3):
+        for i in range(11):
+            ref = sum(q[r, j] * k[i, j] for j in range(8)) / math.sqrt(8)
+            assert z[r, i] == pytest.approx(ref, rel=1e-13, abs=1e-14)
+    big = rng.normal(size=(4, 500)) * 30
+    assert np.allclose(og.softmax(big), scipy.special.softmax(big, axis=-1), rtol=1e-12, atol=1e-300)
+    a = og.kv_head_distribution(big)
+    assert a.sum() == pytest.approx(1.0, abs=1e-13)
+    # G = 1 reduces to the single query head's softmax
+    assert np.allclose(og.kv_head_distribution(big[:1]), scipy.special.softmax(big[0]), rtol=1e-12)
+
+
+def test_unit_candidate_sets():
+    rng = np.random.default_rng(10)
+    b, P, R, G, d = 8, 3, 2, 2, 4
+    keys = rng.normal(size=(P * b, d))
+    qt = rng.normal(size=(2, G, d))
+    u = og.unit_boundary(qt, keys, P, b, R, 0.9)
+    assert u.a_dem.shape == (2, (P - 1) * b)
+    assert u.a_cmp.shape == (2, P * b - R)
+    # demand distribution: mean over the G heads of a softmax over Cdem only
+    for x in range(2):
+        z = np.array([[qt[x, g] @ keys[i] / 2.0 for i in range((P - 1) * b)] for g in range(G)])
+        ref = np.mean([scipy.special.softmax(z[g]) for g in range(G)], axis=0)
+        assert np.allclose(u.a_dem[x], ref, rtol=1e-12)
+    assert np.allclose(u.s, np.maximum(u.a_cmp[0], u.a_cmp[1]))
+
+
+# ---------------------------------------------------------------------------
+# Eq. 8 and the decision rule
+# ---------------------------------------------------------------------------
+
+def test_decide_rules():
+    assert og.decide(0.01, 4, 10, 0, 0.0).kind == og.GROW
+    assert og.decide(0.0, 4, 10, 0, 0.0).kind == og.COMPRESS       # Delta = tau compresses
+    assert og.decide(-0.01, 4, 10, 0, 0.0).kind == og.COMPRESS
+    a = og.decide(0.01, 4, 0, 0, 0.0)
+    assert a.kind == og.COMPRESS and a.fallback                   # fallback (Sec. 4.2)
+    a = og.decide(0.01, 4, 3, 3, 0.0)
+    assert a.kind == og.COMPRESS and a.fallback                   # reserve respected
+    a = og.decide(-1.0, 1, 0, 0, 0.0)
+    assert a.kind == og.GROW and a.forced                         # P = 1
+    assert og.decide(0.5, 4, 10, 0, 0.0, policy="fixed").kind == og.COMPRESS
+    assert og.decide(0.002, 4, 10, 0, 0.003).kind == og.COMPRESS  # tau threshold
+
+
+def test_demand_trend_forms_agree_in_sign():
+    rng = np.random.default_rng(11)
+    for _ in range(100):
+        ks = rng.integers(1, 500, size=(4, 2))
+        kl = rng.integers(1, 500, size=(4, 2))
+        n = 768
+        d = og.demand_trend(ks, kl, n)
+        raw = int(ks.sum() - kl.sum())
+        assert np.sign(d) == np.sign(raw)                        # Eq. 8 vs raw D_p difference
+        assert d == pytest.approx(raw / (n * ks.size), rel=1e-12, abs=1e-15)
+
+
+def test_planted_tiny_workloads_take_both_actions():
+    # Sec. 3.2: a more concentrated short summary (Delta < 0) compresses; a
+    # more diffuse one (Delta > 0) grows.  The synthetic tiny workloads put a
+    # concentrated history early or late.
+    import synth
+    for variant, expect in (("grow", og.GROW), ("compress", og.COMPRESS)):
+        w = synth.make_workload("tiny", variant=variant)
+        cfg = _cfg(w)
+        s = l = None
+        for t, q in enumerate(w.history):
+            s, l = og.ema_update(s, l, q[:, 0].double().numpy(), t == 0, 0.9, 0.999)
+        q_cur = w.history[-1][:, 0].double().numpy()
+        res = og.request_boundary(s, l, q_cur, w.k_cache.double().numpy(),
+                                  w.block_tables[0], w.positions[0], cfg)
+        act = og.decide(res["delta"], len(w.block_tables[0]), 4, 0, 0.0)
+        assert act.kind == expect, (variant, res["delta"])
+
+
+def _cfg(w):
+    return {"num_kv_heads": w.shape.num_kv_heads, "rope_theta": w.shape.rope_theta,
+            "page_size": w.page_size, "recent_window": 16, "p": 0.99}
+
+
+# ---------------------------------------------------------------------------
+# Eq. 10 and the window mask
+# ---------------------------------------------------------------------------
+
+def _check_selection(s, P, b, R, k_loc, keep):
+    n_cmp = P * b - R
+    k_t = (P - 1) * b - R
+    assert keep.sum() == (P - 1) * b                        # exactly one page freed
+    assert keep[n_cmp:].all()                               # recent window kept
+    quota = min(k_loc, k_t // P)
+    for j in range(P):
+        lo, hi = j * b, min((j + 1) * b, n_cmp)
+        kj = min(quota, hi - lo)
+        blk = np.arange(lo, hi)
+        # the block's own top-kj (by score, ties to lower index) are kept
+        order = sorted(blk.tolist(), key=lambda i: (-s[i], i))
+        assert keep[order[:kj]].all()
+
+
+def test_selection_invariants_and_global_top():
+    rng = np.random.default_rng(12)
+    for t in range(300):
+        b = int(rng.integers(2, 9))
+        P = int(rng.integers(2, 6))
+        R = int(rng.integers(0, b))
+        k_loc = int(rng.integers(0, b + 2))
+        s = rng.dirichlet(np.full(P * b, 0.3))
+        if t % 5 == 0:
+            s = np.round(s * 20) / 20                            # many ties
+        keep = og.select_retained(s, P, b, R, k_loc)
+        _check_selection(s, P, b, R, k_loc, keep)
+        # the global fill is a top set of what the blocks left: no dropped
+        # candidate beats a globally added one (ties: lower index first)
+        n_cmp = P * b - R
+        k_t = (P - 1) * b - R
+        quota = min(k_loc, k_t // P)
+        loc = np.zeros(P * b, bool)
+        for j in range(P):
+            lo, hi = j * b, min((j + 1) * b, n_cmp)
+            order = sorted(range(lo, hi), key=lambda i: (-s[i], i))
+            loc[order[:min(quota, hi - lo)]] = True
+        glob = keep.copy()
+        glob[loc] = False
+        glob[n_cmp:] = False
+        dropped = np.nonzero(~keep[:n_cmp])[0]
+        for i in np.nonzero(glob)[0]:
+            for j in dropped:
+                assert (s[i], -i) > (s[j], -j)
+
+
+def test_selection_kloc0_is_plain_topk():
+    # k_loc = 0 leaves only the global top-K_t (special case of Eq. 10)
+    rng = np.random.default_rng(13)
+    for _ in range(50):
+        b, P, R = 16, 4, 3
+        s = rng.random(P * b)
+        keep = og.select_retained(s, P, b, R, 0)
+        k_t = (P - 1) * b - R
+        top = np.argsort(-s[:P * b - R], kind="stable")[:k_t]
+        ref = np.zeros(P * b, bool)
+        ref[top] = True
+        ref[P * b - R:] = True
+        assert np.array_equal(keep, ref)
+
+
+def test_selection_kloc_changes_which_not_how_many():
+    # App. D.2: k_loc changes which states are kept, not how many
+    rng = np.random.default_rng(14)
+    s = rng.dirichlet(np.full(5 * 256, 0.2))
+    counts = {int(og.select_retained(s, 5, 256, 16, k).sum()) for k in (0, 16, 32, 64, 128)}
+    assert counts == {4 * 256}
+
+
+# ---------------------------------------------------------------------------
+# App. E.2: pool, copy-on-write, compaction
+# ---------------------------------------------------------------------------
+
+def test_pool_cow_and_compaction():
+    rng = np.random.default_rng(15)
+    pool = og.PagePool(12)
+    a = [pool.alloc() for _ in range(4)]                 # 0..3 lowest first
+    assert a == [0, 1, 2, 3]
+    pool.ref(0)
+    pool.ref(1)                                          # prefix pages 0,1 shared
+    total_before = sum(pool.refcount)
+    new, replaced = og.cow_plan(a, pool)
+    assert replaced == [0, 1] and new == [4, 5, 2, 3]    # lowest free, ascending order
+    og.release_replaced(replaced, pool)
+    assert pool.refcount[0] == 1 and pool.refcount[1] == 1
+    assert sum(pool.refcount) == total_before + 2 - 2
+    # not enough pages: nothing changes
+    pool2 = og.PagePool(3)
+    t = [pool2.alloc(), pool2.alloc(), pool2.alloc()]
+    pool2.ref(0)
+    pool2.ref(1)
+    before = list(pool2.refcount)
+    with pytest.raises(MemoryError):
+        og.cow_plan(t, pool2)
+    assert pool2.refcount == before
+    # compaction of one request, two layers, one head
+    L, b, d = 2, 4, 3
+    P = 3
+    k = rng.normal(size=(L, 12, 1, b, d))
+    v = rng.normal(size=(L, 12, 1, b, d))
+    old = [7, 2, 9]
+    newt = [7, 11, 9]
+    keep = np.zeros((L, 1, P * b), bool)
+    for layer in range(L):
+        keep[layer, 0, rng.choice(P * b - 1, size=(P - 1) * b - 1, replace=False)] = True
+        keep[layer, 0, P * b - 1] = True
+    k2, v2 = og.compress_cache(k, v, old, newt, keep, b)
+    for layer in range(L):
+        rows = og.gather_logical(k, old, layer, 0)[keep[layer, 0]]
+        got = og.gather_logical(k2, newt, layer, 0)[:(P - 1) * b]
+        assert np.array_equal(got, rows)                 # order kept, bytes equal
+    assert np.array_equal(k2[:, 2], k[:, 2])             # replaced page untouched
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes (in the oracle, on the CPU) are caught by the pins
+# ---------------------------------------------------------------------------
+
+def _dp_strict(a, p):
+    srt = np.sort(np.asarray(a, float))[::-1]
+    cum = np.cumsum(srt)
+    hit = np.nonzero(cum > p)[0]
+    return int(hit[0]) + 1 if hit.size else srt.size
+
+
+def _dp_off_by_one(a, p):
+    return og.coverage_demand(a, p) + (1 if len(a) > 3 else 0)
+
+
+def _dp_ascending(a, p):
+    srt = np.sort(np.asarray(a, float))
+    cum = np.cumsum(srt)
+    hit = np.nonzero(cum >= p)[0]
+    return int(hit[0]) + 1 if hit.size else srt.size
+
+
+def _ema_swapped(s, l, q, first, bs, bl):
+    q = np.asarray(q, float)
+    if first:
+        return q.copy(), q.copy()
+    return (1 - bs) * s + bs * q, (1 - bl) * l + bl * q
+
+
+@pytest.mark.parametrize("mutant", [_dp_strict, _dp_off_by_one, _dp_ascending])
+def test_pins_catch_dp_mutants(mutant):
+    caught = 0
+    for check in (lambda: check_dp_golden(mutant), lambda: check_theorem31(mutant)):
+        try:
+            check()
+        except AssertionError:
+            caught += 1
+    assert caught >= 1
+
+
+def test_pins_catch_ema_mutant():
+    with pytest.raises(AssertionError):
+        check_ema_golden(_ema_swapped)
+
+
+def test_oracle_exports():
+    for name in ("ema_update", "calibrate", "rope", "logits", "softmax",
+                 "coverage_demand", "select_retained", "cow_plan", "compress_cache",
+                 "worst_case_capacity"):
+        assert hasattr(oracle, name)
