@@ -1,0 +1,275 @@
+/*
+ * growpage.h -- C ABI of a GB300-native (sm_103a) capacity-boundary engine
+ * for GrowPage ("GrowPage: On-Demand KV Budgeting for Efficient LLM
+ * Reasoning Serving", arXiv 2609.03494) over a paged KV cache.
+ *
+ * What the engine computes (paper sections in brackets):
+ *   - every decode step: the dual-timescale query summaries      [Sec. 3.2 Eq. 6, App. E.1]
+ *   - at a capacity boundary: calibration + RoPE of both summaries,
+ *     scores against every cached key through the block table,
+ *     softmax, GQA mean and the p-coverage demand D_p per
+ *     (layer, KV head), and the request-level trend Delta          [Sec. 3.2 Eqs. 7-8, App. E.1 Eq. 12]
+ *   - the decision Grow by One Page vs Compress & Hold             [Sec. 3.2, Sec. 4.2]
+ *   - Grow: append a fresh page to the block table                 [Sec. 3.3, Sec. 4.2]
+ *   - Compress & Hold: importance max(a^S, a^L), protected recent
+ *     window, block-local + global top-k, and copy-on-write
+ *     compaction of the retained K/V into (P-1) b slots            [Sec. 3.3 Eqs. 9-10, App. E.2]
+ *   - a refcounted page pool and a slot pool for the summaries    [Sec. 4.2, App. E.1 Eq. 11, App. E.2]
+ *
+ * Conventions
+ *   - Every call returns gp_status; nothing throws across the ABI.  The
+ *     text of the last failure is available from gp_last_error().
+ *   - Device pointers ("_dev") are CUDA device addresses owned by the caller
+ *     (for example PyTorch tensors); host pointers are plain memory owned by
+ *     the caller.  The engine owns the summary pool, its scratch buffers, the
+ *     page refcounts, the free-page list and the slot list.
+ *   - All device work is issued on the stream given to gp_create, in call
+ *     order.  gp_boundary_demand synchronises that stream before returning
+ *     (the decision is a host decision, Sec. 4.2); the other hot-path calls
+ *     are asynchronous.
+ *   - Allocation failures (GP_ERR_NO_PAGES, GP_ERR_NO_SLOTS) leave every
+ *     piece of state unchanged.
+ *   - A context is not thread-safe; use one per host thread.
+ *
+ * Layouts
+ *   K and V caches: [L][num_pages][Hkv][page_size][head_dim] of kv_dtype,
+ *     so one (layer, page, KV head) tile is page_size * head_dim contiguous
+ *     elements (64 KiB for bf16, d = 128, page_size = 256).
+ *   Query summaries (engine-owned, fp64): [L][max_slots][2][Hq][head_dim],
+ *     index 0 = short (beta_s), 1 = long (beta_l)  (App. E.1 Eq. 11).  fp64
+ *     because the long summary's 1 - beta_l = 0.001 increments and the
+ *     large logits of concentrated heads need more than fp32's 24 bits to
+ *     keep importance scores within 1e-5 relative.
+ *   Queries: [L][n][Hq][head_dim] of q_dtype, normalised and pre-RoPE.
+ *   Query head j belongs to KV head j / (Hq / Hkv).
+ *
+ * EMA convention (fixed here because the paper's pages disagree): the stored
+ * beta is the decay, the weight on the previous summary:
+ *   qbar <- beta * qbar + (1 - beta) * q,  beta_s = 0.9 < beta_l = 0.999.
+ */
+#ifndef GROWPAGE_H
+#define GROWPAGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GP_OK = 0,
+  GP_ERR_INVALID = 1,     /* bad argument; nothing changed */
+  GP_ERR_NO_PAGES = 2,    /* the free pool cannot supply the pages; nothing changed */
+  GP_ERR_NO_SLOTS = 3,    /* no free summary slot; nothing changed */
+  GP_ERR_CUDA = 4,        /* a CUDA runtime call failed (text in gp_last_error) */
+  GP_ERR_TIMEOUT = 5,     /* reserved: a bounded device-side wait gave up */
+  GP_ERR_STATE = 6,       /* call out of order (e.g. compress without a fresh demand) */
+  GP_ERR_UNSUPPORTED = 7  /* shape outside what the kernels were built for */
+} gp_status;
+
+typedef enum { GP_DTYPE_BF16 = 0, GP_DTYPE_F32 = 1 } gp_dtype;
+typedef enum { GP_POLICY_GROWPAGE = 0, GP_POLICY_FIXED = 1 } gp_policy;
+typedef enum { GP_ACT_GROW = 0, GP_ACT_COMPRESS = 1 } gp_action_kind;
+
+/* Engine configuration.  Defaults (gp_config_default) follow the paper:
+ * page_size 256, recent_window 16, k_loc 64, beta_s 0.9, beta_l 0.999,
+ * p 0.99, tau 0, max_slots 512 (Sec. 3.2, Sec. 5.1, App. D, App. E.1). */
+typedef struct gp_config {
+  int32_t num_layers;        /* L */
+  int32_t num_q_heads;       /* Hq */
+  int32_t num_kv_heads;      /* Hkv; Hq / Hkv in {1, 2, 4, 8} */
+  int32_t head_dim;          /* d: 64 or 128 */
+  int32_t page_size;         /* b: 256 (the only size the kernels support) */
+  int32_t kv_dtype;          /* gp_dtype of the K/V caches */
+  int32_t q_dtype;           /* gp_dtype of the query inputs */
+  int32_t max_slots;         /* M: rows of the summary pool */
+  int32_t num_pages;         /* physical pages in the K/V caches */
+  int32_t max_pages_per_req; /* block-table capacity; at most 256 */
+  int32_t recent_window;     /* R: always-kept recent tokens, 0 <= R < b */
+  int32_t k_loc;             /* Eq. 10 per-block quota */
+  int32_t reserve_pages;     /* Grow only while free pages > reserve (Sec. 4.2) */
+  int32_t policy;            /* gp_policy */
+  double beta_s;             /* short-summary decay */
+  double beta_l;             /* long-summary decay */
+  double p;                  /* coverage target of D_p, 0 < p < 1 */
+  double tau;                /* decision threshold on Delta */
+  double rope_theta;         /* rotate-half RoPE base */
+} gp_config;
+
+/* One request as the caller's scheduler sees it.  block_table is a HOST
+ * array owned by the caller, capacity max_pages_per_req, holding num_pages
+ * physical page ids in logical order.  gp_grow_page and gp_compress_hold
+ * rewrite it in place.  pos is the current decode position (tokens
+ * generated so far, evicted ones included); RoPE of the summaries uses it. */
+typedef struct gp_request {
+  int32_t slot;
+  int32_t num_pages;
+  int32_t* block_table;
+  int64_t pos;
+} gp_request;
+
+/* Result of the demand estimation for one request (Eqs. 7-8):
+ * sum_k_short = sum over (layer, KV head) of K^S, likewise sum_k_long;
+ * num_candidates = |C_t| = (P - 1) * b; num_units = L * Hkv;
+ * delta = (sum_k_short - sum_k_long) / (num_candidates * num_units). */
+typedef struct gp_demand {
+  int64_t sum_k_short;
+  int64_t sum_k_long;
+  int32_t num_candidates;
+  int32_t num_units;
+  double delta;
+} gp_demand;
+
+typedef struct gp_action {
+  int32_t kind;      /* gp_action_kind */
+  int32_t fallback;  /* 1: Delta asked for Grow but the pool could not grant it */
+  int32_t forced;    /* 1: P == 1, nothing to compress, Grow forced */
+} gp_action;
+
+typedef struct gp_stats_t {
+  int64_t demand_calls;
+  int64_t demand_requests;
+  int64_t grow;
+  int64_t compress;
+  int64_t fallback;
+  int64_t forced_grow;
+  int64_t cow_pages;       /* shared pages replaced by copy-on-write */
+  int64_t moved_rows;      /* (layer, head, token) rows moved by compaction */
+} gp_stats_t;
+
+typedef struct gp_ctx gp_ctx;
+
+/* ---- lifecycle --------------------------------------------------------- */
+
+/* Fill *cfg with the paper's defaults (shape fields zero). */
+gp_status gp_config_default(gp_config* cfg);
+
+/* Create an engine.  k_cache / v_cache: device base addresses of the caller's
+ * caches (layout above), which must stay alive and unmoved for the engine's
+ * lifetime.  stream: a cudaStream_t (NULL = legacy default stream).
+ * If k_cache and v_cache are both NULL the context is host-only: pages,
+ * refcounts, slots and decisions work, no CUDA call is made, and the device
+ * calls return GP_ERR_STATE.  On success *out owns the engine. */
+gp_status gp_create(const gp_config* cfg, void* k_cache, void* v_cache,
+                    void* stream, gp_ctx** out);
+gp_status gp_destroy(gp_ctx* ctx);
+const char* gp_last_error(const gp_ctx* ctx);
+const char* gp_status_string(gp_status st);
+
+/* ---- page pool with refcounts (Sec. 4.2, App. E.2) -----------------------
+ * Pages index the caller's caches.  Allocation is deterministic: the lowest
+ * free id.  gp_page_ref shares a page (prefix caching); gp_page_unref drops
+ * one reference and frees the page at zero; an unref of a free page is
+ * GP_ERR_INVALID. */
+gp_status gp_page_alloc(gp_ctx* ctx, int32_t* page);
+gp_status gp_page_ref(gp_ctx* ctx, int32_t page);
+gp_status gp_page_unref(gp_ctx* ctx, int32_t page);
+gp_status gp_page_refcount(const gp_ctx* ctx, int32_t page, int32_t* rc);
+gp_status gp_free_page_count(const gp_ctx* ctx, int32_t* n);
+
+/* ---- summary slots (App. E.1) --------------------------------------------
+ * A slot is bound to a running request; its first gp_update_summaries must
+ * pass first = 1, which overwrites stale values (no clearing needed). */
+gp_status gp_slot_acquire(gp_ctx* ctx, int32_t* slot);
+gp_status gp_slot_release(gp_ctx* ctx, int32_t slot);
+
+/* ---- hot path -------------------------------------------------------------
+ * gp_update_summaries: Sec. 3.2 Eq. 6 with the App. E.1 initialisation, for
+ * n requests of one decode step.  slots_dev: int32[n] device; q_dev:
+ * [L][n][Hq][d] q_dtype device; first_dev: uint8[n] device (1 = slot's first
+ * step).  Asynchronous.  Slot ids out of range are skipped and reported as
+ * GP_ERR_INVALID by the next synchronising call. */
+gp_status gp_update_summaries(gp_ctx* ctx, int32_t n, const int32_t* slots_dev,
+                              const void* q_dev, const uint8_t* first_dev);
+
+/* gp_boundary_demand: for n requests at a capacity boundary (each holding
+ * num_pages full pages), App. E.1 Eq. 12 calibration against q_cur, RoPE at
+ * pos, scores of both summaries against every key of the request through
+ * its block table, softmax over C_t = [0, (P-1) b) and D_p per (layer, KV
+ * head) (Eqs. 2 and 7), and Delta (Eq. 8).  q_cur_dev: [L][n][Hq][d] q_dtype
+ * device (the same q_t just passed to gp_update_summaries).  out: host
+ * gp_demand[n].  It also caches, per (layer, KV head), the importance
+ * max(a^S, a^L) of Eq. 9 over [0, P b - R) for a following
+ * gp_compress_hold.  Synchronises the stream. */
+gp_status gp_boundary_demand(gp_ctx* ctx, int32_t n, const gp_request* reqs,
+                             const void* q_cur_dev, gp_demand* out);
+
+/* gp_decide: Grow iff Delta > tau, else Compress & Hold (Sec. 3.2); P == 1
+ * forces Grow; a Grow that would leave the pool at or below reserve_pages
+ * (counting earlier grants of this call) becomes a fallback Compress
+ * (Sec. 4.2).  policy FIXED never grows except when forced.  Host only. */
+gp_status gp_decide(gp_ctx* ctx, int32_t n, const gp_request* reqs,
+                    const gp_demand* demand, gp_action* out);
+
+/* gp_grow_page: Grow by One Page -- take the lowest free page (refcount 1)
+ * and append it to req->block_table (num_pages + 1).  GP_ERR_NO_PAGES or a
+ * full block table leave the request unchanged.  Host only. */
+gp_status gp_grow_page(gp_ctx* ctx, gp_request* req);
+
+/* gp_compress_hold: Compress & Hold for n requests, each of which must have
+ * been passed to the last gp_boundary_demand with the same slot, pages and
+ * block table (else GP_ERR_STATE).  Per (layer, KV head): importance
+ * (Eq. 9), the recent R tokens always kept, block-local top-k_loc' with
+ * k_loc' = min(k_loc, |B_j|, floor(K_t / P)) plus global top-(K_t - |S_loc|)
+ * (Eq. 10, K_t = (P-1) b - R, equal scores: lower slot first), then stable
+ * compaction: the k-th kept slot moves to logical slot k.  Copy-on-write
+ * (App. E.2): every page with refcount > 1 is first replaced in the block
+ * table by a fresh page (lowest id first, ascending logical order) and the
+ * request's reference to the shared page is dropped after the copy.
+ * num_pages is unchanged; logical slots [(P-1) b, P b) become free.
+ * GP_ERR_NO_PAGES (not enough fresh pages for copy-on-write) changes
+ * nothing.  Asynchronous on the stream. */
+gp_status gp_compress_hold(gp_ctx* ctx, int32_t n, gp_request* reqs);
+
+/* gp_compact_kv: the compaction step of Compress & Hold for a caller-given
+ * index set (App. E.2), with the same copy-on-write handling.
+ * keep_masks_dev: device uint32, per request [L][Hkv][ceil(P b / 32)] bit
+ * masks (bit i%32 of word i/32 = keep slot i), requests concatenated in
+ * order; each (layer, KV head) must keep exactly (P-1) b slots (else the
+ * masks are rejected with GP_ERR_INVALID at the next synchronising call and
+ * that unit is not moved).  Asynchronous. */
+gp_status gp_compact_kv(gp_ctx* ctx, int32_t n, gp_request* reqs,
+                        const uint32_t* keep_masks_dev);
+
+/* ---- inspection (tests, benchmarks) ---------------------------------------
+ * All of these synchronise the stream.  req_idx indexes the request list of
+ * the last gp_boundary_demand (k, probabilities, scores) or of the last
+ * gp_compress_hold (keep masks). */
+
+/* K^S, K^L per unit: k_out host int32[L * Hkv * 2] ([unit][x]). */
+gp_status gp_debug_demand_k(gp_ctx* ctx, int32_t req_idx, int32_t* k_out);
+/* Importance log2 max(a^S, a^L) over [0, P b - R): host float[L*Hkv][P b - R]. */
+gp_status gp_debug_scores(gp_ctx* ctx, int32_t req_idx, float* out);
+/* Demand distributions a^S, a^L over C_t: host float[L*Hkv][2][(P-1) b].
+ * Only filled when gp_set_debug(ctx, GP_DEBUG_PROBS) was set before the
+ * demand call. */
+gp_status gp_debug_probs(gp_ctx* ctx, int32_t req_idx, float* out);
+/* Keep masks of the last gp_compress_hold: host uint32[L*Hkv][ceil(P b/32)]. */
+gp_status gp_debug_keep_mask(gp_ctx* ctx, int32_t req_idx, uint32_t* out);
+/* Summaries of one slot: host double[L][2][Hq][d]. */
+gp_status gp_read_summaries(gp_ctx* ctx, int32_t slot, double* out);
+
+#define GP_DEBUG_PROBS 1
+gp_status gp_set_debug(gp_ctx* ctx, int32_t flags);
+
+/* Per-kernel device time: when enabled, every kernel launch is bracketed by
+ * CUDA events on the engine stream.  names: GP_KERNEL_* below.  The query
+ * synchronises and returns the summed milliseconds and launch count since
+ * the last reset. */
+#define GP_KERNEL_EMA 0
+#define GP_KERNEL_PREP 1
+#define GP_KERNEL_DEMAND 2
+#define GP_KERNEL_COMPRESS 3
+#define GP_KERNEL_COUNT 4
+gp_status gp_set_timing(gp_ctx* ctx, int32_t enabled);
+gp_status gp_kernel_time(gp_ctx* ctx, int32_t kernel, double* ms, int64_t* launches);
+gp_status gp_reset_timing(gp_ctx* ctx);
+
+gp_status gp_stats(const gp_ctx* ctx, gp_stats_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GROWPAGE_H */

@@ -1,0 +1,369 @@
+"""Thin ctypes binding of the C ABI in include/growpage.h.
+
+Argument marshalling only: every step of the hot path runs in the sm_103a
+kernels of libgrowpage.so.  There is no fallback: if the library is missing
+and cannot be built, ``load()`` raises.
+
+Module-level functions carry the C names (``gp_create``, ``gp_boundary_demand``
+...), take a context as first argument and raise ``GrowPageError`` on a
+non-OK status.  Tensors are passed by device pointer; PyTorch only provides
+device memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import _build_lib
+
+GP_OK, GP_ERR_INVALID, GP_ERR_NO_PAGES, GP_ERR_NO_SLOTS = 0, 1, 2, 3
+GP_ERR_CUDA, GP_ERR_TIMEOUT, GP_ERR_STATE, GP_ERR_UNSUPPORTED = 4, 5, 6, 7
+GP_DTYPE_BF16, GP_DTYPE_F32 = 0, 1
+GP_POLICY_GROWPAGE, GP_POLICY_FIXED = 0, 1
+GP_ACT_GROW, GP_ACT_COMPRESS = 0, 1
+GP_DEBUG_PROBS = 1
+GP_KERNEL_EMA, GP_KERNEL_PREP, GP_KERNEL_DEMAND, GP_KERNEL_COMPRESS = 0, 1, 2, 3
+KERNEL_NAMES = {0: "ema_update", 1: "prep_queries", 2: "boundary_demand", 3: "compress_hold"}
+
+EXPORTS = [
+    "gp_config_default", "gp_create", "gp_destroy", "gp_last_error", "gp_status_string",
+    "gp_page_alloc", "gp_page_ref", "gp_page_unref", "gp_page_refcount", "gp_free_page_count",
+    "gp_slot_acquire", "gp_slot_release", "gp_update_summaries", "gp_boundary_demand",
+    "gp_decide", "gp_grow_page", "gp_compress_hold", "gp_compact_kv", "gp_debug_demand_k",
+    "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
+    "gp_set_debug", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
+]
+
+
+class GpConfig(C.Structure):
+    _fields_ = [
+        ("num_layers", C.c_int32), ("num_q_heads", C.c_int32), ("num_kv_heads", C.c_int32),
+        ("head_dim", C.c_int32), ("page_size", C.c_int32), ("kv_dtype", C.c_int32),
+        ("q_dtype", C.c_int32), ("max_slots", C.c_int32), ("num_pages", C.c_int32),
+        ("max_pages_per_req", C.c_int32), ("recent_window", C.c_int32), ("k_loc", C.c_int32),
+        ("reserve_pages", C.c_int32), ("policy", C.c_int32),
+        ("beta_s", C.c_double), ("beta_l", C.c_double), ("p", C.c_double), ("tau", C.c_double),
+        ("rope_theta", C.c_double),
+    ]
+
+
+class GpRequest(C.Structure):
+    _fields_ = [("slot", C.c_int32), ("num_pages", C.c_int32),
+                ("block_table", C.POINTER(C.c_int32)), ("pos", C.c_int64)]
+
+
+class GpDemand(C.Structure):
+    _fields_ = [("sum_k_short", C.c_int64), ("sum_k_long", C.c_int64),
+                ("num_candidates", C.c_int32), ("num_units", C.c_int32), ("delta", C.c_double)]
+
+
+class GpAction(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("fallback", C.c_int32), ("forced", C.c_int32)]
+
+
+class GpStats(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("demand_calls", "demand_requests", "grow", "compress",
+                                          "fallback", "forced_grow", "cow_pages", "moved_rows")]
+
+
+class GrowPageError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[{status}] {message}")
+        self.status = status
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build_lib.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libgrowpage.so (building it in-tree with nvcc if absent)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build_lib.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"native library {path} is missing; run __graft_entry__.build()")
+        _build_lib.build()
+    lib = C.CDLL(path)
+    P, I32, I64 = C.c_void_p, C.c_int32, C.c_int64
+    PI32 = C.POINTER(C.c_int32)
+    sig = {
+        "gp_config_default": (I32, [C.POINTER(GpConfig)]),
+        "gp_create": (I32, [C.POINTER(GpConfig), P, P, P, C.POINTER(P)]),
+        "gp_destroy": (I32, [P]),
+        "gp_last_error": (C.c_char_p, [P]),
+        "gp_status_string": (C.c_char_p, [I32]),
+        "gp_page_alloc": (I32, [P, PI32]),
+        "gp_page_ref": (I32, [P, I32]),
+        "gp_page_unref": (I32, [P, I32]),
+        "gp_page_refcount": (I32, [P, I32, PI32]),
+        "gp_free_page_count": (I32, [P, PI32]),
+        "gp_slot_acquire": (I32, [P, PI32]),
+        "gp_slot_release": (I32, [P, I32]),
+        "gp_update_summaries": (I32, [P, I32, P, P, P]),
+        "gp_boundary_demand": (I32, [P, I32, C.POINTER(GpRequest), P, C.POINTER(GpDemand)]),
+        "gp_decide": (I32, [P, I32, C.POINTER(GpRequest), C.POINTER(GpDemand), C.POINTER(GpAction)]),
+        "gp_grow_page": (I32, [P, C.POINTER(GpRequest)]),
+        "gp_compress_hold": (I32, [P, I32, C.POINTER(GpRequest)]),
+        "gp_compact_kv": (I32, [P, I32, C.POINTER(GpRequest), P]),
+        "gp_debug_demand_k": (I32, [P, I32, P]),
+        "gp_debug_scores": (I32, [P, I32, P]),
+        "gp_debug_probs": (I32, [P, I32, P]),
+        "gp_debug_keep_mask": (I32, [P, I32, P]),
+        "gp_read_summaries": (I32, [P, I32, P]),
+        "gp_set_debug": (I32, [P, I32]),
+        "gp_set_timing": (I32, [P, I32]),
+        "gp_kernel_time": (I32, [P, I32, C.POINTER(C.c_double), C.POINTER(I64)]),
+        "gp_reset_timing": (I32, [P]),
+        "gp_stats": (I32, [P, C.POINTER(GpStats)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(ctx, st: int):
+    if st != GP_OK:
+        lib = load()
+        msg = lib.gp_last_error(ctx).decode() if ctx else lib.gp_status_string(st).decode()
+        raise GrowPageError(st, msg or lib.gp_status_string(st).decode())
+
+
+def _ptr(t) -> int:
+    """Device (or host) address of a tensor / numpy array, or 0."""
+    if t is None:
+        return 0
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return int(t)
+
+
+# ---------------------------------------------------------------------------
+# requests
+# ---------------------------------------------------------------------------
+
+class Request:
+    """A request as the scheduler holds it: slot, block table (host), position."""
+
+    def __init__(self, slot: int, pages, pos: int, capacity: int):
+        self.slot = int(slot)
+        self.table = np.zeros(capacity, dtype=np.int32)
+        pages = list(pages)
+        self.table[:len(pages)] = pages
+        self.num_pages = len(pages)
+        self.pos = int(pos)
+
+    @property
+    def pages(self):
+        return self.table[:self.num_pages].tolist()
+
+
+def _marshal(reqs):
+    arr = (GpRequest * max(1, len(reqs)))()
+    for i, r in enumerate(reqs):
+        arr[i].slot = r.slot
+        arr[i].num_pages = r.num_pages
+        arr[i].block_table = r.table.ctypes.data_as(C.POINTER(C.c_int32))
+        arr[i].pos = r.pos
+    return arr
+
+
+def _unmarshal(arr, reqs):
+    for i, r in enumerate(reqs):
+        r.num_pages = arr[i].num_pages
+
+
+# ---------------------------------------------------------------------------
+# C-named wrappers
+# ---------------------------------------------------------------------------
+
+def gp_config_default(**overrides) -> GpConfig:
+    cfg = GpConfig()
+    _check(None, load().gp_config_default(C.byref(cfg)))
+    for k, v in overrides.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+def gp_create(cfg: GpConfig, k_cache=None, v_cache=None, stream=None):
+    ctx = C.c_void_p()
+    s = 0 if stream is None else (stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    st = load().gp_create(C.byref(cfg), _ptr(k_cache) or None, _ptr(v_cache) or None, s or None, C.byref(ctx))
+    _check(None, st)
+    return ctx
+
+
+def gp_destroy(ctx):
+    _check(None, load().gp_destroy(ctx))
+
+
+def gp_page_alloc(ctx) -> int:
+    p = C.c_int32()
+    _check(ctx, load().gp_page_alloc(ctx, C.byref(p)))
+    return p.value
+
+
+def gp_page_ref(ctx, page: int):
+    _check(ctx, load().gp_page_ref(ctx, page))
+
+
+def gp_page_unref(ctx, page: int):
+    _check(ctx, load().gp_page_unref(ctx, page))
+
+
+def gp_page_refcount(ctx, page: int) -> int:
+    rc = C.c_int32()
+    _check(ctx, load().gp_page_refcount(ctx, page, C.byref(rc)))
+    return rc.value
+
+
+def gp_free_page_count(ctx) -> int:
+    n = C.c_int32()
+    _check(ctx, load().gp_free_page_count(ctx, C.byref(n)))
+    return n.value
+
+
+def gp_slot_acquire(ctx) -> int:
+    s = C.c_int32()
+    _check(ctx, load().gp_slot_acquire(ctx, C.byref(s)))
+    return s.value
+
+
+def gp_slot_release(ctx, slot: int):
+    _check(ctx, load().gp_slot_release(ctx, slot))
+
+
+def gp_update_summaries(ctx, n: int, slots_dev, q_dev, first_dev):
+    _check(ctx, load().gp_update_summaries(ctx, n, _ptr(slots_dev), _ptr(q_dev), _ptr(first_dev)))
+
+
+def gp_boundary_demand(ctx, reqs, q_cur_dev):
+    arr = _marshal(reqs)
+    out = (GpDemand * max(1, len(reqs)))()
+    _check(ctx, load().gp_boundary_demand(ctx, len(reqs), arr, _ptr(q_cur_dev), out))
+    return [out[i] for i in range(len(reqs))]
+
+
+def gp_decide(ctx, reqs, demand):
+    arr = _marshal(reqs)
+    dem = (GpDemand * max(1, len(reqs)))(*demand)
+    out = (GpAction * max(1, len(reqs)))()
+    _check(ctx, load().gp_decide(ctx, len(reqs), arr, dem, out))
+    return [out[i] for i in range(len(reqs))]
+
+
+def gp_grow_page(ctx, req: Request):
+    if req.num_pages >= len(req.table):
+        raise GrowPageError(GP_ERR_INVALID, "block table is full (Python capacity)")
+    arr = _marshal([req])
+    st = load().gp_grow_page(ctx, arr)
+    _unmarshal(arr, [req])
+    _check(ctx, st)
+
+
+def gp_compress_hold(ctx, reqs):
+    arr = _marshal(reqs)
+    st = load().gp_compress_hold(ctx, len(reqs), arr)
+    _unmarshal(arr, reqs)
+    _check(ctx, st)
+
+
+def gp_compact_kv(ctx, reqs, keep_masks_dev):
+    arr = _marshal(reqs)
+    st = load().gp_compact_kv(ctx, len(reqs), arr, _ptr(keep_masks_dev))
+    _unmarshal(arr, reqs)
+    _check(ctx, st)
+
+
+def gp_debug_demand_k(ctx, req_idx: int, units: int) -> np.ndarray:
+    out = np.zeros((units, 2), dtype=np.int32)
+    _check(ctx, load().gp_debug_demand_k(ctx, req_idx, out.ctypes.data))
+    return out
+
+
+def gp_debug_scores(ctx, req_idx: int, units: int, ncmp: int) -> np.ndarray:
+    out = np.zeros((units, ncmp), dtype=np.float32)
+    _check(ctx, load().gp_debug_scores(ctx, req_idx, out.ctypes.data))
+    return out
+
+
+def gp_debug_probs(ctx, req_idx: int, units: int, ndem: int) -> np.ndarray:
+    out = np.zeros((units, 2, ndem), dtype=np.float32)
+    _check(ctx, load().gp_debug_probs(ctx, req_idx, out.ctypes.data))
+    return out
+
+
+def gp_debug_keep_mask(ctx, req_idx: int, units: int, num_pages: int, page_size: int = 256) -> np.ndarray:
+    out = np.zeros((units, num_pages * page_size // 32), dtype=np.uint32)
+    _check(ctx, load().gp_debug_keep_mask(ctx, req_idx, out.ctypes.data))
+    return out
+
+
+def gp_read_summaries(ctx, slot: int, L: int, hq: int, d: int) -> np.ndarray:
+    out = np.zeros((L, 2, hq, d), dtype=np.float64)
+    _check(ctx, load().gp_read_summaries(ctx, slot, out.ctypes.data))
+    return out
+
+
+def gp_set_debug(ctx, flags: int):
+    _check(ctx, load().gp_set_debug(ctx, flags))
+
+
+def gp_set_timing(ctx, enabled: bool):
+    _check(ctx, load().gp_set_timing(ctx, int(bool(enabled))))
+
+
+def gp_kernel_time(ctx, kernel: int):
+    ms, n = C.c_double(), C.c_int64()
+    _check(ctx, load().gp_kernel_time(ctx, kernel, C.byref(ms), C.byref(n)))
+    return ms.value, n.value
+
+
+def gp_reset_timing(ctx):
+    _check(ctx, load().gp_reset_timing(ctx))
+
+
+def gp_stats(ctx) -> dict:
+    s = GpStats()
+    _check(ctx, load().gp_stats(ctx, C.byref(s)))
+    return {n: getattr(s, n) for n, _ in GpStats._fields_}
+
+
+@dataclass
+class Shape:
+    num_layers: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+
+    @property
+    def units(self) -> int:
+        return self.num_layers * self.num_kv_heads
+
+
+def unpack_mask(words: np.ndarray, n: int) -> np.ndarray:
+    """uint32 keep-mask words -> bool[..., n] (bit i%32 of word i/32)."""
+    w = np.asarray(words, dtype=np.uint32)
+    bits = ((w[..., :, None] >> np.arange(32, dtype=np.uint32)) & 1).astype(bool)
+    return bits.reshape(*w.shape[:-1], -1)[..., :n]
+
+
+def pack_mask(keep: np.ndarray) -> np.ndarray:
+    """bool[..., n] (n a multiple of 32) -> uint32 words."""
+    k = np.asarray(keep, dtype=bool)
+    k = k.reshape(*k.shape[:-1], -1, 32).astype(np.uint32)
+    return (k << np.arange(32, dtype=np.uint32)).sum(axis=-1).astype(np.uint32)

@@ -1,0 +1,920 @@
+// Host side of the GrowPage capacity-boundary engine: the C ABI declared in
+// include/growpage.h.  Owns the page pool (refcounts, lowest-id-first free
+// set), the summary slots, the device scratch and the orchestration of the
+// sm_103a kernels.  Every device step runs in the kernels; this file only
+// validates, plans, uploads descriptors and reads back results.
+#include "growpage.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <set>
+#include <string>
+#include <unordered_set>
+#include <vector>
+
+#include "gp_kernels.h"
+
+namespace {
+
+constexpr int kPage = 256;
+constexpr int kMaxPagesPerReq = 256;
+
+struct DevBuf {
+  void* p = nullptr;
+  size_t cap = 0;
+};
+
+struct DemandRec {
+  int32_t slot = -1;
+  int32_t num_pages = 0;
+  std::vector<int32_t> pages;
+  uint64_t gen = 0;
+  int64_t score_off = 0;
+  int64_t dbg_off = -1;
+};
+
+struct CompressRec {
+  int32_t num_pages = 0;
+  int64_t mask_off = 0;
+};
+
+struct TimedEvent {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+
+}  // namespace
+
+struct gp_ctx {
+  gp_config cfg{};
+  bool host_only = true;
+  void* k_cache = nullptr;
+  void* v_cache = nullptr;
+  cudaStream_t stream = nullptr;
+  std::string err;
+
+  // page pool (Sec. 4.2, App. E.2)
+  std::vector<int32_t> refcnt;
+  std::set<int32_t> free_pages;
+  // summary slots (App. E.1)
+  std::vector<uint8_t> slot_bound;
+  std::vector<uint64_t> slot_gen;
+  std::set<int32_t> free_slots;
+
+  // device state
+  double* pool = nullptr;          // [L][M][2][Hq][D]
+  int* err_dev = nullptr;          // kernel error bits
+  unsigned long long* moved_dev = nullptr;
+  DevBuf upload, bt2, qt, scores, kout, ksum, dbg, masks;
+  void* pinned = nullptr;
+  size_t pinned_cap = 0;
+  cudaEvent_t pinned_free = nullptr;  // recorded after the last async use of `pinned`
+
+  std::vector<DemandRec> last_demand;
+  std::vector<CompressRec> last_compress;
+  int64_t last_dbg_total = 0;
+
+  gp_stats_t stats{};
+  int debug = 0;
+  bool timing = false;
+  std::vector<TimedEvent> timed;
+  std::vector<cudaEvent_t> event_pool;
+  double t_ms[GP_KERNEL_COUNT] = {};
+  int64_t t_count[GP_KERNEL_COUNT] = {};
+};
+
+namespace {
+
+gp_status fail(gp_ctx* c, gp_status st, const char* fmt, ...) {
+  if (c) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    c->err = buf;
+  }
+  return st;
+}
+
+#define GP_CUDA(ctx, call)                                                              \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail((ctx), GP_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+int elt_bytes(int dtype) { return dtype == GP_DTYPE_F32 ? 4 : 2; }
+
+gp_status ensure(gp_ctx* c, DevBuf& b, size_t bytes) {
+  if (bytes <= b.cap) return GP_OK;
+  size_t cap = std::max(bytes, b.cap + b.cap / 2);
+  cap = (cap + 255) & ~size_t(255);
+  if (b.p) GP_CUDA(c, cudaFree(b.p));
+  b.p = nullptr;
+  b.cap = 0;
+  GP_CUDA(c, cudaMalloc(&b.p, cap));
+  b.cap = cap;
+  return GP_OK;
+}
+
+gp_status ensure_pinned(gp_ctx* c, size_t bytes) {
+  if (c->pinned_free) GP_CUDA(c, cudaEventSynchronize(c->pinned_free));
+  if (bytes <= c->pinned_cap) return GP_OK;
+  size_t cap = std::max(bytes, c->pinned_cap * 2);
+  cap = (cap + 4095) & ~size_t(4095);
+  if (c->pinned) GP_CUDA(c, cudaFreeHost(c->pinned));
+  c->pinned = nullptr;
+  c->pinned_cap = 0;
+  GP_CUDA(c, cudaHostAlloc(&c->pinned, cap, cudaHostAllocDefault));
+  c->pinned_cap = cap;
+  return GP_OK;
+}
+
+cudaEvent_t take_event(gp_ctx* c) {
+  if (!c->event_pool.empty()) {
+    cudaEvent_t e = c->event_pool.back();
+    c->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Launch wrapper: brackets the launch with events when timing is on.
+template <typename F>
+gp_status timed_launch(gp_ctx* c, int kernel, const char* name, F&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (c->timing) {
+    a = take_event(c);
+    b = take_event(c);
+    cudaEventRecord(a, c->stream);
+  }
+  cudaError_t e = launch();
+  if (e != cudaSuccess) return fail(c, GP_ERR_CUDA, "%s launch failed: %s", name, cudaGetErrorString(e));
+  if (c->timing) {
+    cudaEventRecord(b, c->stream);
+    c->timed.push_back({kernel, a, b});
+  }
+  return GP_OK;
+}
+
+gp_status need_device(gp_ctx* c) {
+  if (!c) return GP_ERR_INVALID;
+  if (c->host_only) return fail(c, GP_ERR_STATE, "host-only context has no device caches");
+  return GP_OK;
+}
+
+// Read and clear the kernels' error word (synchronises the stream).
+gp_status check_kernel_errors(gp_ctx* c) {
+  int e = 0;
+  GP_CUDA(c, cudaMemcpyAsync(&e, c->err_dev, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+  GP_CUDA(c, cudaStreamSynchronize(c->stream));
+  if (e) {
+    GP_CUDA(c, cudaMemsetAsync(c->err_dev, 0, sizeof(int), c->stream));
+    return fail(c, GP_ERR_INVALID,
+                "device-side check failed (bits 0x%x: 1 slot, 2 page, 4 keep mask count, 8 selection)", e);
+  }
+  return GP_OK;
+}
+
+gp_status validate_request(gp_ctx* c, const gp_request& r, int idx, bool need_slot) {
+  const gp_config& g = c->cfg;
+  if (need_slot && (r.slot < 0 || r.slot >= g.max_slots || !c->slot_bound[r.slot]))
+    return fail(c, GP_ERR_INVALID, "request %d: slot %d is not bound", idx, r.slot);
+  if (r.num_pages < 1 || r.num_pages > g.max_pages_per_req)
+    return fail(c, GP_ERR_INVALID, "request %d: num_pages %d outside [1, %d]", idx, r.num_pages,
+                g.max_pages_per_req);
+  if (!r.block_table) return fail(c, GP_ERR_INVALID, "request %d: null block table", idx);
+  if (r.pos < 0) return fail(c, GP_ERR_INVALID, "request %d: negative position", idx);
+  std::unordered_set<int32_t> seen;
+  for (int j = 0; j < r.num_pages; ++j) {
+    const int32_t pg = r.block_table[j];
+    if (pg < 0 || pg >= g.num_pages || c->refcnt[pg] <= 0)
+      return fail(c, GP_ERR_INVALID, "request %d: block %d holds page %d that is not allocated", idx, j, pg);
+    if (!seen.insert(pg).second)
+      return fail(c, GP_ERR_INVALID, "request %d: page %d appears twice in the block table", idx, pg);
+  }
+  return GP_OK;
+}
+
+int units_of(const gp_ctx* c) { return c->cfg.num_layers * c->cfg.num_kv_heads; }
+
+}  // namespace
+
+// The C linkage of every gp_* definition below comes from its declaration
+// in growpage.h.
+
+const char* gp_status_string(gp_status st) {
+  switch (st) {
+    case GP_OK: return "ok";
+    case GP_ERR_INVALID: return "invalid argument";
+    case GP_ERR_NO_PAGES: return "no free pages";
+    case GP_ERR_NO_SLOTS: return "no free slots";
+    case GP_ERR_CUDA: return "CUDA error";
+    case GP_ERR_TIMEOUT: return "device wait timed out";
+    case GP_ERR_STATE: return "invalid state";
+    case GP_ERR_UNSUPPORTED: return "unsupported shape";
+  }
+  return "unknown status";
+}
+
+gp_status gp_config_default(gp_config* cfg) {
+  if (!cfg) return GP_ERR_INVALID;
+  std::memset(cfg, 0, sizeof(*cfg));
+  cfg->page_size = kPage;
+  cfg->kv_dtype = GP_DTYPE_BF16;
+  cfg->q_dtype = GP_DTYPE_BF16;
+  cfg->max_slots = 512;
+  cfg->max_pages_per_req = 128;
+  cfg->recent_window = 16;
+  cfg->k_loc = 64;
+  cfg->reserve_pages = 0;
+  cfg->policy = GP_POLICY_GROWPAGE;
+  cfg->beta_s = 0.9;
+  cfg->beta_l = 0.999;
+  cfg->p = 0.99;
+  cfg->tau = 0.0;
+  cfg->rope_theta = 10000.0;
+  return GP_OK;
+}
+
+gp_status gp_create(const gp_config* cfg, void* k_cache, void* v_cache, void* stream, gp_ctx** out) {
+  if (!cfg || !out) return GP_ERR_INVALID;
+  *out = nullptr;
+  const gp_config& g = *cfg;
+  if (g.num_layers < 1 || g.num_q_heads < 1 || g.num_kv_heads < 1 || g.num_q_heads % g.num_kv_heads)
+    return GP_ERR_INVALID;
+  if (g.page_size != kPage) return GP_ERR_UNSUPPORTED;
+  if (g.head_dim != 64 && g.head_dim != 128) return GP_ERR_UNSUPPORTED;
+  const int G = g.num_q_heads / g.num_kv_heads;
+  if (G != 2 && G != 4) return GP_ERR_UNSUPPORTED;
+  if ((g.kv_dtype != GP_DTYPE_BF16 && g.kv_dtype != GP_DTYPE_F32) ||
+      (g.q_dtype != GP_DTYPE_BF16 && g.q_dtype != GP_DTYPE_F32))
+    return GP_ERR_INVALID;
+  if (g.max_slots < 1 || g.num_pages < 1 || g.max_pages_per_req < 1) return GP_ERR_INVALID;
+  if (g.max_pages_per_req > kMaxPagesPerReq) return GP_ERR_UNSUPPORTED;
+  if (g.recent_window < 0 || g.recent_window >= kPage || g.k_loc < 0 || g.reserve_pages < 0)
+    return GP_ERR_INVALID;
+  if (g.policy != GP_POLICY_GROWPAGE && g.policy != GP_POLICY_FIXED) return GP_ERR_INVALID;
+  if (!(g.p > 0.0 && g.p < 1.0) || !(g.beta_s >= 0.0 && g.beta_s < 1.0) ||
+      !(g.beta_l >= 0.0 && g.beta_l < 1.0) || !(g.rope_theta > 0.0) || !std::isfinite(g.tau))
+    return GP_ERR_INVALID;
+  if ((k_cache == nullptr) != (v_cache == nullptr)) return GP_ERR_INVALID;
+
+  gp_ctx* c = new gp_ctx();
+  c->cfg = g;
+  c->host_only = (k_cache == nullptr);
+  c->k_cache = k_cache;
+  c->v_cache = v_cache;
+  c->stream = static_cast<cudaStream_t>(stream);
+  c->refcnt.assign(g.num_pages, 0);
+  for (int i = 0; i < g.num_pages; ++i) c->free_pages.insert(i);
+  c->slot_bound.assign(g.max_slots, 0);
+  c->slot_gen.assign(g.max_slots, 0);
+  for (int i = 0; i < g.max_slots; ++i) c->free_slots.insert(i);
+  if (!c->host_only) {
+    const size_t pool_bytes =
+        sizeof(double) * (size_t)g.num_layers * g.max_slots * 2 * g.num_q_heads * g.head_dim;
+    cudaError_t e = cudaMalloc((void**)&c->pool, pool_bytes);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->pool, 0, pool_bytes, c->stream);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&c->err_dev, 64);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->err_dev, 0, 64, c->stream);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pinned_free, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) {
+      gp_destroy(c);
+      return GP_ERR_CUDA;
+    }
+    c->moved_dev = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(c->err_dev) + 8);
+  }
+  *out = c;
+  return GP_OK;
+}
+
+gp_status gp_destroy(gp_ctx* c) {
+  if (!c) return GP_ERR_INVALID;
+  if (!c->host_only) {
+    cudaStreamSynchronize(c->stream);
+    for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->scores, &c->kout, &c->ksum, &c->dbg, &c->masks})
+      if (b->p) cudaFree(b->p);
+    if (c->pool) cudaFree(c->pool);
+    if (c->err_dev) cudaFree(c->err_dev);
+    if (c->pinned) cudaFreeHost(c->pinned);
+    if (c->pinned_free) cudaEventDestroy(c->pinned_free);
+    for (auto& t : c->timed) {
+      cudaEventDestroy(t.start);
+      cudaEventDestroy(t.stop);
+    }
+    for (auto e : c->event_pool) cudaEventDestroy(e);
+  }
+  delete c;
+  return GP_OK;
+}
+
+const char* gp_last_error(const gp_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+// ---- page pool ----------------------------------------------------------------
+
+gp_status gp_page_alloc(gp_ctx* c, int32_t* page) {
+  if (!c || !page) return GP_ERR_INVALID;
+  if (c->free_pages.empty()) return fail(c, GP_ERR_NO_PAGES, "no free pages");
+  const int32_t p = *c->free_pages.begin();
+  c->free_pages.erase(c->free_pages.begin());
+  c->refcnt[p] = 1;
+  *page = p;
+  return GP_OK;
+}
+
+gp_status gp_page_ref(gp_ctx* c, int32_t page) {
+  if (!c) return GP_ERR_INVALID;
+  if (page < 0 || page >= c->cfg.num_pages || c->refcnt[page] <= 0)
+    return fail(c, GP_ERR_INVALID, "ref of page %d that is not allocated", page);
+  ++c->refcnt[page];
+  return GP_OK;
+}
+
+gp_status gp_page_unref(gp_ctx* c, int32_t page) {
+  if (!c) return GP_ERR_INVALID;
+  if (page < 0 || page >= c->cfg.num_pages || c->refcnt[page] <= 0)
+    return fail(c, GP_ERR_INVALID, "unref of page %d that is not allocated", page);
+  if (--c->refcnt[page] == 0) c->free_pages.insert(page);
+  return GP_OK;
+}
+
+gp_status gp_page_refcount(const gp_ctx* c, int32_t page, int32_t* rc) {
+  if (!c || !rc || page < 0 || page >= c->cfg.num_pages) return GP_ERR_INVALID;
+  *rc = c->refcnt[page];
+  return GP_OK;
+}
+
+gp_status gp_free_page_count(const gp_ctx* c, int32_t* n) {
+  if (!c || !n) return GP_ERR_INVALID;
+  *n = (int32_t)c->free_pages.size();
+  return GP_OK;
+}
+
+// ---- slots --------------------------------------------------------------------
+
+gp_status gp_slot_acquire(gp_ctx* c, int32_t* slot) {
+  if (!c || !slot) return GP_ERR_INVALID;
+  if (c->free_slots.empty()) return fail(c, GP_ERR_NO_SLOTS, "no free summary slots");
+  const int32_t s = *c->free_slots.begin();
+  c->free_slots.erase(c->free_slots.begin());
+  c->slot_bound[s] = 1;
+  ++c->slot_gen[s];
+  *slot = s;
+  return GP_OK;
+}
+
+gp_status gp_slot_release(gp_ctx* c, int32_t slot) {
+  if (!c) return GP_ERR_INVALID;
+  if (slot < 0 || slot >= c->cfg.max_slots || !c->slot_bound[slot])
+    return fail(c, GP_ERR_INVALID, "release of slot %d that is not bound", slot);
+  c->slot_bound[slot] = 0;
+  ++c->slot_gen[slot];
+  c->free_slots.insert(slot);
+  return GP_OK;
+}
+
+// ---- hot path ---------------------------------------------------------------
+
+gp_status gp_update_summaries(gp_ctx* c, int32_t n, const int32_t* slots_dev, const void* q_dev,
+                              const uint8_t* first_dev) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if (n < 0 || n > c->cfg.max_slots) return fail(c, GP_ERR_INVALID, "n = %d outside [0, max_slots]", n);
+  if (n == 0) return GP_OK;
+  if (!slots_dev || !q_dev || !first_dev) return fail(c, GP_ERR_INVALID, "null device pointer");
+  const gp_config& g = c->cfg;
+  gp::EmaArgs a{};
+  a.pool = c->pool;
+  a.q = q_dev;
+  a.q_f32 = g.q_dtype == GP_DTYPE_F32;
+  a.slots = slots_dev;
+  a.first = first_dev;
+  a.n = n;
+  a.L = g.num_layers;
+  a.Hq = g.num_q_heads;
+  a.D = g.head_dim;
+  a.M = g.max_slots;
+  a.beta_s = g.beta_s;
+  a.beta_l = g.beta_l;
+  a.err = c->err_dev;
+  return timed_launch(c, GP_KERNEL_EMA, "ema_update", [&] { return gp::launch_ema(a, c->stream); });
+}
+
+namespace {
+
+struct Staged {
+  gp::DevReq* reqs;
+  int32_t* bt;
+  int32_t* bt_new;
+  int32_t* work;
+  size_t bytes;
+  size_t off_bt, off_bt_new, off_work;
+};
+
+// Pinned layout [DevReq n][bt n*maxP][bt_new n*maxP][work n], mirrored in `upload`.
+gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s) {
+  const int maxp = c->cfg.max_pages_per_req;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o += (bytes + 255) & ~size_t(255); return r; };
+  const size_t off_req = take(sizeof(gp::DevReq) * n);
+  s->off_bt = take(sizeof(int32_t) * (size_t)n * maxp);
+  s->off_bt_new = with_new ? take(sizeof(int32_t) * (size_t)n * maxp) : s->off_bt;
+  s->off_work = take(sizeof(int32_t) * n);
+  s->bytes = o;
+  gp_status st = ensure_pinned(c, o);
+  if (st != GP_OK) return st;
+  st = ensure(c, c->upload, o);
+  if (st != GP_OK) return st;
+  char* p = static_cast<char*>(c->pinned);
+  s->reqs = reinterpret_cast<gp::DevReq*>(p + off_req);
+  s->bt = reinterpret_cast<int32_t*>(p + s->off_bt);
+  s->bt_new = reinterpret_cast<int32_t*>(p + s->off_bt_new);
+  s->work = reinterpret_cast<int32_t*>(p + s->off_work);
+  return GP_OK;
+}
+
+gp_status upload(gp_ctx* c, const Staged& s) {
+  GP_CUDA(c, cudaMemcpyAsync(c->upload.p, c->pinned, s.bytes, cudaMemcpyHostToDevice, c->stream));
+  GP_CUDA(c, cudaEventRecord(c->pinned_free, c->stream));
+  return GP_OK;
+}
+
+template <typename T>
+T* dev_at(const gp_ctx* c, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(c->upload.p) + off);
+}
+
+}  // namespace
+
+gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const void* q_cur_dev,
+                             gp_demand* out) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if (n < 0 || n > c->cfg.max_slots) return fail(c, GP_ERR_INVALID, "n = %d outside [0, max_slots]", n);
+  if (n == 0) return GP_OK;
+  if (!reqs || !out || !q_cur_dev) return fail(c, GP_ERR_INVALID, "null argument");
+  const gp_config& g = c->cfg;
+  std::unordered_set<int32_t> slots;
+  for (int r = 0; r < n; ++r) {
+    st = validate_request(c, reqs[r], r, true);
+    if (st != GP_OK) return st;
+    if (!slots.insert(reqs[r].slot).second)
+      return fail(c, GP_ERR_INVALID, "slot %d appears twice in one call", reqs[r].slot);
+  }
+  const int units = units_of(c);
+  const int G = g.num_q_heads / g.num_kv_heads;
+  const int rows = 2 * G;
+  const int maxp = g.max_pages_per_req;
+
+  // offsets of the importance cache and debug buffers
+  std::vector<int64_t> score_off(n), dbg_off(n, -1);
+  int64_t score_total = 0, dbg_total = 0;
+  for (int r = 0; r < n; ++r) {
+    const int P = reqs[r].num_pages;
+    score_off[r] = score_total;
+    score_total += (int64_t)units * (P * kPage - g.recent_window);
+    if (c->debug & GP_DEBUG_PROBS) {
+      dbg_off[r] = dbg_total;
+      dbg_total += (int64_t)units * 2 * (P - 1) * kPage;
+    }
+  }
+  Staged s{};
+  st = stage(c, n, false, &s);
+  if (st != GP_OK) return st;
+  if ((st = ensure(c, c->qt, sizeof(float) * (size_t)n * units * rows * g.head_dim)) != GP_OK) return st;
+  if ((st = ensure(c, c->scores, sizeof(float) * (size_t)std::max<int64_t>(score_total, 1))) != GP_OK) return st;
+  if ((st = ensure(c, c->kout, sizeof(int32_t) * (size_t)n * units * 2)) != GP_OK) return st;
+  if ((st = ensure(c, c->ksum, sizeof(unsigned long long) * (size_t)n * 2)) != GP_OK) return st;
+  if (dbg_total > 0 && (st = ensure(c, c->dbg, sizeof(float) * (size_t)dbg_total)) != GP_OK) return st;
+
+  // work buckets: pages per CTA (ppc) and cluster size (C) per request
+  std::map<std::pair<int, int>, std::vector<int32_t>> buckets;
+  for (int r = 0; r < n; ++r) {
+    const int P = reqs[r].num_pages;
+    const int ppc = P <= 128 ? 8 : 16;
+    const int C = (P + ppc - 1) / ppc;
+    buckets[{C, ppc}].push_back(r);
+  }
+  for (int r = 0; r < n; ++r) {
+    gp::DevReq& d = s.reqs[r];
+    d.num_pages = reqs[r].num_pages;
+    d.slot = reqs[r].slot;
+    d.pos = reqs[r].pos;
+    d.score_off = score_off[r];
+    d.dbg_off = dbg_off[r];
+    d.mask_off = 0;
+    d.bt_off = r * maxp;
+    d.pad = 0;
+    std::memcpy(s.bt + (size_t)r * maxp, reqs[r].block_table, sizeof(int32_t) * reqs[r].num_pages);
+  }
+  int wpos = 0;
+  std::vector<std::pair<std::pair<int, int>, std::pair<int, int>>> launches;  // (C,ppc),(offset,count)
+  for (auto it = buckets.rbegin(); it != buckets.rend(); ++it) {
+    launches.push_back({it->first, {wpos, (int)it->second.size()}});
+    for (int32_t r : it->second) s.work[wpos++] = r;
+  }
+  if ((st = upload(c, s)) != GP_OK) return st;
+  GP_CUDA(c, cudaMemsetAsync(c->ksum.p, 0, sizeof(unsigned long long) * (size_t)n * 2, c->stream));
+
+  gp::PrepArgs pa{};
+  pa.pool = c->pool;
+  pa.q = q_cur_dev;
+  pa.q_f32 = g.q_dtype == GP_DTYPE_F32;
+  pa.reqs = dev_at<gp::DevReq>(c, 0);
+  pa.n = n;
+  pa.L = g.num_layers;
+  pa.Hq = g.num_q_heads;
+  pa.Hkv = g.num_kv_heads;
+  pa.D = g.head_dim;
+  pa.M = g.max_slots;
+  pa.theta = g.rope_theta;
+  pa.qt = static_cast<float*>(c->qt.p);
+  pa.err = c->err_dev;
+  st = timed_launch(c, GP_KERNEL_PREP, "prep_queries", [&] { return gp::launch_prep(pa, c->stream); });
+  if (st != GP_OK) return st;
+
+  for (auto& l : launches) {
+    gp::DemandArgs da{};
+    da.k_cache = c->k_cache;
+    da.kv_f32 = g.kv_dtype == GP_DTYPE_F32;
+    da.num_pages_total = g.num_pages;
+    da.L = g.num_layers;
+    da.Hkv = g.num_kv_heads;
+    da.D = g.head_dim;
+    da.G = G;
+    da.b = kPage;
+    da.R = g.recent_window;
+    da.p = g.p;
+    da.qt = pa.qt;
+    da.reqs = pa.reqs;
+    da.bt = dev_at<int32_t>(c, s.off_bt);
+    da.work = dev_at<int32_t>(c, s.off_work) + l.second.first;
+    da.n_work = l.second.second;
+    da.C = l.first.first;
+    da.ppc = l.first.second;
+    da.scores = static_cast<float*>(c->scores.p);
+    da.kout = static_cast<int32_t*>(c->kout.p);
+    da.ksum = static_cast<unsigned long long*>(c->ksum.p);
+    da.dbg = dbg_total > 0 ? static_cast<float*>(c->dbg.p) : nullptr;
+    da.err = c->err_dev;
+    st = timed_launch(c, GP_KERNEL_DEMAND, "boundary_demand", [&] { return gp::launch_demand(da, c->stream); });
+    if (st != GP_OK) return st;
+  }
+  std::vector<unsigned long long> sums((size_t)n * 2);
+  GP_CUDA(c, cudaMemcpyAsync(sums.data(), c->ksum.p, sizeof(unsigned long long) * sums.size(),
+                             cudaMemcpyDeviceToHost, c->stream));
+  st = check_kernel_errors(c);  // synchronises
+  if (st != GP_OK) return st;
+
+  c->last_demand.assign(n, DemandRec{});
+  for (int r = 0; r < n; ++r) {
+    const int P = reqs[r].num_pages;
+    gp_demand& o = out[r];
+    o.sum_k_short = (int64_t)sums[2 * r];
+    o.sum_k_long = (int64_t)sums[2 * r + 1];
+    o.num_candidates = (P - 1) * kPage;
+    o.num_units = units;
+    o.delta = o.num_candidates > 0
+                  ? (double)(o.sum_k_short - o.sum_k_long) / ((double)o.num_candidates * units)
+                  : 0.0;
+    DemandRec& rec = c->last_demand[r];
+    rec.slot = reqs[r].slot;
+    rec.num_pages = P;
+    rec.pages.assign(reqs[r].block_table, reqs[r].block_table + P);
+    rec.gen = c->slot_gen[reqs[r].slot];
+    rec.score_off = score_off[r];
+    rec.dbg_off = dbg_off[r];
+  }
+  c->last_dbg_total = dbg_total;
+  c->stats.demand_calls += 1;
+  c->stats.demand_requests += n;
+  return GP_OK;
+}
+
+gp_status gp_decide(gp_ctx* c, int32_t n, const gp_request* reqs, const gp_demand* demand, gp_action* out) {
+  if (!c) return GP_ERR_INVALID;
+  if (n < 0) return fail(c, GP_ERR_INVALID, "negative n");
+  if (n > 0 && (!reqs || !demand || !out)) return fail(c, GP_ERR_INVALID, "null argument");
+  const gp_config& g = c->cfg;
+  int64_t free_now = (int64_t)c->free_pages.size();
+  int64_t granted = 0;
+  for (int r = 0; r < n; ++r) {
+    const int P = reqs[r].num_pages;
+    if (P < 1) return fail(c, GP_ERR_INVALID, "request %d: num_pages %d", r, P);
+    gp_action a{GP_ACT_COMPRESS, 0, 0};
+    if (P == 1) {
+      a.kind = GP_ACT_GROW;
+      a.forced = 1;
+    } else {
+      // Delta > tau, evaluated exactly from the integer sums for tau = 0
+      const double units = (double)demand[r].num_units;
+      const double cand = (double)demand[r].num_candidates;
+      const int64_t diff = demand[r].sum_k_short - demand[r].sum_k_long;
+      bool want = false;
+      if (g.policy == GP_POLICY_GROWPAGE) {
+        want = (g.tau == 0.0) ? diff > 0 : ((double)diff / (cand * units)) > g.tau;
+      }
+      if (want) {
+        if (free_now - granted > (int64_t)g.reserve_pages) {
+          a.kind = GP_ACT_GROW;
+          ++granted;
+        } else {
+          a.kind = GP_ACT_COMPRESS;
+          a.fallback = 1;
+        }
+      }
+    }
+    out[r] = a;
+    if (a.kind == GP_ACT_GROW) {
+      c->stats.grow += 1;
+      if (a.forced) c->stats.forced_grow += 1;
+    } else {
+      c->stats.compress += 1;
+      if (a.fallback) c->stats.fallback += 1;
+    }
+  }
+  return GP_OK;
+}
+
+gp_status gp_grow_page(gp_ctx* c, gp_request* req) {
+  if (!c || !req) return GP_ERR_INVALID;
+  if (!req->block_table) return fail(c, GP_ERR_INVALID, "null block table");
+  if (req->num_pages < 0 || req->num_pages >= c->cfg.max_pages_per_req)
+    return fail(c, GP_ERR_INVALID, "block table is full (%d pages)", req->num_pages);
+  int32_t page = -1;
+  gp_status st = gp_page_alloc(c, &page);
+  if (st != GP_OK) return st;
+  req->block_table[req->num_pages] = page;
+  req->num_pages += 1;
+  if (req->slot >= 0 && req->slot < c->cfg.max_slots) ++c->slot_gen[req->slot];
+  return GP_OK;
+}
+
+namespace {
+
+// Shared path of gp_compress_hold (keep_in == null) and gp_compact_kv.
+gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t* keep_in) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if (n < 0 || n > c->cfg.max_slots) return fail(c, GP_ERR_INVALID, "n = %d outside [0, max_slots]", n);
+  if (n == 0) return GP_OK;
+  if (!reqs) return fail(c, GP_ERR_INVALID, "null requests");
+  const gp_config& g = c->cfg;
+  const int units = units_of(c);
+  const int maxp = g.max_pages_per_req;
+  std::vector<int64_t> score_off(n, 0);
+  std::unordered_set<int32_t> slots;
+  for (int r = 0; r < n; ++r) {
+    st = validate_request(c, reqs[r], r, keep_in == nullptr);
+    if (st != GP_OK) return st;
+    if (reqs[r].num_pages < 2)
+      return fail(c, GP_ERR_INVALID, "request %d: Compress & Hold needs at least 2 pages", r);
+    if (keep_in == nullptr) {
+      if (!slots.insert(reqs[r].slot).second)
+        return fail(c, GP_ERR_INVALID, "slot %d appears twice in one call", reqs[r].slot);
+      const DemandRec* rec = nullptr;
+      for (const auto& d : c->last_demand)
+        if (d.slot == reqs[r].slot) rec = &d;
+      if (!rec || rec->gen != c->slot_gen[reqs[r].slot] || rec->num_pages != reqs[r].num_pages ||
+          !std::equal(rec->pages.begin(), rec->pages.end(), reqs[r].block_table))
+        return fail(c, GP_ERR_STATE,
+                    "request %d: no gp_boundary_demand result for its current pages (call it first)", r);
+      score_off[r] = rec->score_off;
+    }
+  }
+  // copy-on-write plan (App. E.2): every shared page gets a fresh target page
+  size_t need = 0;
+  for (int r = 0; r < n; ++r)
+    for (int j = 0; j < reqs[r].num_pages; ++j)
+      if (c->refcnt[reqs[r].block_table[j]] > 1) ++need;
+  if (need > c->free_pages.size())
+    return fail(c, GP_ERR_NO_PAGES, "copy-on-write needs %zu fresh pages, %zu free", need,
+                c->free_pages.size());
+
+  Staged s{};
+  if ((st = stage(c, n, true, &s)) != GP_OK) return st;
+  int64_t mask_total = 0;
+  std::vector<int64_t> mask_off(n);
+  for (int r = 0; r < n; ++r) {
+    mask_off[r] = mask_total;
+    mask_total += (int64_t)units * (reqs[r].num_pages * kPage / 32);
+  }
+  if ((st = ensure(c, c->masks, sizeof(uint32_t) * (size_t)mask_total)) != GP_OK) return st;
+
+  // allocate the CoW targets (cannot fail now), lowest id first, ascending logical order
+  std::vector<std::vector<int32_t>> replaced(n);
+  for (int r = 0; r < n; ++r) {
+    gp::DevReq& d = s.reqs[r];
+    const int P = reqs[r].num_pages;
+    d.num_pages = P;
+    d.slot = reqs[r].slot;
+    d.pos = reqs[r].pos;
+    d.score_off = score_off[r];
+    d.dbg_off = -1;
+    d.mask_off = mask_off[r];
+    d.bt_off = r * maxp;
+    d.pad = 0;
+    for (int j = 0; j < P; ++j) {
+      const int32_t pg = reqs[r].block_table[j];
+      s.bt[(size_t)r * maxp + j] = pg;
+      int32_t tgt = pg;
+      if (c->refcnt[pg] > 1) {
+        gp_page_alloc(c, &tgt);
+        replaced[r].push_back(pg);
+      }
+      s.bt_new[(size_t)r * maxp + j] = tgt;
+    }
+    s.work[r] = r;
+  }
+  if ((st = upload(c, s)) != GP_OK) return st;
+
+  gp::CompressArgs ca{};
+  ca.k_cache = c->k_cache;
+  ca.v_cache = c->v_cache;
+  ca.num_pages_total = g.num_pages;
+  ca.L = g.num_layers;
+  ca.Hkv = g.num_kv_heads;
+  ca.D = g.head_dim;
+  ca.elt = elt_bytes(g.kv_dtype);
+  ca.b = kPage;
+  ca.R = g.recent_window;
+  ca.k_loc = g.k_loc;
+  ca.reqs = dev_at<gp::DevReq>(c, 0);
+  ca.old_bt = dev_at<int32_t>(c, s.off_bt);
+  ca.new_bt = dev_at<int32_t>(c, s.off_bt_new);
+  ca.scores = static_cast<const float*>(c->scores.p);
+  ca.keep_in = keep_in;
+  ca.keep_out = static_cast<uint32_t*>(c->masks.p);
+  ca.work = dev_at<int32_t>(c, s.off_work);
+  ca.n_work = n;
+  ca.moved = c->moved_dev;
+  ca.err = c->err_dev;
+  st = timed_launch(c, GP_KERNEL_COMPRESS, "compress_hold", [&] { return gp::launch_compress(ca, c->stream); });
+  if (st != GP_OK) {
+    // roll back the page allocations
+    for (int r = 0; r < n; ++r)
+      for (int j = 0; j < reqs[r].num_pages; ++j) {
+        const int32_t t = s.bt_new[(size_t)r * maxp + j];
+        if (t != reqs[r].block_table[j]) gp_page_unref(c, t);
+      }
+    return st;
+  }
+  // host bookkeeping: new tables, drop the references to replaced shared pages
+  c->last_compress.assign(n, CompressRec{});
+  for (int r = 0; r < n; ++r) {
+    const int P = reqs[r].num_pages;
+    for (int j = 0; j < P; ++j) reqs[r].block_table[j] = s.bt_new[(size_t)r * maxp + j];
+    for (int32_t pg : replaced[r]) gp_page_unref(c, pg);
+    c->stats.cow_pages += (int64_t)replaced[r].size();
+    if (reqs[r].slot >= 0 && reqs[r].slot < g.max_slots) ++c->slot_gen[reqs[r].slot];
+    c->last_compress[r].num_pages = P;
+    c->last_compress[r].mask_off = mask_off[r];
+  }
+  return GP_OK;
+}
+
+}  // namespace
+
+gp_status gp_compress_hold(gp_ctx* c, int32_t n, gp_request* reqs) { return compress_common(c, n, reqs, nullptr); }
+
+gp_status gp_compact_kv(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t* keep_masks_dev) {
+  if (!c) return GP_ERR_INVALID;
+  if (n > 0 && !keep_masks_dev) return fail(c, GP_ERR_INVALID, "null keep masks");
+  return compress_common(c, n, reqs, keep_masks_dev);
+}
+
+// ---- inspection --------------------------------------------------------------
+
+gp_status gp_debug_demand_k(gp_ctx* c, int32_t req_idx, int32_t* k_out) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if (!k_out || req_idx < 0 || req_idx >= (int)c->last_demand.size())
+    return fail(c, GP_ERR_INVALID, "no demand result %d", req_idx);
+  const int units = units_of(c);
+  GP_CUDA(c, cudaMemcpyAsync(k_out, static_cast<int32_t*>(c->kout.p) + (size_t)req_idx * units * 2,
+                             sizeof(int32_t) * units * 2, cudaMemcpyDeviceToHost, c->stream));
+  GP_CUDA(c, cudaStreamSynchronize(c->stream));
+  return GP_OK;
+}
+
+gp_status gp_debug_scores(gp_ctx* c, int32_t req_idx, float* out) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if (!out || req_idx < 0 || req_idx >= (int)c->last_demand.size())
+    return fail(c, GP_ERR_INVALID, "no demand result %d", req_idx);
+  const DemandRec& rec = c->last_demand[req_idx];
+  const size_t count = (size_t)units_of(c) * (rec.num_pages * kPage - c->cfg.recent_window);
+  GP_CUDA(c, cudaMemcpyAsync(out, static_cast<float*>(c->scores.p) + rec.score_off, sizeof(float) * count,
+                             cudaMemcpyDeviceToHost, c->stream));
+  GP_CUDA(c, cudaStreamSynchronize(c->stream));
+  return GP_OK;
+}
+
+gp_status gp_debug_probs(gp_ctx* c, int32_t req_idx, float* out) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if (!out || req_idx < 0 || req_idx >= (int)c->last_demand.size())
+    return fail(c, GP_ERR_INVALID, "no demand result %d", req_idx);
+  const DemandRec& rec = c->last_demand[req_idx];
+  if (rec.dbg_off < 0) return fail(c, GP_ERR_STATE, "probabilities were not recorded (gp_set_debug)");
+  const size_t count = (size_t)units_of(c) * 2 * (rec.num_pages - 1) * kPage;
+  GP_CUDA(c, cudaMemcpyAsync(out, static_cast<float*>(c->dbg.p) + rec.dbg_off, sizeof(float) * count,
+                             cudaMemcpyDeviceToHost, c->stream));
+  GP_CUDA(c, cudaStreamSynchronize(c->stream));
+  return GP_OK;
+}
+
+gp_status gp_debug_keep_mask(gp_ctx* c, int32_t req_idx, uint32_t* out) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if (!out || req_idx < 0 || req_idx >= (int)c->last_compress.size())
+    return fail(c, GP_ERR_INVALID, "no compress result %d", req_idx);
+  const CompressRec& rec = c->last_compress[req_idx];
+  const size_t count = (size_t)units_of(c) * (rec.num_pages * kPage / 32);
+  GP_CUDA(c, cudaMemcpyAsync(out, static_cast<uint32_t*>(c->masks.p) + rec.mask_off, sizeof(uint32_t) * count,
+                             cudaMemcpyDeviceToHost, c->stream));
+  return check_kernel_errors(c);
+}
+
+gp_status gp_read_summaries(gp_ctx* c, int32_t slot, double* out) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  const gp_config& g = c->cfg;
+  if (!out || slot < 0 || slot >= g.max_slots) return fail(c, GP_ERR_INVALID, "bad slot %d", slot);
+  const size_t row = sizeof(double) * 2 * g.num_q_heads * g.head_dim;
+  GP_CUDA(c, cudaMemcpy2DAsync(out, row, reinterpret_cast<char*>(c->pool) + row * slot, row * g.max_slots, row,
+                               g.num_layers, cudaMemcpyDeviceToHost, c->stream));
+  return check_kernel_errors(c);
+}
+
+gp_status gp_set_debug(gp_ctx* c, int32_t flags) {
+  if (!c) return GP_ERR_INVALID;
+  c->debug = flags;
+  return GP_OK;
+}
+
+gp_status gp_set_timing(gp_ctx* c, int32_t enabled) {
+  if (!c) return GP_ERR_INVALID;
+  c->timing = enabled != 0;
+  return GP_OK;
+}
+
+static gp_status resolve_timing(gp_ctx* c) {
+  if (c->timed.empty()) return GP_OK;
+  GP_CUDA(c, cudaStreamSynchronize(c->stream));
+  for (auto& t : c->timed) {
+    float ms = 0.f;
+    GP_CUDA(c, cudaEventElapsedTime(&ms, t.start, t.stop));
+    c->t_ms[t.kernel] += ms;
+    c->t_count[t.kernel] += 1;
+    c->event_pool.push_back(t.start);
+    c->event_pool.push_back(t.stop);
+  }
+  c->timed.clear();
+  return GP_OK;
+}
+
+gp_status gp_kernel_time(gp_ctx* c, int32_t kernel, double* ms, int64_t* launches) {
+  if (!c || kernel < 0 || kernel >= GP_KERNEL_COUNT || !ms || !launches) return GP_ERR_INVALID;
+  gp_status st = resolve_timing(c);
+  if (st != GP_OK) return st;
+  *ms = c->t_ms[kernel];
+  *launches = c->t_count[kernel];
+  return GP_OK;
+}
+
+gp_status gp_reset_timing(gp_ctx* c) {
+  if (!c) return GP_ERR_INVALID;
+  gp_status st = resolve_timing(c);
+  if (st != GP_OK) return st;
+  for (int k = 0; k < GP_KERNEL_COUNT; ++k) {
+    c->t_ms[k] = 0.0;
+    c->t_count[k] = 0;
+  }
+  return GP_OK;
+}
+
+gp_status gp_stats(const gp_ctx* c, gp_stats_t* out) {
+  if (!c || !out) return GP_ERR_INVALID;
+  *out = c->stats;
+  if (!c->host_only) {
+    unsigned long long moved = 0;
+    if (cudaMemcpyAsync(&moved, c->moved_dev, sizeof(moved), cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
+        cudaStreamSynchronize(c->stream) != cudaSuccess)
+      return GP_ERR_CUDA;
+    out->moved_rows = (int64_t)moved;
+  }
+  return GP_OK;
+}
+

@@ -1,0 +1,230 @@
+"""CPU tests of the C-ABI library: it loads, exports every declared symbol,
+its structs match the header, and the host-side logic (page pool with
+refcounts, slots, decision, Grow) behaves as the oracle's model says.
+No compute call touches a GPU here: the contexts are host-only."""
+
+import os
+import re
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle.growpage as og
+import paged_kv_cache_step_gb300 as gp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "growpage.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return gp.load()
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:gp_status|const char\*)\s+(gp_\w+)\s*\(", txt, re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert len(declared) >= 25
+    out = subprocess.run(["nm", "-D", "--defined-only", gp.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(gp_\w+)", out))
+    missing = [d for d in declared if d not in exported]
+    assert not missing, missing
+    assert set(declared) == set(gp.EXPORTS)
+    for name in declared:
+        getattr(lib, name)
+
+
+def test_struct_layout_matches_header():
+    src = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "growpage.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(gp_config), offsetof(gp_config, beta_s),
+         offsetof(gp_config, rope_theta), sizeof(gp_request), offsetof(gp_request, pos),
+         sizeof(gp_demand), sizeof(gp_action), sizeof(gp_stats_t));
+  return 0;
+}
+"""
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
+        vals = list(map(int, subprocess.run([exe], capture_output=True, text=True,
+                                            check=True).stdout.split()))
+    import ctypes as C
+    ref = [C.sizeof(gp.GpConfig), gp.GpConfig.beta_s.offset, gp.GpConfig.rope_theta.offset,
+           C.sizeof(gp.GpRequest), gp.GpRequest.pos.offset, C.sizeof(gp.GpDemand),
+           C.sizeof(gp.GpAction), C.sizeof(gp.GpStats)]
+    assert vals == ref
+
+
+def _host_ctx(num_pages=16, **over):
+    cfg = gp.gp_config_default(num_layers=2, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                               max_slots=8, num_pages=num_pages, max_pages_per_req=8)
+    for k, v in over.items():
+        setattr(cfg, k, v)
+    return gp.gp_create(cfg)
+
+
+def test_config_validation():
+    bad = [dict(head_dim=96), dict(page_size=128), dict(num_q_heads=6), dict(p=1.0),
+           dict(beta_s=1.0), dict(max_pages_per_req=300), dict(recent_window=256),
+           dict(num_q_heads=16)]
+    for over in bad:
+        with pytest.raises(gp.GrowPageError):
+            _host_ctx(**over)
+
+
+def test_page_pool_matches_oracle_model():
+    ctx = _host_ctx(12)
+    model = og.PagePool(12)
+    rng = np.random.default_rng(0)
+    owned = []
+    try:
+        for step in range(400):
+            op = rng.integers(3)
+            if op == 0:
+                if model.free_count() == 0:
+                    with pytest.raises(gp.GrowPageError) as ei:
+                        gp.gp_page_alloc(ctx)
+                    assert ei.value.status == gp.GP_ERR_NO_PAGES
+                else:
+                    a = gp.gp_page_alloc(ctx)
+                    assert a == model.alloc()          # lowest free id first
+                    owned.append(a)
+            elif op == 1 and owned:
+                p = owned[rng.integers(len(owned))]
+                gp.gp_page_ref(ctx, p)
+                model.ref(p)
+                owned.append(p)
+            elif op == 2 and owned:
+                p = owned.pop(rng.integers(len(owned)))
+                gp.gp_page_unref(ctx, p)
+                model.unref(p)
+            assert gp.gp_free_page_count(ctx) == model.free_count()
+            for p in range(12):
+                assert gp.gp_page_refcount(ctx, p) == model.refcount[p]
+            # conservation: references held == sum of refcounts
+            assert sum(model.refcount) == len(owned)
+        with pytest.raises(gp.GrowPageError):
+            gp.gp_page_unref(ctx, 11 if model.refcount[11] == 0 else -1)
+    finally:
+        gp.gp_destroy(ctx)
+
+
+def test_slots_lowest_first_and_release():
+    ctx = _host_ctx()
+    try:
+        got = [gp.gp_slot_acquire(ctx) for _ in range(8)]
+        assert got == list(range(8))
+        with pytest.raises(gp.GrowPageError) as ei:
+            gp.gp_slot_acquire(ctx)
+        assert ei.value.status == gp.GP_ERR_NO_SLOTS
+        gp.gp_slot_release(ctx, 3)
+        with pytest.raises(gp.GrowPageError):
+            gp.gp_slot_release(ctx, 3)
+        assert gp.gp_slot_acquire(ctx) == 3
+    finally:
+        gp.gp_destroy(ctx)
+
+
+def _demand(sk, sl, P, units=4):
+    d = gp.GpDemand()
+    d.sum_k_short, d.sum_k_long = sk, sl
+    d.num_candidates = (P - 1) * 256
+    d.num_units = units
+    d.delta = (sk - sl) / (d.num_candidates * units) if P > 1 else 0.0
+    return d
+
+
+def test_decide_matches_oracle_rules():
+    rng = np.random.default_rng(1)
+    for trial in range(200):
+        free = int(rng.integers(0, 4))
+        reserve = int(rng.integers(0, 2))
+        tau = float(rng.choice([0.0, 0.001, -0.001]))
+        policy = int(rng.integers(2))
+        ctx = _host_ctx(num_pages=8, reserve_pages=reserve, tau=tau, policy=policy)
+        try:
+            for _ in range(8 - free):
+                gp.gp_page_alloc(ctx)
+            n = int(rng.integers(1, 5))
+            reqs, dem, ref = [], [], []
+            granted = 0
+            for r in range(n):
+                P = int(rng.integers(1, 5))
+                sk, sl = int(rng.integers(0, 2000)), int(rng.integers(0, 2000))
+                if trial % 7 == 0:
+                    sl = sk                       # Delta = 0 compresses
+                reqs.append(gp.Request(r, [0] * P, 0, 8))
+                d = _demand(sk, sl, P)
+                dem.append(d)
+                a = og.decide(d.delta, P, free - granted, reserve, tau,
+                              policy="growpage" if policy == 0 else "fixed")
+                if a.kind == og.GROW and not a.forced:
+                    granted += 1
+                ref.append(a)
+            acts = gp.gp_decide(ctx, reqs, dem)
+            for a, b in zip(acts, ref):
+                assert (a.kind, bool(a.fallback), bool(a.forced)) == (b.kind, b.fallback, b.forced)
+        finally:
+            gp.gp_destroy(ctx)
+
+
+def test_grow_appends_lowest_free_and_never_touches_prefix():
+    ctx = _host_ctx(num_pages=6)
+    try:
+        pages = [gp.gp_page_alloc(ctx) for _ in range(3)]   # 0,1,2
+        gp.gp_page_ref(ctx, 0)                              # shared prefix page
+        slot = gp.gp_slot_acquire(ctx)
+        req = gp.Request(slot, pages, 768, 4)
+        gp.gp_grow_page(ctx, req)
+        assert req.pages == [0, 1, 2, 3]
+        assert gp.gp_page_refcount(ctx, 0) == 2 and gp.gp_page_refcount(ctx, 3) == 1
+        with pytest.raises(gp.GrowPageError):               # block table full
+            gp.gp_grow_page(ctx, req)
+        assert req.num_pages == 4
+        req2 = gp.Request(slot, [gp.gp_page_alloc(ctx)], 0, 4)   # page 4
+        gp.gp_grow_page(ctx, req2)                          # takes page 5
+        with pytest.raises(gp.GrowPageError) as ei:
+            gp.gp_grow_page(ctx, req2)
+        assert ei.value.status == gp.GP_ERR_NO_PAGES and req2.pages == [4, 5]
+        # the C side enforces max_pages_per_req
+        ctx2 = _host_ctx(num_pages=16, max_pages_per_req=2)
+        try:
+            r3 = gp.Request(0, [gp.gp_page_alloc(ctx2), gp.gp_page_alloc(ctx2)], 0, 8)
+            with pytest.raises(gp.GrowPageError) as ei:
+                gp.gp_grow_page(ctx2, r3)
+            assert ei.value.status == gp.GP_ERR_INVALID and r3.num_pages == 2
+        finally:
+            gp.gp_destroy(ctx2)
+    finally:
+        gp.gp_destroy(ctx)
+
+
+def test_host_only_context_refuses_device_calls():
+    ctx = _host_ctx()
+    try:
+        with pytest.raises(gp.GrowPageError) as ei:
+            gp.gp_update_summaries(ctx, 1, 0, 0, 0)
+        assert ei.value.status == gp.GP_ERR_STATE
+        with pytest.raises(gp.GrowPageError) as ei:
+            gp.gp_boundary_demand(ctx, [gp.Request(0, [0], 0, 8)], 0)
+        assert ei.value.status == gp.GP_ERR_STATE
+    finally:
+        gp.gp_destroy(ctx)
+
+
+def test_mask_pack_roundtrip():
+    rng = np.random.default_rng(2)
+    keep = rng.random((3, 512)) < 0.5
+    assert np.array_equal(gp.unpack_mask(gp.pack_mask(keep), 512), keep)
