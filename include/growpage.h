@@ -195,6 +195,32 @@ gp_status gp_update_summaries(gp_ctx* ctx, int32_t n, const int32_t* slots_dev,
 gp_status gp_boundary_demand(gp_ctx* ctx, int32_t n, const gp_request* reqs,
                              const void* q_cur_dev, gp_demand* out);
 
+/* gp_boundary_demand_noalloc: the same demand estimation as
+ * gp_boundary_demand (same kernels, same results) for callers that must not
+ * allocate memory -- for example a serving process that reserves all of its
+ * GPU memory at start-up so that no request can fail later on an
+ * out-of-memory error and no cudaMalloc/cudaFree synchronises the device
+ * mid-flight.  The paper has no counterpart to this call.
+ * It calls no cudaMalloc, cudaFree or other allocating routine: every
+ * temporary (request descriptors, block tables, calibrated summaries,
+ * importance values, per-unit D_p and their sums) lives in one file-scope
+ * device array of 64 MiB that every GPU loading the library holds until the
+ * process exits.  A call needing more (roughly: the sum over requests of
+ * L * Hkv * (P * b - R) * 4 bytes, plus about 1 MiB per request) is
+ * rejected with GP_ERR_INVALID and a message naming the size; n is at most
+ * 512.  On the first call on a device, with that device current, the
+ * array's address is looked up once (cudaGetSymbolAddress); make that first
+ * call before any stream capture.  All calls share the array and its host
+ * staging, which keep the last call's contents: calls that overlap on the
+ * GPU, or run on several host threads at once, race.  Inputs and outputs
+ * are the caller's: out is host gp_demand[n]; k_units, if not NULL, is host
+ * int32[n][L * Hkv][2] receiving K^S, K^L per (layer, KV head).  It does not
+ * prepare a following gp_compress_hold (call gp_boundary_demand for that).
+ * Synchronises the stream. */
+gp_status gp_boundary_demand_noalloc(gp_ctx* ctx, int32_t n, const gp_request* reqs,
+                                     const void* q_cur_dev, gp_demand* out,
+                                     int32_t* k_units);
+
 /* gp_decide: Grow iff Delta > tau, else Compress & Hold (Sec. 3.2); P == 1
  * forces Grow; a Grow that would leave the pool at or below reserve_pages
  * (counting earlier grants of this call) becomes a fallback Compress

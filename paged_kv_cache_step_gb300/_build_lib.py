@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgrowpage.so")
 
-SOURCES = ["growpage.cpp", "k_summaries.cu", "k_demand.cu", "k_compress.cu"]
+SOURCES = ["growpage.cpp", "k_summaries.cu", "k_demand.cu", "k_compress.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,7 +38,8 @@ def _stale(obj: str, src: str) -> bool:
     if not os.path.exists(obj):
         return True
     t = os.path.getmtime(obj)
-    deps = [src, os.path.join(CSRC, "gp_kernels.h"), os.path.join(INCLUDE, "growpage.h")]
+    deps = [src, os.path.join(CSRC, "gp_kernels.h"), os.path.join(CSRC, "gp_internal.h"),
+            os.path.join(INCLUDE, "growpage.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 

@@ -33,6 +33,7 @@ EXPORTS = [
     "gp_config_default", "gp_create", "gp_destroy", "gp_last_error", "gp_status_string",
     "gp_page_alloc", "gp_page_ref", "gp_page_unref", "gp_page_refcount", "gp_free_page_count",
     "gp_slot_acquire", "gp_slot_release", "gp_update_summaries", "gp_boundary_demand",
+    "gp_boundary_demand_noalloc",
     "gp_decide", "gp_grow_page", "gp_compress_hold", "gp_compact_kv", "gp_debug_demand_k",
     "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
     "gp_set_debug", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
@@ -111,6 +112,7 @@ def load(build_if_missing: bool = True):
         "gp_slot_release": (I32, [P, I32]),
         "gp_update_summaries": (I32, [P, I32, P, P, P]),
         "gp_boundary_demand": (I32, [P, I32, C.POINTER(GpRequest), P, C.POINTER(GpDemand)]),
+        "gp_boundary_demand_noalloc": (I32, [P, I32, C.POINTER(GpRequest), P, C.POINTER(GpDemand), P]),
         "gp_decide": (I32, [P, I32, C.POINTER(GpRequest), C.POINTER(GpDemand), C.POINTER(GpAction)]),
         "gp_grow_page": (I32, [P, C.POINTER(GpRequest)]),
         "gp_compress_hold": (I32, [P, I32, C.POINTER(GpRequest)]),
@@ -255,6 +257,15 @@ def gp_boundary_demand(ctx, reqs, q_cur_dev):
     arr = _marshal(reqs)
     out = (GpDemand * max(1, len(reqs)))()
     _check(ctx, load().gp_boundary_demand(ctx, len(reqs), arr, _ptr(q_cur_dev), out))
+    return [out[i] for i in range(len(reqs))]
+
+
+def gp_boundary_demand_noalloc(ctx, reqs, q_cur_dev, k_units=None):
+    """No-allocation variant; k_units (host int32 [n][L*Hkv][2]) is optional."""
+    arr = _marshal(reqs)
+    out = (GpDemand * max(1, len(reqs)))()
+    _check(ctx, load().gp_boundary_demand_noalloc(ctx, len(reqs), arr, _ptr(q_cur_dev), out,
+                                                  _ptr(k_units) or None))
     return [out[i] for i in range(len(reqs))]
 
 

@@ -1,0 +1,28 @@
+// Read-only view of an engine context for translation units other than
+// growpage.cpp (which owns the gp_ctx definition).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "growpage.h"
+
+namespace gp {
+
+struct CtxView {
+  const gp_config* cfg;
+  void* k_cache;
+  void* v_cache;
+  const double* pool;   // summary pool [L][M][2][Hq][D]
+  cudaStream_t stream;
+  int* err_dev;         // kernel error word
+  bool host_only;
+};
+
+// Fills *out; false for a null context.
+bool ctx_view(const gp_ctx* c, CtxView* out);
+// True if `slot` is bound to a request.
+bool ctx_slot_bound(const gp_ctx* c, int slot);
+// Records the text returned by gp_last_error and returns `st`.
+gp_status ctx_fail(gp_ctx* c, gp_status st, const char* msg);
+
+}  // namespace gp

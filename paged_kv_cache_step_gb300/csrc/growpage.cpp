@@ -918,3 +918,29 @@ gp_status gp_stats(const gp_ctx* c, gp_stats_t* out) {
   return GP_OK;
 }
 
+
+// ---- read-only view for other translation units (gp_internal.h) ------------
+
+#include "gp_internal.h"
+
+namespace gp {
+
+bool ctx_view(const gp_ctx* c, CtxView* out) {
+  if (!c || !out) return false;
+  out->cfg = &c->cfg;
+  out->k_cache = c->k_cache;
+  out->v_cache = c->v_cache;
+  out->pool = c->pool;
+  out->stream = c->stream;
+  out->err_dev = c->err_dev;
+  out->host_only = c->host_only;
+  return true;
+}
+
+bool ctx_slot_bound(const gp_ctx* c, int slot) {
+  return c && slot >= 0 && slot < c->cfg.max_slots && c->slot_bound[slot];
+}
+
+gp_status ctx_fail(gp_ctx* c, gp_status st, const char* msg) { return fail(c, st, "%s", msg); }
+
+}  // namespace gp
