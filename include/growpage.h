@@ -267,17 +267,24 @@ gp_status gp_compact_kv(gp_ctx* ctx, int32_t n, gp_request* reqs,
 gp_status gp_debug_demand_k(gp_ctx* ctx, int32_t req_idx, int32_t* k_out);
 /* Importance log2 max(a^S, a^L) over [0, P b - R): host float[L*Hkv][P b - R]. */
 gp_status gp_debug_scores(gp_ctx* ctx, int32_t req_idx, float* out);
-/* Demand distributions a^S, a^L over C_t: host float[L*Hkv][2][(P-1) b].
- * Only filled when gp_set_debug(ctx, GP_DEBUG_PROBS) was set before the
- * demand call. */
+/* Demand distributions a^S, a^L over C_t: host float[L*Hkv][2][(P-1) b]
+ * (the kernels keep them for the D_p select of every demand call). */
 gp_status gp_debug_probs(gp_ctx* ctx, int32_t req_idx, float* out);
 /* Keep masks of the last gp_compress_hold: host uint32[L*Hkv][ceil(P b/32)]. */
 gp_status gp_debug_keep_mask(gp_ctx* ctx, int32_t req_idx, uint32_t* out);
 /* Summaries of one slot: host double[L][2][Hq][d]. */
 gp_status gp_read_summaries(gp_ctx* ctx, int32_t slot, double* out);
 
-#define GP_DEBUG_PROBS 1
-gp_status gp_set_debug(gp_ctx* ctx, int32_t flags);
+/* Which kernel scans the cache in gp_boundary_demand.  AUTO (default): the
+ * tensor-core (tcgen05) scan for bf16 caches and requests of at most 128
+ * pages, the CUDA-core (fp32 FMA) scan otherwise.  CUDA_CORE forces the
+ * latter everywhere; TENSOR_CORE makes requests it cannot serve fail with
+ * GP_ERR_UNSUPPORTED.  Both give the same results within the tolerances of
+ * fp32 arithmetic.  Host only. */
+#define GP_SCAN_AUTO 0
+#define GP_SCAN_CUDA_CORE 1
+#define GP_SCAN_TENSOR_CORE 2
+gp_status gp_set_scan_kernel(gp_ctx* ctx, int32_t kind);
 
 /* Per-kernel device time: when enabled, every kernel launch is bracketed by
  * CUDA events on the engine stream.  names: GP_KERNEL_* below.  The query

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgrowpage.so")
 
-SOURCES = ["growpage.cpp", "k_summaries.cu", "k_demand.cu", "k_compress.cu", "noalloc.cu"]
+SOURCES = ["growpage.cpp", "k_summaries.cu", "k_demand.cu", "k_demand_tc.cu", "k_compress.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -39,7 +39,7 @@ def _stale(obj: str, src: str) -> bool:
         return True
     t = os.path.getmtime(obj)
     deps = [src, os.path.join(CSRC, "gp_kernels.h"), os.path.join(CSRC, "gp_internal.h"),
-            os.path.join(INCLUDE, "growpage.h")]
+            os.path.join(CSRC, "demand_common.cuh"), os.path.join(INCLUDE, "growpage.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 

@@ -25,7 +25,7 @@ GP_ERR_CUDA, GP_ERR_TIMEOUT, GP_ERR_STATE, GP_ERR_UNSUPPORTED = 4, 5, 6, 7
 GP_DTYPE_BF16, GP_DTYPE_F32 = 0, 1
 GP_POLICY_GROWPAGE, GP_POLICY_FIXED = 0, 1
 GP_ACT_GROW, GP_ACT_COMPRESS = 0, 1
-GP_DEBUG_PROBS = 1
+GP_SCAN_AUTO, GP_SCAN_CUDA_CORE, GP_SCAN_TENSOR_CORE = 0, 1, 2
 GP_KERNEL_EMA, GP_KERNEL_PREP, GP_KERNEL_DEMAND, GP_KERNEL_COMPRESS = 0, 1, 2, 3
 KERNEL_NAMES = {0: "ema_update", 1: "prep_queries", 2: "boundary_demand", 3: "compress_hold"}
 
@@ -36,7 +36,7 @@ EXPORTS = [
     "gp_boundary_demand_noalloc",
     "gp_decide", "gp_grow_page", "gp_compress_hold", "gp_compact_kv", "gp_debug_demand_k",
     "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
-    "gp_set_debug", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
+    "gp_set_scan_kernel", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
 ]
 
 
@@ -122,7 +122,7 @@ def load(build_if_missing: bool = True):
         "gp_debug_probs": (I32, [P, I32, P]),
         "gp_debug_keep_mask": (I32, [P, I32, P]),
         "gp_read_summaries": (I32, [P, I32, P]),
-        "gp_set_debug": (I32, [P, I32]),
+        "gp_set_scan_kernel": (I32, [P, I32]),
         "gp_set_timing": (I32, [P, I32]),
         "gp_kernel_time": (I32, [P, I32, C.POINTER(C.c_double), C.POINTER(I64)]),
         "gp_reset_timing": (I32, [P]),
@@ -330,8 +330,9 @@ def gp_read_summaries(ctx, slot: int, L: int, hq: int, d: int) -> np.ndarray:
     return out
 
 
-def gp_set_debug(ctx, flags: int):
-    _check(ctx, load().gp_set_debug(ctx, flags))
+
+def gp_set_scan_kernel(ctx, kind: int):
+    _check(ctx, load().gp_set_scan_kernel(ctx, int(kind)))
 
 
 def gp_set_timing(ctx, enabled: bool):

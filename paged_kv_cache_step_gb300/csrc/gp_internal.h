@@ -2,6 +2,7 @@
 // growpage.cpp (which owns the gp_ctx definition).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "growpage.h"
@@ -16,6 +17,10 @@ struct CtxView {
   cudaStream_t stream;
   int* err_dev;         // kernel error word
   bool host_only;
+  const double* inv_freq;     // RoPE inverse frequencies [D/2]
+  const CUtensorMap* kmap;    // K cache tensor map (valid when tc_ok)
+  bool tc_ok;                 // the tensor-core scan may be used
+  int scan_kernel;            // GP_SCAN_*
 };
 
 // Fills *out; false for a null context.

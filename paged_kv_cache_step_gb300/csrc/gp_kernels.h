@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace gp {
@@ -15,7 +16,7 @@ struct DevReq {
   int32_t slot;        // summary-pool row
   int64_t pos;         // current decode position (RoPE)
   int64_t score_off;   // float offset of the request's importance cache
-  int64_t dbg_off;     // float offset of its debug probabilities (or -1)
+  int64_t aval_off;    // float offset of its a-values [units][2][(P-1) b]
   int64_t mask_off;    // word offset of its keep masks
   int32_t bt_off;      // offset of its block table in the packed table array
   int32_t pad;
@@ -27,6 +28,7 @@ enum : int {
   ERR_BAD_PAGE = 2,
   ERR_BAD_MASK = 4,
   ERR_BAD_COUNT = 8,
+  ERR_TIMEOUT = 16,
 };
 
 // ---- A1: EMA update -------------------------------------------------------
@@ -49,14 +51,20 @@ struct PrepArgs {
   int q_f32;
   const DevReq* reqs;      // [n]
   int n, L, Hq, Hkv, D, M;
-  double theta;
+  const double* inv_freq;  // [D/2] theta^(-2i/D)
   float* qt;               // [n][L][Hkv][2G][D], scaled by log2(e)/sqrt(D)
+  unsigned char* bq;       // optional tensor-core operand per unit (bq_bytes each)
   int* err;
 };
+// Bytes of the tensor-core B operand of one unit: D/64 swizzle halves of NB
+// rows x 128 B, NB = 3 x 2G rounded up to 16 (three bf16 parts per row).
+__host__ __device__ inline size_t bq_bytes(int D, int G) { return (size_t)(D / 64) * ((6 * G + 15) / 16 * 16) * 128; }
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 
-// ---- A3-A5: score scan, softmax, GQA mean, D_p, importance cache -----------
+// ---- A3-A5: score scan, softmax, GQA mean, a-values, importance cache, D_p --
 struct DemandArgs {
+  CUtensorMap kmap;        // K cache as [rows][D] bf16, box 64 x 128, 128-byte swizzle
+  int variant;             // DEMAND_FFMA or DEMAND_TC
   const void* k_cache;     // [L][num_pages][Hkv][b][D]
   int kv_f32;
   int num_pages_total;
@@ -64,6 +72,7 @@ struct DemandArgs {
   int b, R;
   double p;
   const float* qt;
+  const unsigned char* bq; // tensor-core operand per unit (prep kernel output)
   const DevReq* reqs;
   const int32_t* bt;       // packed block tables
   const int32_t* work;     // request indices handled by this launch
@@ -71,13 +80,38 @@ struct DemandArgs {
   int C;                   // cluster size (CTAs per unit)
   int ppc;                 // pages per CTA
   float* scores;           // importance cache, log2 domain
-  int32_t* kout;           // [n][L*Hkv][2]
-  unsigned long long* ksum;// [n][2]
-  float* dbg;              // optional [..][2][(P-1) b] per unit
+  float* aval;             // a^S, a^L over C_t: per unit [2][(P-1) b]
+  unsigned* tickets;       // [n][units] arrival counters, zero between calls
+  int32_t* kout;           // D_p per unit: [n][units][2]
+  unsigned long long* ksum;// sums over units: [n][2]
   int* err;
 };
-size_t demand_smem_bytes(int D, int G, int ppc);
-cudaError_t launch_demand(const DemandArgs& a, cudaStream_t s);
+enum : int { DEMAND_FFMA = 0, DEMAND_TC = 1 };
+cudaError_t launch_demand_ffma(const DemandArgs& a, cudaStream_t s);
+cudaError_t launch_demand_tc(const DemandArgs& a, cudaStream_t s);
+inline cudaError_t launch_demand(const DemandArgs& a, cudaStream_t s) {
+  return a.variant == DEMAND_TC ? launch_demand_tc(a, s) : launch_demand_ffma(a, s);
+}
+
+// How a request of P pages is split: kernel variant, pages per CTA (ppc) and
+// CTAs per cluster (C).  The tensor-core variant keeps a CTA's logits in
+// TMEM (32 columns per 128 keys, 512 columns per SM), so it takes up to 8
+// pages per CTA and 16 CTAs per cluster: P <= 128.
+struct DemandPlan {
+  int variant, ppc, C;
+};
+inline DemandPlan demand_plan(int P, bool tc_ok) {
+  DemandPlan pl;
+  if (tc_ok && P <= 128) {
+    pl.variant = DEMAND_TC;
+    pl.ppc = P <= 64 ? 4 : 8;
+  } else {
+    pl.variant = DEMAND_FFMA;
+    pl.ppc = P <= 128 ? 8 : 16;
+  }
+  pl.C = (P + pl.ppc - 1) / pl.ppc;
+  return pl;
+}
 
 // ---- A8-A10: window mask, Eq. 10 top-k, copy-on-write compaction -----------
 struct CompressArgs {

@@ -5,6 +5,8 @@
 // validates, plans, uploads descriptors and reads back results.
 #include "growpage.h"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -15,6 +17,7 @@
 #include <map>
 #include <set>
 #include <string>
+#include <tuple>
 #include <unordered_set>
 #include <vector>
 
@@ -36,7 +39,7 @@ struct DemandRec {
   std::vector<int32_t> pages;
   uint64_t gen = 0;
   int64_t score_off = 0;
-  int64_t dbg_off = -1;
+  int64_t aval_off = 0;
 };
 
 struct CompressRec {
@@ -71,17 +74,19 @@ struct gp_ctx {
   double* pool = nullptr;          // [L][M][2][Hq][D]
   int* err_dev = nullptr;          // kernel error bits
   unsigned long long* moved_dev = nullptr;
-  DevBuf upload, bt2, qt, scores, kout, ksum, dbg, masks;
+  DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks;
+  double* inv_freq = nullptr;      // [D/2] theta^(-2i/D) for RoPE
+  CUtensorMap kmap;                // K cache as a 2-D bf16 tensor (tensor-core scan)
+  bool tc_ok = false;              // kmap is valid
+  int scan_kernel = GP_SCAN_AUTO;
   void* pinned = nullptr;
   size_t pinned_cap = 0;
   cudaEvent_t pinned_free = nullptr;  // recorded after the last async use of `pinned`
 
   std::vector<DemandRec> last_demand;
   std::vector<CompressRec> last_compress;
-  int64_t last_dbg_total = 0;
 
   gp_stats_t stats{};
-  int debug = 0;
   bool timing = false;
   std::vector<TimedEvent> timed;
   std::vector<cudaEvent_t> event_pool;
@@ -207,6 +212,33 @@ gp_status validate_request(gp_ctx* c, const gp_request& r, int idx, bool need_sl
 
 int units_of(const gp_ctx* c) { return c->cfg.num_layers * c->cfg.num_kv_heads; }
 
+// Tensor map of the K cache for the tensor-core scan: a 2-D bf16 tensor of
+// rows = L * num_pages * Hkv * b keys by d elements, copied in boxes of
+// 64 elements x 128 keys with the 128-byte swizzle the MMA descriptors use.
+// False (and the CUDA-core scan is used) when the cache is not bf16, its
+// base is not 16-byte aligned, or the row count does not fit a coordinate.
+bool make_kmap(gp_ctx* c) {
+  const gp_config& g = c->cfg;
+  if (g.kv_dtype != GP_DTYPE_BF16) return false;
+  if (reinterpret_cast<uintptr_t>(c->k_cache) & 15u) return false;
+  const uint64_t rows = (uint64_t)g.num_layers * (uint64_t)g.num_pages * (uint64_t)g.num_kv_heads * kPage;
+  if (rows + 128 >= (1ull << 31)) return false;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  cuuint64_t dims[2] = {(cuuint64_t)g.head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)g.head_dim * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(&c->kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->k_cache, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 // The C linkage of every gp_* definition below comes from its declaration
@@ -288,12 +320,19 @@ gp_status gp_create(const gp_config* cfg, void* k_cache, void* v_cache, void* st
     if (e == cudaSuccess) e = cudaMalloc((void**)&c->err_dev, 64);
     if (e == cudaSuccess) e = cudaMemsetAsync(c->err_dev, 0, 64, c->stream);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pinned_free, cudaEventDisableTiming);
+    // RoPE inverse frequencies theta^(-2i/d), computed once in fp64
+    std::vector<double> inv(g.head_dim / 2);
+    for (int i = 0; i < g.head_dim / 2; ++i) inv[i] = std::pow(g.rope_theta, -2.0 * i / g.head_dim);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&c->inv_freq, sizeof(double) * inv.size());
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(c->inv_freq, inv.data(), sizeof(double) * inv.size(), cudaMemcpyHostToDevice, c->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) {
       gp_destroy(c);
       return GP_ERR_CUDA;
     }
     c->moved_dev = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(c->err_dev) + 8);
+    c->tc_ok = make_kmap(c);
   }
   *out = c;
   return GP_OK;
@@ -303,8 +342,10 @@ gp_status gp_destroy(gp_ctx* c) {
   if (!c) return GP_ERR_INVALID;
   if (!c->host_only) {
     cudaStreamSynchronize(c->stream);
-    for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->scores, &c->kout, &c->ksum, &c->dbg, &c->masks})
+    for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->bq, &c->scores, &c->aval, &c->tickets, &c->kout, &c->ksum,
+                      &c->masks})
       if (b->p) cudaFree(b->p);
+    if (c->inv_freq) cudaFree(c->inv_freq);
     if (c->pool) cudaFree(c->pool);
     if (c->err_dev) cudaFree(c->err_dev);
     if (c->pinned) cudaFreeHost(c->pinned);
@@ -477,34 +518,36 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   const int rows = 2 * G;
   const int maxp = g.max_pages_per_req;
 
-  // offsets of the importance cache and debug buffers
-  std::vector<int64_t> score_off(n), dbg_off(n, -1);
-  int64_t score_total = 0, dbg_total = 0;
+  // offsets of the importance cache and the a-values
+  std::vector<int64_t> score_off(n), aval_off(n);
+  int64_t score_total = 0, aval_total = 0;
   for (int r = 0; r < n; ++r) {
     const int P = reqs[r].num_pages;
     score_off[r] = score_total;
     score_total += (int64_t)units * (P * kPage - g.recent_window);
-    if (c->debug & GP_DEBUG_PROBS) {
-      dbg_off[r] = dbg_total;
-      dbg_total += (int64_t)units * 2 * (P - 1) * kPage;
-    }
+    aval_off[r] = aval_total;
+    aval_total += (int64_t)units * 2 * (P - 1) * kPage;
   }
   Staged s{};
   st = stage(c, n, false, &s);
   if (st != GP_OK) return st;
   if ((st = ensure(c, c->qt, sizeof(float) * (size_t)n * units * rows * g.head_dim)) != GP_OK) return st;
+  if ((st = ensure(c, c->bq, gp::bq_bytes(g.head_dim, G) * (size_t)n * units)) != GP_OK) return st;
   if ((st = ensure(c, c->scores, sizeof(float) * (size_t)std::max<int64_t>(score_total, 1))) != GP_OK) return st;
+  if ((st = ensure(c, c->aval, sizeof(float) * (size_t)std::max<int64_t>(aval_total, 1))) != GP_OK) return st;
+  if ((st = ensure(c, c->tickets, sizeof(unsigned) * (size_t)n * units)) != GP_OK) return st;
   if ((st = ensure(c, c->kout, sizeof(int32_t) * (size_t)n * units * 2)) != GP_OK) return st;
   if ((st = ensure(c, c->ksum, sizeof(unsigned long long) * (size_t)n * 2)) != GP_OK) return st;
-  if (dbg_total > 0 && (st = ensure(c, c->dbg, sizeof(float) * (size_t)dbg_total)) != GP_OK) return st;
 
-  // work buckets: pages per CTA (ppc) and cluster size (C) per request
-  std::map<std::pair<int, int>, std::vector<int32_t>> buckets;
+  // work buckets: (variant, cluster size C, pages per CTA), one launch each
+  const bool tc = c->tc_ok && c->scan_kernel != GP_SCAN_CUDA_CORE;
+  std::map<std::tuple<int, int, int>, std::vector<int32_t>> buckets;
   for (int r = 0; r < n; ++r) {
-    const int P = reqs[r].num_pages;
-    const int ppc = P <= 128 ? 8 : 16;
-    const int C = (P + ppc - 1) / ppc;
-    buckets[{C, ppc}].push_back(r);
+    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, tc);
+    if (c->scan_kernel == GP_SCAN_TENSOR_CORE && pl.variant != gp::DEMAND_TC)
+      return fail(c, GP_ERR_UNSUPPORTED, "request %d: the tensor-core scan needs a bf16 cache and at most 128 pages",
+                  r);
+    buckets[{pl.variant, pl.C, pl.ppc}].push_back(r);
   }
   for (int r = 0; r < n; ++r) {
     gp::DevReq& d = s.reqs[r];
@@ -512,20 +555,25 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     d.slot = reqs[r].slot;
     d.pos = reqs[r].pos;
     d.score_off = score_off[r];
-    d.dbg_off = dbg_off[r];
+    d.aval_off = aval_off[r];
     d.mask_off = 0;
     d.bt_off = r * maxp;
     d.pad = 0;
     std::memcpy(s.bt + (size_t)r * maxp, reqs[r].block_table, sizeof(int32_t) * reqs[r].num_pages);
   }
+  struct Launch {
+    int variant, C, ppc, first, count;
+  };
+  std::vector<Launch> launches;
   int wpos = 0;
-  std::vector<std::pair<std::pair<int, int>, std::pair<int, int>>> launches;  // (C,ppc),(offset,count)
-  for (auto it = buckets.rbegin(); it != buckets.rend(); ++it) {
-    launches.push_back({it->first, {wpos, (int)it->second.size()}});
+  for (auto it = buckets.rbegin(); it != buckets.rend(); ++it) {  // largest clusters first
+    launches.push_back({std::get<0>(it->first), std::get<1>(it->first), std::get<2>(it->first), wpos,
+                        (int)it->second.size()});
     for (int32_t r : it->second) s.work[wpos++] = r;
   }
   if ((st = upload(c, s)) != GP_OK) return st;
   GP_CUDA(c, cudaMemsetAsync(c->ksum.p, 0, sizeof(unsigned long long) * (size_t)n * 2, c->stream));
+  GP_CUDA(c, cudaMemsetAsync(c->tickets.p, 0, sizeof(unsigned) * (size_t)n * units, c->stream));
 
   gp::PrepArgs pa{};
   pa.pool = c->pool;
@@ -538,14 +586,17 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   pa.Hkv = g.num_kv_heads;
   pa.D = g.head_dim;
   pa.M = g.max_slots;
-  pa.theta = g.rope_theta;
+  pa.inv_freq = c->inv_freq;
   pa.qt = static_cast<float*>(c->qt.p);
+  pa.bq = static_cast<unsigned char*>(c->bq.p);
   pa.err = c->err_dev;
   st = timed_launch(c, GP_KERNEL_PREP, "prep_queries", [&] { return gp::launch_prep(pa, c->stream); });
   if (st != GP_OK) return st;
 
-  for (auto& l : launches) {
+  for (const Launch& l : launches) {
     gp::DemandArgs da{};
+    da.kmap = c->kmap;
+    da.variant = l.variant;
     da.k_cache = c->k_cache;
     da.kv_f32 = g.kv_dtype == GP_DTYPE_F32;
     da.num_pages_total = g.num_pages;
@@ -557,16 +608,18 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     da.R = g.recent_window;
     da.p = g.p;
     da.qt = pa.qt;
+    da.bq = pa.bq;
     da.reqs = pa.reqs;
     da.bt = dev_at<int32_t>(c, s.off_bt);
-    da.work = dev_at<int32_t>(c, s.off_work) + l.second.first;
-    da.n_work = l.second.second;
-    da.C = l.first.first;
-    da.ppc = l.first.second;
+    da.work = dev_at<int32_t>(c, s.off_work) + l.first;
+    da.n_work = l.count;
+    da.C = l.C;
+    da.ppc = l.ppc;
     da.scores = static_cast<float*>(c->scores.p);
+    da.aval = static_cast<float*>(c->aval.p);
+    da.tickets = static_cast<unsigned*>(c->tickets.p);
     da.kout = static_cast<int32_t*>(c->kout.p);
     da.ksum = static_cast<unsigned long long*>(c->ksum.p);
-    da.dbg = dbg_total > 0 ? static_cast<float*>(c->dbg.p) : nullptr;
     da.err = c->err_dev;
     st = timed_launch(c, GP_KERNEL_DEMAND, "boundary_demand", [&] { return gp::launch_demand(da, c->stream); });
     if (st != GP_OK) return st;
@@ -594,9 +647,8 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     rec.pages.assign(reqs[r].block_table, reqs[r].block_table + P);
     rec.gen = c->slot_gen[reqs[r].slot];
     rec.score_off = score_off[r];
-    rec.dbg_off = dbg_off[r];
+    rec.aval_off = aval_off[r];
   }
-  c->last_dbg_total = dbg_total;
   c->stats.demand_calls += 1;
   c->stats.demand_requests += n;
   return GP_OK;
@@ -721,7 +773,7 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
     d.slot = reqs[r].slot;
     d.pos = reqs[r].pos;
     d.score_off = score_off[r];
-    d.dbg_off = -1;
+    d.aval_off = 0;
     d.mask_off = mask_off[r];
     d.bt_off = r * maxp;
     d.pad = 0;
@@ -827,9 +879,9 @@ gp_status gp_debug_probs(gp_ctx* c, int32_t req_idx, float* out) {
   if (!out || req_idx < 0 || req_idx >= (int)c->last_demand.size())
     return fail(c, GP_ERR_INVALID, "no demand result %d", req_idx);
   const DemandRec& rec = c->last_demand[req_idx];
-  if (rec.dbg_off < 0) return fail(c, GP_ERR_STATE, "probabilities were not recorded (gp_set_debug)");
   const size_t count = (size_t)units_of(c) * 2 * (rec.num_pages - 1) * kPage;
-  GP_CUDA(c, cudaMemcpyAsync(out, static_cast<float*>(c->dbg.p) + rec.dbg_off, sizeof(float) * count,
+  if (count == 0) return GP_OK;
+  GP_CUDA(c, cudaMemcpyAsync(out, static_cast<float*>(c->aval.p) + rec.aval_off, sizeof(float) * count,
                              cudaMemcpyDeviceToHost, c->stream));
   GP_CUDA(c, cudaStreamSynchronize(c->stream));
   return GP_OK;
@@ -858,9 +910,13 @@ gp_status gp_read_summaries(gp_ctx* c, int32_t slot, double* out) {
   return check_kernel_errors(c);
 }
 
-gp_status gp_set_debug(gp_ctx* c, int32_t flags) {
+gp_status gp_set_scan_kernel(gp_ctx* c, int32_t kind) {
   if (!c) return GP_ERR_INVALID;
-  c->debug = flags;
+  if (kind != GP_SCAN_AUTO && kind != GP_SCAN_CUDA_CORE && kind != GP_SCAN_TENSOR_CORE)
+    return fail(c, GP_ERR_INVALID, "unknown scan kernel %d", kind);
+  if (kind == GP_SCAN_TENSOR_CORE && !c->host_only && !c->tc_ok)
+    return fail(c, GP_ERR_UNSUPPORTED, "the tensor-core scan needs a 16-byte aligned bf16 K cache");
+  c->scan_kernel = kind;
   return GP_OK;
 }
 
@@ -934,6 +990,10 @@ bool ctx_view(const gp_ctx* c, CtxView* out) {
   out->stream = c->stream;
   out->err_dev = c->err_dev;
   out->host_only = c->host_only;
+  out->inv_freq = c->inv_freq;
+  out->kmap = &c->kmap;
+  out->tc_ok = c->tc_ok && c->scan_kernel != GP_SCAN_CUDA_CORE;
+  out->scan_kernel = c->scan_kernel;
   return true;
 }
 

@@ -7,10 +7,10 @@
 //                   HBM traffic per element for bf16 queries.
 //  k_prep_queries -- App. E.1 Eq. 12 calibration gamma = RMS(q_t)/RMS(qbar)
 //                   and rotate-half RoPE at the current position, for the
-//                   requests at a capacity boundary.  One warp per
-//                   (request, layer, query head); fp64 arithmetic, rounded
-//                   once to fp32 and pre-scaled by log2(e)/sqrt(D) so the
-//                   score kernel works in base 2.
+//                   requests at a capacity boundary, pre-scaled by
+//                   log2(e)/sqrt(D) so the score kernels work in base 2.
+//                   Writes the fp32 rows and their three-part bf16 split in
+//                   the tensor-core operand layout.
 #include <cuda_bf16.h>
 
 #include "gp_kernels.h"
@@ -75,19 +75,36 @@ __global__ void __launch_bounds__(256) k_ema_update(EmaArgs a) {
   }
 }
 
-// One warp per (request, layer, query head).  Lane l owns elements
-// l + 32 m, so each rotate-half pair (i, i + D/2) sits in one lane.
+// Block per (request, layer, 8 query heads); warp per query head.  The
+// RoPE angles depend only on (position, pair index), so each block computes
+// them once: the angle pos * theta^(-2i/d) and its reduction to [-pi, pi]
+// in fp64 (exact enough for positions in the millions), cos/sin of the
+// reduced angle in fp32.  Calibration and rotation run in fp32 on the fp64
+// summaries rounded once; the result is rounded to fp32 (the qt rows) and
+// split into three bf16 parts for the tensor-core scan.
 template <int D>
 __global__ void __launch_bounds__(256) k_prep_queries(PrepArgs a) {
   constexpr int PER = D / 32;
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int total = a.n * a.L * a.Hq;
-  if (warp >= total) return;
-  const int g = warp % a.Hq;
-  const int l = (warp / a.Hq) % a.L;
-  const int r = warp / (a.Hq * a.L);
+  __shared__ float cs_s[D / 2], sn_s[D / 2];
+  const int hblocks = (a.Hq + 7) / 8;
+  const int hb = blockIdx.x % hblocks;
+  const int l = (blockIdx.x / hblocks) % a.L;
+  const int r = blockIdx.x / (hblocks * a.L);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const DevReq rq = a.reqs[r];
+  if (threadIdx.x < D / 2) {
+    const double ang = (double)rq.pos * a.inv_freq[threadIdx.x];
+    const double k = rint(ang * 0.15915494309189535);                  // 1 / (2 pi)
+    double red = fma(-k, 6.283185307179586, ang);                      // 2 pi, high part
+    red = fma(-k, 2.4492935982947064e-16, red);                        // 2 pi, low part
+    float sn, cs;
+    sincosf((float)red, &sn, &cs);
+    cs_s[threadIdx.x] = cs;
+    sn_s[threadIdx.x] = sn;
+  }
+  __syncthreads();
+  const int g = hb * 8 + warp;
+  if (g >= a.Hq) return;
   const int slot = rq.slot;
   const int G = a.Hq / a.Hkv;
   const int h = g / G, gi = g % G;
@@ -96,51 +113,74 @@ __global__ void __launch_bounds__(256) k_prep_queries(PrepArgs a) {
     return;
   }
   const size_t qoff = (((size_t)l * a.n + r) * a.Hq + g) * D;
-  double q[PER];
+  float sq = 0.f;
 #pragma unroll
   for (int m = 0; m < PER; ++m) {
     const int i = lane + 32 * m;
-    float v;
-    if (a.q_f32) {
-      v = static_cast<const float*>(a.q)[qoff + i];
-    } else {
-      v = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[qoff + i]);
-    }
-    q[m] = v;
+    const float v = a.q_f32 ? static_cast<const float*>(a.q)[qoff + i]
+                            : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[qoff + i]);
+    sq = fmaf(v, v, sq);
   }
-  double sq = 0.0;
-#pragma unroll
-  for (int m = 0; m < PER; ++m) sq += q[m] * q[m];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-  const double rms_q = sqrt(sq / D);
-  const double scale = 1.4426950408889634 / sqrt((double)D);  // log2(e)/sqrt(D)
-  const double pos = (double)rq.pos;
-  const double ltheta = log2(a.theta);
+  const float rms_q = sqrtf(sq / D);
+  const float scale = 1.4426950408889634f / sqrtf((float)D);  // log2(e)/sqrt(D)
+  const int ROWS = 2 * G;
+  const int NB = (3 * ROWS + 15) / 16 * 16;
+  unsigned char* bq = a.bq ? a.bq + (((size_t)r * a.L + l) * a.Hkv + h) * bq_bytes(D, G) : nullptr;
   for (int x = 0; x < 2; ++x) {
     const double* row = a.pool + (((size_t)l * a.M + slot) * 2 + x) * ((size_t)a.Hq * D) + (size_t)g * D;
-    double v[PER];
-    double sv = 0.0;
+    float v[PER];
+    float sv = 0.f;
 #pragma unroll
     for (int m = 0; m < PER; ++m) {
-      v[m] = row[lane + 32 * m];
-      sv += v[m] * v[m];
+      v[m] = (float)row[lane + 32 * m];
+      sv = fmaf(v[m], v[m], sv);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
-    const double rms_v = sqrt(sv / D);
-    const double gamma = rms_v > 0.0 ? rms_q / rms_v : 0.0;
-    float* out = a.qt + ((((size_t)r * a.L + l) * a.Hkv + h) * (2 * G) + x * G + gi) * D;
+    const float rms_v = sqrtf(sv / D);
+    const float gs = rms_v > 0.f ? (rms_q / rms_v) * scale : 0.f;   // Eq. 12 gain, base-2 scale
+    const int rr = x * G + gi;
+    float* out = a.qt + ((((size_t)r * a.L + l) * a.Hkv + h) * ROWS + rr) * D;
 #pragma unroll
     for (int m = 0; m < PER / 2; ++m) {
       const int i = lane + 32 * m;          // i < D/2; partner i + D/2 is v[m + PER/2]
-      const double inv_freq = exp2(-(2.0 * i / D) * ltheta);
-      double sn, cs;
-      sincos(pos * inv_freq, &sn, &cs);
-      const double x1 = gamma * v[m], x2 = gamma * v[m + PER / 2];
-      out[i] = (float)((x1 * cs - x2 * sn) * scale);
-      out[i + D / 2] = (float)((x2 * cs + x1 * sn) * scale);
+      const float x1 = v[m], x2 = v[m + PER / 2];
+      const float c = cs_s[i], sn = sn_s[i];
+      const float o1 = gs * fmaf(x1, c, -x2 * sn);
+      const float o2 = gs * fmaf(x2, c, x1 * sn);
+      out[i] = o1;
+      out[i + D / 2] = o2;
+      if (bq) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int d = e ? i + D / 2 : i;
+          const float q = e ? o2 : o1;
+          const __nv_bfloat16 h1 = __float2bfloat16_rn(q);
+          const float r1 = q - __bfloat162float(h1);
+          const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
+          const __nv_bfloat16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+          const __nv_bfloat16 parts[3] = {h1, h2, h3};
+#pragma unroll
+          for (int sp = 0; sp < 3; ++sp) {
+            const int n = sp * ROWS + rr;
+            const size_t off = (size_t)(d >> 6) * NB * 128 + (size_t)n * 128 + ((((d & 63) >> 3) ^ (n & 7)) << 4) +
+                               (size_t)(d & 7) * 2;
+            *reinterpret_cast<__nv_bfloat16*>(bq + off) = parts[sp];
+          }
+        }
+      }
     }
+  }
+  // the padding rows of the unit's operand are zero
+  if (bq && gi == 0) {
+    const int pad_rows = NB - 3 * ROWS;
+    for (int hf = 0; hf < D / 64; ++hf)
+      for (int k = lane; k < pad_rows * 32; k += 32) {
+        const int n = 3 * ROWS + k / 32;
+        reinterpret_cast<uint32_t*>(bq + (size_t)hf * NB * 128 + (size_t)n * 128)[k % 32] = 0u;
+      }
   }
 }
 
@@ -156,9 +196,8 @@ cudaError_t launch_ema(const EmaArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
-  const int warps = a.n * a.L * a.Hq;
-  if (warps == 0) return cudaSuccess;
-  const int blocks = (warps * 32 + 255) / 256;
+  const int blocks = a.n * a.L * ((a.Hq + 7) / 8);
+  if (blocks == 0) return cudaSuccess;
   if (a.D == 128) {
     k_prep_queries<128><<<blocks, 256, 0, s>>>(a);
   } else if (a.D == 64) {

@@ -6,8 +6,9 @@
 // cudaFree stalls the device with an implicit synchronisation) cannot let a
 // library grow scratch buffers on demand.  This entry point therefore uses
 // only the file-scope device array below for every temporary it needs: the
-// request descriptors and block tables, the calibrated summaries, the
-// importance values, the per-(layer, KV head) D_p results and their sums.
+// request descriptors and block tables, the calibrated summaries and their
+// tensor-core operands, the importance values, the a-values and arrival
+// tickets of the D_p select, the per-(layer, KV head) D_p and their sums.
 // It calls no cudaMalloc, cudaFree, cudaHostAlloc or other allocating routine;
 // host-side staging lives in fixed file-scope arrays.  Inputs (the caches,
 // the summaries in the engine's pool, the current queries) and outputs (the
@@ -18,7 +19,7 @@
 // library holds it until the process exits.  Every call shares it (and the
 // host staging arrays): calls whose work overlaps on the GPU, or that run on
 // several host threads at once, race.  It keeps the last call's contents;
-// the D_p sums that must start at zero are cleared by each call.
+// the D_p sums and tickets that must start at zero are cleared by each call.
 //
 // Set-up: on the first call on a device (with that device current) the
 // array's device address is looked up once with cudaGetSymbolAddress and
@@ -116,19 +117,23 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   const size_t off_bt = o;    o = align256(o + sizeof(int32_t) * (size_t)n * maxp);
   const size_t off_work = o;  o = align256(o + sizeof(int32_t) * n);
   const size_t off_qt = o;    o = align256(o + sizeof(float) * (size_t)n * units * 2 * G * g.head_dim);
+  const size_t off_bq = o;    o = align256(o + gp::bq_bytes(g.head_dim, G) * (size_t)n * units);
   const size_t off_kout = o;  o = align256(o + sizeof(int32_t) * (size_t)n * units * 2);
   const size_t off_ksum = o;  o = align256(o + sizeof(unsigned long long) * (size_t)n * 2);
+  const size_t off_tk = o;    o = align256(o + sizeof(unsigned) * (size_t)n * units);
+  // one float region: per request its importance values, then its a-values
   const size_t off_sc = o;
   for (int r = 0; r < n; ++r) {
     g_reqs[r].num_pages = reqs[r].num_pages;
     g_reqs[r].slot = reqs[r].slot;
     g_reqs[r].pos = reqs[r].pos;
     g_reqs[r].score_off = (int64_t)((o - off_sc) / sizeof(float));
-    g_reqs[r].dbg_off = -1;
+    o += sizeof(float) * (size_t)units * (reqs[r].num_pages * kPage - g.recent_window);
+    g_reqs[r].aval_off = (int64_t)((o - off_sc) / sizeof(float));
+    o += sizeof(float) * (size_t)units * 2 * (reqs[r].num_pages - 1) * kPage;
     g_reqs[r].mask_off = 0;
     g_reqs[r].bt_off = r * maxp;
     g_reqs[r].pad = 0;
-    o += sizeof(float) * (size_t)units * (reqs[r].num_pages * kPage - g.recent_window);
   }
   if (o > GP_NOALLOC_SCRATCH_BYTES)
     return fail(c, GP_ERR_INVALID,
@@ -149,28 +154,30 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   }
   unsigned char* base = g_scratch_addr[dev];
 
-  // ---- work buckets (cluster size C, pages per CTA), largest first ----------
-  int bucket_count[2][17] = {};
+  // ---- work buckets (scan variant, pages per CTA, cluster size C) ----------
+  // Key k = 2 * variant + wide: demand_plan gives each variant two CTA widths
+  // (tensor core 4 or 8 pages, CUDA core 8 or 16).
+  const int ppc_of[4] = {8, 16, 4, 8};
+  int bucket_count[4][17] = {};
+  auto key_of = [&](const gp::DemandPlan& pl) { return 2 * pl.variant + (pl.ppc == ppc_of[2 * pl.variant + 1]); };
   for (int r = 0; r < n; ++r) {
-    const int P = reqs[r].num_pages;
-    const int big = P > 128;
-    const int ppc = big ? 16 : 8;
-    bucket_count[big][(P + ppc - 1) / ppc] += 1;
+    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok);
+    if (v.scan_kernel == GP_SCAN_TENSOR_CORE && pl.variant != gp::DEMAND_TC)
+      return fail(c, GP_ERR_UNSUPPORTED, "request %lld: the tensor-core scan cannot serve it", r);
+    bucket_count[key_of(pl)][pl.C] += 1;
   }
-  int bucket_start[2][17];
+  int bucket_start[4][17];
   int pos = 0;
-  for (int big = 1; big >= 0; --big)
+  for (int k = 3; k >= 0; --k)
     for (int C = 16; C >= 1; --C) {
-      bucket_start[big][C] = pos;
-      pos += bucket_count[big][C];
+      bucket_start[k][C] = pos;
+      pos += bucket_count[k][C];
     }
-  int fill[2][17];
+  int fill[4][17];
   memcpy(fill, bucket_start, sizeof(fill));
   for (int r = 0; r < n; ++r) {
-    const int P = reqs[r].num_pages;
-    const int big = P > 128;
-    const int ppc = big ? 16 : 8;
-    g_work[fill[big][(P + ppc - 1) / ppc]++] = r;
+    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok);
+    g_work[fill[key_of(pl)][pl.C]++] = r;
   }
 
   // ---- uploads (from the caller's / static host memory; no staging buffers) --
@@ -182,6 +189,7 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + off_work, g_work, sizeof(int32_t) * n, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(base + off_ksum, 0, sizeof(unsigned long long) * n * 2, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(base + off_tk, 0, sizeof(unsigned) * (size_t)n * units, s);
   if (e != cudaSuccess) return cuda_fail(c, "upload", e);
 
   gp::PrepArgs pa{};
@@ -195,16 +203,20 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   pa.Hkv = g.num_kv_heads;
   pa.D = g.head_dim;
   pa.M = g.max_slots;
-  pa.theta = g.rope_theta;
+  pa.inv_freq = v.inv_freq;
   pa.qt = reinterpret_cast<float*>(base + off_qt);
+  pa.bq = base + off_bq;
   pa.err = v.err_dev;
   e = gp::launch_prep(pa, s);
   if (e != cudaSuccess) return cuda_fail(c, "prep_queries launch", e);
 
-  for (int big = 1; big >= 0; --big)
+  for (int k = 3; k >= 0; --k)
     for (int C = 16; C >= 1; --C) {
-      if (!bucket_count[big][C]) continue;
+      if (!bucket_count[k][C]) continue;
+      const int var = k / 2;
       gp::DemandArgs da{};
+      if (var == gp::DEMAND_TC) da.kmap = *v.kmap;
+      da.variant = var;
       da.k_cache = v.k_cache;
       da.kv_f32 = g.kv_dtype == GP_DTYPE_F32;
       da.num_pages_total = g.num_pages;
@@ -216,16 +228,18 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
       da.R = g.recent_window;
       da.p = g.p;
       da.qt = pa.qt;
+      da.bq = pa.bq;
       da.reqs = pa.reqs;
       da.bt = reinterpret_cast<const int32_t*>(base + off_bt);
-      da.work = reinterpret_cast<const int32_t*>(base + off_work) + bucket_start[big][C];
-      da.n_work = bucket_count[big][C];
+      da.work = reinterpret_cast<const int32_t*>(base + off_work) + bucket_start[k][C];
+      da.n_work = bucket_count[k][C];
       da.C = C;
-      da.ppc = big ? 16 : 8;
+      da.ppc = ppc_of[k];
       da.scores = reinterpret_cast<float*>(base + off_sc);
+      da.aval = reinterpret_cast<float*>(base + off_sc);
+      da.tickets = reinterpret_cast<unsigned*>(base + off_tk);
       da.kout = reinterpret_cast<int32_t*>(base + off_kout);
       da.ksum = reinterpret_cast<unsigned long long*>(base + off_ksum);
-      da.dbg = nullptr;
       da.err = v.err_dev;
       e = gp::launch_demand(da, s);
       if (e != cudaSuccess) return cuda_fail(c, "boundary_demand launch", e);

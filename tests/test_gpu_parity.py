@@ -93,7 +93,6 @@ def test_tiny_boundary_event(variant):
     w = synth.make_workload("tiny", device="cuda", variant=variant)
     run = hz.EngineRun(w)
     try:
-        gp.gp_set_debug(run.ctx, gp.GP_DEBUG_PROBS)
         run.feed_history()
         req = run.reqs[0]
         P = req.num_pages
@@ -173,7 +172,6 @@ def test_llama_single_boundary_event():
     w = synth.make_workload("llama8b_single", device="cuda")
     run = hz.EngineRun(w)
     try:
-        gp.gp_set_debug(run.ctx, gp.GP_DEBUG_PROBS)
         # a short history: 48 concentrated steps then 16 diffuse ones
         for t in range(64):
             w.history.append(synth.query_step(w, [t < 48]))

@@ -61,7 +61,7 @@ def test_noalloc_refuses_calls_beyond_its_scratch():
     try:
         pages = run.reqs[0].pages
         reqs = [run.reqs[0]]
-        for _ in range(7):   # 8 requests x 32 pages x 256 units: > 64 MiB of importance values
+        for _ in range(7):   # 8 requests x 32 pages x 256 units: > 64 MiB of importance and a-values
             slot = gp.gp_slot_acquire(run.ctx)
             reqs.append(gp.Request(slot, pages, run.reqs[0].pos, run.cfg.max_pages_per_req))
         with pytest.raises(gp.GrowPageError) as ei:
