@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(NT, 2) k_demand_ffma(const __grid_constant__ D
     float m[2][ROWS], s[2][ROWS];
 #pragma unroll
     for (int rr = 0; rr < ROWS; ++rr) {
-      m[0][rr] = m[1][rr] = -INFINITY;
+      m[0][rr] = m[1][rr] = NEG;
       s[0][rr] = s[1][rr] = 0.f;
     }
     for (int kl = tid; kl < nloc; kl += NT) {
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(NT, 2) k_demand_ffma(const __grid_constant__ D
       }
   }
   __syncthreads();
-  float cm = -INFINITY, cs = 0.f;
+  float cm = NEG, cs = 0.f;
   if (tid < 2 * ROWS) {
     for (int w = 0; w < NW; ++w) combine(cm, cs, part[(w * 2 * ROWS + tid) * 2], part[(w * 2 * ROWS + tid) * 2 + 1]);
   }
@@ -251,9 +251,10 @@ __global__ void __launch_bounds__(NT, 2) k_demand_ffma(const __grid_constant__ D
   unsigned k = 0;
   if (u.ndem > 0) {
     const float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
-    k = coverage_demand(av, u.ndem, a.p, reinterpret_cast<unsigned*>(zb), a.ppc * PAGE * ROWS, dps, a.err);
+    k = coverage_demand<NT, 0>(av, u.ndem, a.p, reinterpret_cast<unsigned*>(zb), a.ppc * PAGE * ROWS, dps, a.err, tid,
+                               0u, 0u);
   }
-  write_demand(a, u, k);
+  write_demand(a, u.r, u.unit, tid, k);
 }
 
 template <bool BF16, int D, int ROWS>

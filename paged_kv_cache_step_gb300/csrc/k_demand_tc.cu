@@ -15,19 +15,28 @@
 // in fp32, summed afterwards.  The prep kernel writes these parts already in
 // the 128-byte-swizzled K-major layout the MMA reads (one bulk copy).
 //
-// Per CTA (cluster rank c of the unit, logical pages [c*ppc, (c+1)*ppc)):
-//   thread 0   : TMA producer and MMA issuer.  A tile is 128 keys x d of one
-//                page (box 64 x 128, 128-byte swizzle), NSTAGE tiles in
-//                flight through an mbarrier ring; each tile's accumulator
-//                (128 lanes x N columns) stays in TMEM until the epilogue.
-//   warps 4..7 : while the scan runs, read each finished tile from TMEM
-//                (warp w owns lane quadrant w % 4) and fold its logits into
-//                online (max, sum) statistics per row.
-//   all        : push the statistics to every rank (DSMEM), merge, then
-//                read TMEM again to write a^S, a^L and the importance.
-//   last CTA   : of the unit (global ticket) computes D_p.
-// Every wait is bounded; on expiry the CTA records ERR_TIMEOUT, drains its
-// copies in flight and finishes with garbage rather than hanging.
+// Persistent and warp-specialised.  A cluster of C CTAs (one CTA per SM)
+// takes units (request, layer, KV head) g, g + #clusters, ...; in each, CTA
+// rank c scores logical pages [c*ppc, (c+1)*ppc).  Roles:
+//   warp 0      producer: per unit, the B operand (bulk copy) and the K tiles
+//               (128 keys x d, box 64 x 128 with the 128-byte swizzle)
+//               through an NSTAGE mbarrier ring, running ahead across units;
+//   warp 1      MMA issuer: tcgen05.mma into one of two TMEM buffers (a
+//               tile's accumulator is 128 lanes x N columns), so the next
+//               unit's scan proceeds while the epilogue reads the last one;
+//   warps 2..9  epilogue (warp w reads TMEM lane quadrant w % 4; two warps
+//               per quadrant split the tiles): online softmax statistics as
+//               tiles finish, a reduce-scatter butterfly over the warp, an
+//               exchange with every rank (st.async into the peers' shared
+//               memory, completing on their mbarriers), the merge, then a^S,
+//               a^L and the importance of every key to global memory, and
+//               a ticket per unit in global memory;
+//   warps 10..15 selector: rank k mod C computes the D_p of the cluster's
+//               k-th unit once all C tickets are in -- the exact radix select
+//               of demand_common.cuh, on the SM's otherwise idle issue slots.
+// Every wait is bounded; on expiry the CTA records ERR_TIMEOUT, raises a
+// shared abort flag that ends every role's loop, drains its copies in
+// flight and finishes with garbage rather than hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -38,6 +47,17 @@ namespace {
 
 using namespace dem;
 
+constexpr int NTHR = 512;       // 16 warps
+constexpr int EPI_W0 = 2;       // epilogue warps 2..9: two per TMEM lane quadrant
+constexpr int EPI_NW = 8;
+constexpr int EPI_NTH = 32 * EPI_NW;
+constexpr int SEL_W0 = 10;      // selector warps 10..15
+constexpr int SEL_NTH = 32 * (16 - SEL_W0);
+constexpr int BAR_EPI = 1;      // named barriers
+constexpr int BAR_SEL = 2;
+constexpr int QLEN = 32;        // select queue
+constexpr long long kWaitLimit = 1ll << 31;  // clock cycles (about one second)
+
 template <int D, int ROWS>
 struct TcCfg {
   static constexpr int NB = (3 * ROWS + 15) / 16 * 16;  // MMA N: 3 parts x ROWS rows, padded
@@ -46,15 +66,13 @@ struct TcCfg {
   static constexpr int HALF_BYTES = 128 * 128;           // one 64-element span of 128 keys
   static constexpr int BQ_BYTES = HALVES * NB * 128;
   static constexpr int KSTEPS = D / 16;
-  static constexpr int NSTAGE = 3;
-  static constexpr int MAX_TILES = 16;
+  static constexpr int NSTAGE = (96 * 1024) / TILE_BYTES;  // 96 KiB of K in flight per SM
+  static constexpr int MAX_READY = 512 / NB;             // tile slots of TMEM
   static constexpr uint32_t IDESC = (1u << 4)        // D: f32
                                     | (1u << 7)      // A: bf16
                                     | (1u << 10)     // B: bf16
                                     | ((uint32_t)(NB >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 };
-
-constexpr long long kWaitLimit = 1ll << 31;  // clock cycles (about one second)
 
 // ---- PTX wrappers ----------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -62,6 +80,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -93,6 +114,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// 8 bytes into rank `rank`'s shared memory at the address that `local` has
+// here, completing on that rank's mbarrier at the address `local_bar` has here.
+__device__ __forceinline__ void st_async_b64(uint32_t local, uint32_t local_bar, int rank, uint64_t v) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(ra), "l"(v), "r"(rb)
+               : "memory");
+}
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
          ((uint64_t)2 << 61);
@@ -109,6 +139,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, %1;" ::"n"(BAR_EPI), "n"(EPI_NTH) : "memory"); }
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 template <int NB>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v);
@@ -142,238 +178,476 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Logits of the key in this thread's lane of tile t: sum of the three parts.
+// Logits of the key in this thread's lane of the tile at TMEM column `col`.
 template <int NB, int ROWS>
-__device__ __forceinline__ void tile_logits(uint32_t tmem, int quad, int t, float* z) {
+__device__ __forceinline__ void tile_logits(uint32_t tmem, int quad, int col, float* z) {
   float v[NB];
-  tmem_ld<NB>(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(t * NB), v);
+  tmem_ld<NB>(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)col, v);
 #pragma unroll
   for (int r = 0; r < ROWS; ++r) z[r] = v[r] + (v[ROWS + r] + v[2 * ROWS + r]);
 }
 
-// Shared memory, after aligning the dynamic base to 1 KiB.
+// Per-unit facts every role derives from the unit index w.
+struct UnitInfo {
+  int r, unit, layer, h, P, ndem, ncmp, npg, j0;
+  DevReq rq;
+};
+__device__ __forceinline__ UnitInfo unit_info(const DemandArgs& a, int w, int crank) {
+  UnitInfo u;
+  const int units = a.L * a.Hkv;
+  u.r = a.work[w / units];
+  u.unit = w % units;
+  u.layer = u.unit / a.Hkv;
+  u.h = u.unit % a.Hkv;
+  u.rq = a.reqs[u.r];
+  u.P = u.rq.num_pages;
+  u.ndem = (u.P - 1) * PAGE;
+  u.ncmp = u.P * PAGE - a.R;
+  u.j0 = crank * a.ppc;
+  u.npg = max(0, min(u.P, u.j0 + a.ppc) - u.j0);
+  return u;
+}
+
+struct XStat {
+  float m, s;
+};
+
+// Shared memory, after aligning the dynamic base to 1 KiB.  The select
+// buffer takes whatever is left of the dynamic allocation.
 template <int D, int ROWS>
 struct TcSmem {
   using T = TcCfg<D, ROWS>;
   static constexpr size_t STAGE = 0;
-  static constexpr size_t BQ = STAGE + (size_t)T::NSTAGE * T::TILE_BYTES;
-  static constexpr size_t BARS = BQ + T::BQ_BYTES;                    // full, empty, bq, ready[]
-  static constexpr int NBARS = 2 * T::NSTAGE + 1 + T::MAX_TILES;
-  static constexpr size_t XG = (BARS + 8 * NBARS + 15) & ~size_t(15);
-  static constexpr size_t PART = XG + sizeof(StatXchg);              // [4 warps][2 sets][ROWS] (m, s)
-  static constexpr size_t LSE = PART + sizeof(float) * 4 * 2 * ROWS * 2;
-  static constexpr size_t MISC = LSE + sizeof(float) * 2 * ROWS;     // tmem holder, abort, flag, pages
-  static constexpr size_t END = MISC + sizeof(int) * (4 + T::MAX_TILES);
-  static constexpr size_t BYTES = END + 1024;                        // alignment slack
-  static_assert(sizeof(DpSmem) + 1024 <= (size_t)T::NSTAGE * T::TILE_BYTES, "select scratch");
+  static constexpr size_t BQ = STAGE + (size_t)T::NSTAGE * T::TILE_BYTES;  // 2 buffers
+  static constexpr size_t XG = BQ + 2 * (size_t)T::BQ_BYTES;               // XStat [2][16][16]
+  static constexpr size_t BARS = XG + sizeof(XStat) * 2 * 16 * 16;
+  // full[NSTAGE], empty[NSTAGE], bqfull[2], bqempty[2], tfree[2], xbar[2], mmadone, sel, ready[MAX_READY]
+  static constexpr int NBARS = 2 * T::NSTAGE + 10 + T::MAX_READY;
+  static constexpr size_t PART = BARS + 8 * (size_t)NBARS;                 // [EPI_NW][16] XStat
+  static constexpr size_t LSE = PART + sizeof(XStat) * EPI_NW * 16;        // lse_dem[8], lse_cmp[8]
+  static constexpr size_t MISC = LSE + sizeof(float) * 16;                 // ints, see kernel
+  static constexpr size_t DPS = (MISC + sizeof(int) * (16 + QLEN + 16) + 15) & ~size_t(15);
+  static constexpr size_t SEL = (DPS + sizeof(DpSmem) + 15) & ~size_t(15);
+  static constexpr size_t MIN_SEL_BYTES = 8 * 1024;
+  static constexpr size_t MIN_BYTES = SEL + MIN_SEL_BYTES + 1024;          // + alignment slack
 };
 
 template <int D, int ROWS>
-__global__ void __launch_bounds__(NT, 2) k_demand_tc(const __grid_constant__ DemandArgs a) {
+__global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ DemandArgs a, int total_units,
+                                                       int smem_bytes) {
   using T = TcCfg<D, ROWS>;
   using S = TcSmem<D, ROWS>;
+  constexpr int NSTAT = 2 * ROWS;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  StatXchg* xg = reinterpret_cast<StatXchg*>(smem + S::XG);
-  float* part = reinterpret_cast<float*>(smem + S::PART);
+  XStat* xg = reinterpret_cast<XStat*>(smem + S::XG);         // [parity][rank][stat]
+  XStat* part = reinterpret_cast<XStat*>(smem + S::PART);
   float* lse_dem = reinterpret_cast<float*>(smem + S::LSE);
-  float* lse_cmp = lse_dem + ROWS;
+  float* lse_cmp = lse_dem + 8;
   int* misc = reinterpret_cast<int*>(smem + S::MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort = misc + 1;
-  int* flag = misc + 2;
-  int* phys = misc + 4;
+  volatile int* q_head = misc + 2;
+  volatile int* q_tail = misc + 3;
+  volatile int* q_done = misc + 4;
+  volatile int* sel_item = misc + 5;
+  int* flag = misc + 6;
+  int* phys = misc + 16;                                      // [16]
+  volatile int* queue = misc + 32;                            // [QLEN]
+  DpSmem* dps = reinterpret_cast<DpSmem*>(smem + S::DPS);
+  unsigned* selbuf = reinterpret_cast<unsigned*>(smem + S::SEL);
+  const int sel_cap =
+      (int)(((size_t)smem_bytes - (size_t)(smem - smem_raw) - S::SEL) / sizeof(unsigned));
+
   const uint32_t bar_full = sbase + (uint32_t)S::BARS;
   const uint32_t bar_empty = bar_full + 8 * T::NSTAGE;
-  const uint32_t bar_bq = bar_empty + 8 * T::NSTAGE;
-  const uint32_t bar_ready = bar_bq + 8;
+  const uint32_t bar_bqfull = bar_empty + 8 * T::NSTAGE;
+  const uint32_t bar_bqempty = bar_bqfull + 16;
+  const uint32_t bar_tfree = bar_bqempty + 16;
+  const uint32_t bar_xg = bar_tfree + 16;
+  const uint32_t bar_mmadone = bar_xg + 16;
+  const uint32_t bar_sel = bar_mmadone + 8;
+  const uint32_t bar_ready = bar_sel + 8;
 
-  cluster_arrive_relaxed();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const Unit u = make_unit(a);
+  const int C = a.C;
+  const int crank = (int)(blockIdx.x % (unsigned)C);
+  const int g0 = (int)(blockIdx.x / (unsigned)C);
+  const int nclus = (int)(gridDim.x / (unsigned)C);
   const int units = a.L * a.Hkv;
-  const int ntiles = 2 * u.npg;
-  const uint32_t ncols = (uint32_t)a.ppc * 2 * T::NB <= 32 ? 32u : (uint32_t)a.ppc * 2 * T::NB;
+  const int TPB = 2 * a.ppc;                                  // tiles per unit and TMEM buffer
+  const int NBUF = (2 * TPB * T::NB <= 512) ? 2 : 1;
 
   if (tid == 0) {
     for (int s = 0; s < T::NSTAGE; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_bq, 1);
-    for (int t = 0; t < T::MAX_TILES; ++t) mbar_init(bar_ready + 8 * t, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_bqfull + 8 * b, 1);
+      mbar_init(bar_bqempty + 8 * b, 1);
+      mbar_init(bar_tfree + 8 * b, 1);
+      mbar_init(bar_xg + 8 * b, 1);
+    }
+    mbar_init(bar_mmadone, 1);
+    mbar_init(bar_sel, 1);
+    for (int t = 0; t < T::MAX_READY; ++t) mbar_init(bar_ready + 8 * t, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *abort = 0;
-    for (int j = 0; j < u.npg; ++j) phys[j] = checked_page(a, u, u.j0 + j);
+    *q_head = 0;
+    *q_tail = 0;
+    *q_done = 0;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
-                 "r"(ncols)
+                 "r"(512)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers of every rank initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  // ---- scan ----------------------------------------------------------------
   if (warp == 0) {
+    // ---- producer --------------------------------------------------------
     if (lane == 0) {
-      const size_t layer_rows = (size_t)u.layer * a.num_pages_total;
-      auto issue = [&](int t) {
-        const int s = t % T::NSTAGE;
-        const int y = (int)(((layer_rows + phys[t >> 1]) * a.Hkv + u.h) * PAGE + (t & 1) * 128);
-        const uint32_t dst = sbase + (uint32_t)(S::STAGE + (size_t)s * T::TILE_BYTES);
-        mbar_expect_tx(bar_full + 8 * s, T::TILE_BYTES);
-#pragma unroll
-        for (int hx = 0; hx < T::HALVES; ++hx) tma_load_2d(dst + hx * T::HALF_BYTES, &a.kmap, hx * 64, y, bar_full + 8 * s);
-      };
-      mbar_expect_tx(bar_bq, T::BQ_BYTES);
-      bulk_load(sbase + (uint32_t)S::BQ, a.bq + ((size_t)u.r * units + u.unit) * T::BQ_BYTES, T::BQ_BYTES, bar_bq);
-      int issued = 0;
-      for (; issued < T::NSTAGE && issued < ntiles; ++issued) issue(issued);
-      bool ok = mbar_wait(bar_bq, 0, abort);
-      int t = 0;
-      for (; ok && t < ntiles; ++t) {
-        const int s = t % T::NSTAGE;
-        if (!(ok = mbar_wait(bar_full + 8 * s, (t / T::NSTAGE) & 1, abort))) break;
-        tc_fence_after();
-        const uint32_t a0 = sbase + (uint32_t)(S::STAGE + (size_t)s * T::TILE_BYTES);
-        const uint32_t b0 = sbase + (uint32_t)S::BQ;
-#pragma unroll
-        for (int k = 0; k < T::KSTEPS; ++k) {
-          const uint32_t ad = a0 + (k >> 2) * T::HALF_BYTES + (k & 3) * 32;
-          const uint32_t bd = b0 + (k >> 2) * (T::NB * 128) + (k & 3) * 32;
-          mma_f16(tmem + (uint32_t)(t * T::NB), sw128_desc(ad), sw128_desc(bd), T::IDESC, k > 0 ? 1u : 0u);
+      int gt = 0, last_gt[T::NSTAGE], last_bq[2] = {-1, -1};
+      for (int s = 0; s < T::NSTAGE; ++s) last_gt[s] = -1;
+      bool ok = true;
+      for (int kk = 0; ok; ++kk) {
+        const int w = g0 + kk * nclus;
+        if (w >= total_units) break;
+        const UnitInfo u = unit_info(a, w, crank);
+        const int b2 = kk & 1;
+        if (kk >= 2 && !(ok = mbar_wait(bar_bqempty + 8 * b2, ((kk >> 1) - 1) & 1, abort))) break;
+        mbar_expect_tx(bar_bqfull + 8 * b2, T::BQ_BYTES);
+        bulk_load(sbase + (uint32_t)(S::BQ + (size_t)b2 * T::BQ_BYTES),
+                  a.bq + ((size_t)u.r * units + u.unit) * T::BQ_BYTES, T::BQ_BYTES, bar_bqfull + 8 * b2);
+        last_bq[b2] = kk;
+        for (int j = 0; j < u.npg; ++j) {
+          int pg = a.bt[u.rq.bt_off + u.j0 + j];
+          if (pg < 0 || pg >= a.num_pages_total) {
+            atomicOr(a.err, ERR_BAD_PAGE);
+            pg = 0;
+          }
+          phys[j] = pg;
         }
-        mma_commit(bar_empty + 8 * s);
-        mma_commit(bar_ready + 8 * t);
-        // refill the stage of the previous tile once its MMAs are done
-        if (t >= 1 && issued < ntiles) {
-          const int tp = t - 1, sp = tp % T::NSTAGE;
-          if (!(ok = mbar_wait(bar_empty + 8 * sp, (tp / T::NSTAGE) & 1, abort))) break;
-          issue(issued++);
+        const size_t layer_rows = (size_t)u.layer * a.num_pages_total;
+        for (int t = 0; t < 2 * u.npg; ++t, ++gt) {
+          const int s = gt % T::NSTAGE;
+          if (gt >= T::NSTAGE && !(ok = mbar_wait(bar_empty + 8 * s, ((gt / T::NSTAGE) - 1) & 1, abort))) break;
+          const int y = (int)(((layer_rows + phys[t >> 1]) * a.Hkv + u.h) * PAGE + (t & 1) * 128);
+          const uint32_t dst = sbase + (uint32_t)(S::STAGE + (size_t)s * T::TILE_BYTES);
+          mbar_expect_tx(bar_full + 8 * s, T::TILE_BYTES);
+#pragma unroll
+          for (int hx = 0; hx < T::HALVES; ++hx)
+            tma_load_2d(dst + hx * T::HALF_BYTES, &a.kmap, hx * 64, y, bar_full + 8 * s);
+          last_gt[s] = gt;
         }
       }
       if (!ok) {
         atomicOr(a.err, ERR_TIMEOUT);
         *abort = 1;
-        // wait (bounded) for the copies still in flight before the memory is reused
-        const int zero = 0;
-        for (int tt = t; tt < issued; ++tt) mbar_wait(bar_full + 8 * (tt % T::NSTAGE), (tt / T::NSTAGE) & 1, &zero);
       }
+      // every copy issued has landed before the CTA moves on (bounded)
+      const int zero = 0;
+      for (int s = 0; s < T::NSTAGE; ++s)
+        if (last_gt[s] >= 0) mbar_wait(bar_full + 8 * s, (last_gt[s] / T::NSTAGE) & 1, &zero);
+      for (int b = 0; b < 2; ++b)
+        if (last_bq[b] >= 0) mbar_wait(bar_bqfull + 8 * b, (last_bq[b] >> 1) & 1, &zero);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // online softmax statistics of the finished tiles
-    const int quad = warp - 4;
-    float m[2][ROWS], sm[2][ROWS];
+  } else if (warp == 1) {
+    // ---- MMA issuer --------------------------------------------------------
+    if (lane == 0) {
+      int gt = 0;
+      bool ok = true;
+      for (int kk = 0; ok; ++kk) {
+        const int w = g0 + kk * nclus;
+        if (w >= total_units) break;
+        const UnitInfo u = unit_info(a, w, crank);
+        const int b = kk % NBUF, b2 = kk & 1;
+        if (kk >= NBUF && !(ok = mbar_wait(bar_tfree + 8 * b, ((kk / NBUF) - 1) & 1, abort))) break;
+        if (!(ok = mbar_wait(bar_bqfull + 8 * b2, (kk >> 1) & 1, abort))) break;
+        const uint32_t b0 = sbase + (uint32_t)(S::BQ + (size_t)b2 * T::BQ_BYTES);
+        for (int t = 0; t < 2 * u.npg; ++t, ++gt) {
+          const int s = gt % T::NSTAGE;
+          if (!(ok = mbar_wait(bar_full + 8 * s, (gt / T::NSTAGE) & 1, abort))) break;
+          tc_fence_after();
+          const uint32_t a0 = sbase + (uint32_t)(S::STAGE + (size_t)s * T::TILE_BYTES);
+          const uint32_t col = (uint32_t)((b * TPB + t) * T::NB);
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r) {
-      m[0][r] = m[1][r] = -INFINITY;
-      sm[0][r] = sm[1][r] = 0.f;
+          for (int k = 0; k < T::KSTEPS; ++k) {
+            const uint32_t ad = a0 + (k >> 2) * T::HALF_BYTES + (k & 3) * 32;
+            const uint32_t bd = b0 + (k >> 2) * (T::NB * 128) + (k & 3) * 32;
+            mma_f16(tmem + col, sw128_desc(ad), sw128_desc(bd), T::IDESC, k > 0 ? 1u : 0u);
+          }
+          mma_commit(bar_empty + 8 * s);
+          mma_commit(bar_ready + 8 * (b * TPB + t));
+        }
+        if (ok) mma_commit(bar_bqempty + 8 * b2);
+      }
+      if (!ok) {
+        atomicOr(a.err, ERR_TIMEOUT);
+        *abort = 1;
+      }
+      // all MMAs issued have completed before TMEM is released (bounded)
+      mma_commit(bar_mmadone);
+      const int zero = 0;
+      mbar_wait(bar_mmadone, 0, &zero);
     }
-    for (int t = 0; t < ntiles; ++t) {
-      // warp-uniform outcome: the TMEM load below is warp-collective
-      if (!__all_sync(FULL, mbar_wait(bar_ready + 8 * t, 0, abort))) {
+    __syncwarp();
+  } else if (warp >= EPI_W0 && warp < SEL_W0) {
+    // ---- epilogue ------------------------------------------------------------
+    const int quad = warp & 3;                  // TMEM lane quadrant of this warp
+    const int half = (warp - EPI_W0) >> 2;      // tiles t with t % 2 == half
+    const int ew = warp - EPI_W0;               // 0..7
+    const int et = tid - 32 * EPI_W0;           // 0..255
+    // Phase parity of each ready barrier (TMEM tile slot).  A unit's last
+    // rank may score fewer pages than the others, so slots are not used
+    // once per unit: follow every use, in the MMA issuer's order.
+    uint32_t ready_par = 0u;
+    for (int kk = 0;; ++kk) {
+      const int w = g0 + kk * nclus;
+      if (w >= total_units || *abort) break;
+      const UnitInfo u = unit_info(a, w, crank);
+      const int b = kk % NBUF, p = kk & 1;
+      const int ntiles = 2 * u.npg;
+      // online softmax statistics (stat = set * ROWS + row) of this warp's tiles
+      float m[NSTAT], sm[NSTAT];
+#pragma unroll
+      for (int e = 0; e < NSTAT; ++e) {
+        m[e] = NEG;
+        sm[e] = 0.f;
+      }
+      bool ok = true;
+      for (int t = half; t < ntiles; t += 2) {
+        // warp-uniform outcome: the TMEM load below is warp-collective
+        const int slot = b * TPB + t;
+        if (!(ok = __all_sync(FULL, mbar_wait(bar_ready + 8 * slot, (ready_par >> slot) & 1u, abort)))) break;
+        tc_fence_after();
+        float z[ROWS];
+        tile_logits<T::NB, ROWS>(tmem, quad, slot * T::NB, z);
+        const int i = u.j0 * PAGE + t * 128 + 32 * quad + lane;
+        if (i < u.ndem) {
+#pragma unroll
+          for (int r = 0; r < ROWS; ++r) online(m[r], sm[r], z[r]);
+        } else if (i < u.ncmp) {
+#pragma unroll
+          for (int r = 0; r < ROWS; ++r) online(m[ROWS + r], sm[ROWS + r], z[r]);
+        }
+      }
+      ready_par ^= ((1u << ntiles) - 1u) << (b * TPB);
+      if (!ok) {
         if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
         *abort = 1;
         break;
       }
-      tc_fence_after();
-      float z[ROWS];
-      tile_logits<T::NB, ROWS>(tmem, quad, t, z);
-      const int i = u.j0 * PAGE + t * 128 + 32 * quad + lane;
-      if (i < u.ndem) {
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r) online(m[0][r], sm[0][r], z[r]);
-      } else if (i < u.ncmp) {
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r) online(m[1][r], sm[1][r], z[r]);
+      {
+        float om, os;
+        int idx;
+        warp_reduce_stats<NSTAT>(m, sm, lane, om, os, idx);
+        if ((lane & (32 / NSTAT - 1)) == 0) part[ew * 16 + idx] = XStat{om, os};
       }
-    }
+      epi_sync();
+      // exchange with every rank: 8 bytes per statistic per rank
+      if (et < NSTAT) {
+        float cm = NEG, cs = 0.f;
 #pragma unroll
-    for (int set = 0; set < 2; ++set)
-#pragma unroll
-      for (int r = 0; r < ROWS; ++r) {
-        warp_combine(m[set][r], sm[set][r]);
-        if (lane == 0) {
-          part[((quad * 2 + set) * ROWS + r) * 2 + 0] = m[set][r];
-          part[((quad * 2 + set) * ROWS + r) * 2 + 1] = sm[set][r];
+        for (int q = 0; q < EPI_NW; ++q) combine(cm, cs, part[q * 16 + et].m, part[q * 16 + et].s);
+        const uint64_t v = ((uint64_t)__float_as_uint(cs) << 32) | __float_as_uint(cm);
+        const uint32_t dst = smem_u32(xg + (p * 16 + crank) * 16 + et);
+        for (int c = 0; c < C; ++c) st_async_b64(dst, bar_xg + 8 * p, c, v);
+      }
+      if (et == 0) mbar_expect_tx(bar_xg + 8 * p, (uint32_t)(C * NSTAT * 8));
+      if (!(ok = mbar_wait(bar_xg + 8 * p, (kk >> 1) & 1, abort))) {
+        if (et == 0) atomicOr(a.err, ERR_TIMEOUT);
+        *abort = 1;
+        break;
+      }
+      // merge into base-2 log-sum-exps over C_t and over C_cmp
+      if (et < ROWS) {
+        const XStat* xs = xg + p * 16 * 16;
+        float md, sd, mt, stl;
+        merge_ranks(&xs[et].m, &xs[et].s, C, 32, &md, &sd);
+        merge_ranks(&xs[ROWS + et].m, &xs[ROWS + et].s, C, 32, &mt, &stl);
+        lse_pair(md, sd, mt, stl, lse_dem + et, lse_cmp + et);
+      }
+      epi_sync();
+      // a^S, a^L and the importance of every key of this warp's tiles
+      {
+        float* sc = a.scores + u.rq.score_off + (size_t)u.unit * u.ncmp;
+        float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
+        for (int t = half; t < ntiles; t += 2) {
+          float z[ROWS];
+          tile_logits<T::NB, ROWS>(tmem, quad, (b * TPB + t) * T::NB, z);
+          key_values<ROWS>(z, u.j0 * PAGE + t * 128 + 32 * quad + lane, u.ndem, u.ncmp, lse_dem, lse_cmp, av, sc);
         }
       }
-  }
-  __syncthreads();
-  float cm = -INFINITY, cs = 0.f;
-  if (tid < 2 * ROWS) {
-    for (int q = 0; q < 4; ++q) combine(cm, cs, part[(q * 2 * ROWS + tid) * 2], part[(q * 2 * ROWS + tid) * 2 + 1]);
-  }
-  push_stats<ROWS>(xg, u.crank, a.C, cm, cs);
-  merge_stats<ROWS>(xg, a.C, lse_dem, lse_cmp);
-  __syncthreads();
-
-  // ---- values: a^S, a^L and the importance of every key ----------------------
-  {
-    float* sc = a.scores + u.rq.score_off + (size_t)u.unit * u.ncmp;
-    float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
-    const int quad = warp & 3;
-    for (int t = warp >> 2; t < ntiles; t += 2) {
-      if (!__all_sync(FULL, mbar_wait(bar_ready + 8 * t, 0, abort))) break;
-      tc_fence_after();
-      float z[ROWS];
-      tile_logits<T::NB, ROWS>(tmem, quad, t, z);
-      key_values<ROWS>(z, u.j0 * PAGE + t * 128 + 32 * quad + lane, u.ndem, u.ncmp, lse_dem, lse_cmp, av, sc);
+      tc_fence_before();
+      epi_sync();
+      if (et == 0) {
+        mbar_arrive(bar_tfree + 8 * b);  // TMEM buffer b may take the unit after next
+        // the CTA's a-values (ordered by the barrier above) before its ticket
+        __threadfence();
+        atomicAdd(a.tickets + (size_t)u.r * units + u.unit, 1u);
+        if (kk % C == crank) {
+          // this rank computes the unit's D_p: queue it for the selector warps
+          const long long t0 = clock64();
+          while (*q_head - *q_tail >= QLEN) {
+            if (*abort || clock64() - t0 > kWaitLimit) {
+              atomicOr(a.err, ERR_TIMEOUT);
+              *abort = 1;
+              break;
+            }
+          }
+          if (!*abort) {
+            queue[*q_head % QLEN] = w;
+            __threadfence_block();
+            *q_head = *q_head + 1;
+          }
+        }
+      }
+    }
+    if (et == 0) {
+      __threadfence_block();
+      *q_done = 1;
+    }
+  } else if (warp >= SEL_W0) {
+    // ---- selector ------------------------------------------------------------
+    const int st = tid - 32 * SEL_W0;
+    uint32_t sel_par = 0u;  // phase of the staging barrier
+    while (true) {
+      if (st == 0) {
+        int item = -1;
+        const long long t0 = clock64();
+        while (true) {
+          const int h = *q_head, tl = *q_tail;
+          if (h != tl) {
+            item = queue[tl % QLEN];
+            break;
+          }
+          if (*q_done) {
+            __threadfence_block();
+            if (*q_head == tl) break;
+            continue;
+          }
+          if (*abort) break;
+          if (clock64() - t0 > kWaitLimit) {
+            atomicOr(a.err, ERR_TIMEOUT);
+            *abort = 1;
+            break;
+          }
+          __nanosleep(200);
+        }
+        if (item >= 0) {
+          // wait until every rank of the cluster has written its a-values
+          const UnitInfo u = unit_info(a, item, 0);
+          const unsigned* tk = a.tickets + (size_t)u.r * units + u.unit;
+          const long long t1 = clock64();
+          while (ld_acquire(tk) < (unsigned)C) {
+            if (*abort || clock64() - t1 > kWaitLimit) {
+              atomicOr(a.err, ERR_TIMEOUT);
+              *abort = 1;
+              item = -1;
+              break;
+            }
+            __nanosleep(100);
+          }
+        }
+        *sel_item = item;
+      }
+      sel_sync<SEL_NTH, BAR_SEL>();
+      const int w = *sel_item;
+      if (w < 0) break;
+      const UnitInfo u = unit_info(a, w, 0);
+      unsigned k = 0;
+      if (u.ndem > 0) {
+        const float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
+        k = coverage_demand<SEL_NTH, BAR_SEL>(av, u.ndem, a.p, selbuf, sel_cap, dps, a.err, st, bar_sel, sel_par);
+        if (2 * u.ndem <= sel_cap) sel_par ^= 1u;
+      }
+      write_demand(a, u.r, u.unit, st, k);
+      sel_sync<SEL_NTH, BAR_SEL>();
+      if (st == 0) *q_tail = *q_tail + 1;
     }
   }
+  (void)flag;
+  (void)phys;
+
+  // ---- teardown ----------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no rank leaves while a peer may still write into it
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
   }
+}
 
-  // ---- D_p, by the unit's last CTA ---------------------------------------------
-  if (!last_of_unit(a, u, flag)) return;
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  unsigned k = 0;
-  if (u.ndem > 0) {
-    DpSmem* dps = reinterpret_cast<DpSmem*>(smem + S::STAGE);
-    const size_t off = (sizeof(DpSmem) + 15) & ~size_t(15);
-    unsigned* buf = reinterpret_cast<unsigned*>(smem + S::STAGE + off);
-    const int cap = (int)(((size_t)T::NSTAGE * T::TILE_BYTES - off) / 4);
-    const float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
-    k = coverage_demand(av, u.ndem, a.p, buf, cap, dps, a.err);
+// Clusters of this shape that fit on the GPU at once.
+template <typename K>
+int max_clusters(K kern, int C, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)C * 152, 1, 1);
+  cfg.blockDim = dim3(NTHR, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 1;
   }
-  write_demand(a, u, k);
+  return n;
 }
 
 template <int D, int ROWS>
 cudaError_t launch_t(const DemandArgs& a, cudaStream_t s) {
   using T = TcCfg<D, ROWS>;
-  if (2 * a.ppc > T::MAX_TILES) return cudaErrorInvalidValue;
-  // TMEM columns per CTA (a power of two >= 32); the CTAs an SM can hold must
-  // never ask for more than its 512 columns, or a blocked allocation could
-  // wait on a CTA that itself waits on its cluster.  Shared memory is padded
-  // so that at most 512 / ncols CTAs fit on an SM.
-  int ncols = 2 * a.ppc * T::NB;
-  if (ncols < 32) ncols = 32;
-  if (ncols & (ncols - 1)) return cudaErrorInvalidValue;
-  const int fit = 512 / ncols;  // CTAs whose TMEM fits at once
-  int dev = 0, sm_total = 0, reserved = 0, max_optin = 0;
+  using S = TcSmem<D, ROWS>;
+  if (2 * a.ppc * T::NB > 512) return cudaErrorInvalidValue;  // one unit's tiles must fit TMEM
+  int dev = 0, max_optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_total, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  size_t smem = TcSmem<D, ROWS>::BYTES;
-  // (fit + 1) CTAs of this size must not fit in one SM
-  const size_t floor_bytes = (size_t)sm_total / (size_t)(fit + 1) - (size_t)reserved + 16;
-  if (smem < floor_bytes) smem = floor_bytes;
-  if (smem > (size_t)max_optin) return cudaErrorInvalidValue;
-  return launch_cluster(k_demand_tc<D, ROWS>, a, smem, s);
+  // the whole opt-in shared memory: one CTA per SM, so TMEM (512 columns)
+  // and the select buffer are the CTA's alone
+  const size_t smem = (size_t)max_optin;
+  if (smem < S::MIN_BYTES) return cudaErrorInvalidValue;
+  auto kern = k_demand_tc<D, ROWS>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (a.C > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int total = a.n_work * a.L * a.Hkv;
+  static int fit_cache[17] = {};  // per kernel instantiation and cluster size
+  if (!fit_cache[a.C]) fit_cache[a.C] = max_clusters(kern, a.C, smem);
+  int nclus = fit_cache[a.C];
+  if (nclus > total) nclus = total;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.C * nclus), 1, 1);
+  cfg.blockDim = dim3(NTHR, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, total, (int)smem);
 }
 
 }  // namespace
