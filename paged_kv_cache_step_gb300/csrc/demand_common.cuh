@@ -237,9 +237,10 @@ __device__ __forceinline__ void merge_stats(const StatXchg* xg, int csize, float
 // ---- per-key epilogue ----------------------------------------------------
 // z[ROWS] base-2 logits of key i (rows x * G + g).  Writes a^S, a^L for
 // i < ndem and the base-2 log importance for i < ncmp.
+// a_out (optional) receives a^S, a^L when i < ndem.
 template <int ROWS>
 __device__ __forceinline__ void key_values(const float* z, int i, int ndem, int ncmp, const float* lse_dem,
-                                           const float* lse_cmp, float* av, float* sc) {
+                                           const float* lse_cmp, float* av, float* sc, float* a_out = nullptr) {
   constexpr int G = ROWS / 2;
   if (i < ndem) {
 #pragma unroll
@@ -247,7 +248,9 @@ __device__ __forceinline__ void key_values(const float* z, int i, int ndem, int 
       float s = 0.f;
 #pragma unroll
       for (int g = 0; g < G; ++g) s += ex2(z[x * G + g] - lse_dem[x * G + g]);
-      __stcg(av + (size_t)x * ndem + i, s * (1.0f / G));
+      s *= 1.0f / G;
+      __stcg(av + (size_t)x * ndem + i, s);
+      if (a_out) a_out[x] = s;
     }
   }
   if (i < ncmp) {
@@ -410,11 +413,20 @@ __device__ __forceinline__ void pick_digit(DpSmem* sm, int shift, bool first, do
     }
   }
   if (first) sel_sync<NTH, BAR>();
+  // Every thread reads the state before the crossing thread updates it.
+  unsigned long long needs[2];
+  bool dones[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    dones[x] = sm->st[x].done != 0;
+    needs[x] = sm->st[x].target - sm->st[x].mass_above;
+  }
+  sel_sync<NTH, BAR>();
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
     DpState& st = sm->st[x];
-    if (st.done) continue;
-    const unsigned long long need = st.target - st.mass_above;
+    if (dones[x]) continue;
+    const unsigned long long need = needs[x];
     const unsigned long long incl = base_m[x] + im[x], excl = incl - lm[x];
     const bool last = tid == NTH - 1;
     if ((excl < need && need <= incl) || (last && incl < need)) {

@@ -63,6 +63,7 @@ CONFIGS = {
                               "concentrated units"),
     "stream256": (5, LLAMA8B, "256-request continuous-batching stream with "
                               "32-page shared prefixes"),
+    "custom": (6, TINY, "any shape and request sizes (edge cases)"),
 }
 
 TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
@@ -271,11 +272,15 @@ def _llama_single(device, num_pages: int = 64, P: int = 32, **_):
 
 
 def _batch(device, name="batch64", shape=LLAMA8B, n=64, p_lo=4, p_hi=128,
-           spare_per_req=2, conc_prob=None, **_):
+           spare_per_req=2, conc_prob=None, sizes=None, seed_xor=0, **_):
     sh = shape
     b = 256
-    gen, hgen = _gens(device, config_seed(name))
-    sizes = torch.randint(p_lo, p_hi + 1, (n,), generator=hgen).tolist()
+    gen, hgen = _gens(device, config_seed(name) ^ seed_xor)
+    if sizes is None:
+        sizes = torch.randint(p_lo, p_hi + 1, (n,), generator=hgen).tolist()
+    else:
+        sizes = list(sizes)
+        n = len(sizes)
     num_pages = sum(sizes) + spare_per_req * n
     perm = torch.randperm(num_pages, generator=hgen).tolist()
     bts, off = [], 0
@@ -323,4 +328,7 @@ def make_workload(name: str, device="cpu", **kw) -> Workload:
         kw.setdefault("spare_per_req", 1)
         return _batch(device, name="qwen3_8b", shape=QWEN3_8B, conc_prob=0.3,
                       **kw)
+    if name == "custom":
+        # explicit shape and request sizes: kw shape=ModelShape, sizes=[P, ...]
+        return _batch(device, name="custom", **kw)
     raise KeyError(name)

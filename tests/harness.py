@@ -116,6 +116,20 @@ def cache_f64(cache: torch.Tensor, pages) -> dict:
     return {pg: sub[:, i] for i, pg in enumerate(pages)}
 
 
+def unit_keys_dev(cache: torch.Tensor, table, layer: int, h: int) -> np.ndarray:
+    """float64 keys (or values) of one (layer, KV head) in logical order,
+    copied from the device cache without touching the other units."""
+    idx = torch.as_tensor(list(table), device=cache.device, dtype=torch.long)
+    sub = cache[layer].index_select(0, idx)[:, h]          # [P][b][d]
+    return sub.double().cpu().numpy().reshape(len(table) * PAGE, -1)
+
+
+def oracle_unit_dev(qt, cache: torch.Tensor, table, layer, h, G, p=0.99, recent=16):
+    qt_unit = qt[layer][:, h * G:(h + 1) * G, :]
+    keys = unit_keys_dev(cache, table, layer, h)
+    return og.unit_boundary(qt_unit, keys, len(table), PAGE, recent, p)
+
+
 def unit_keys(pages_f64: dict, table, layer: int, h: int):
     return np.concatenate([pages_f64[pg][layer, h] for pg in table], axis=0)
 
