@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -53,6 +54,37 @@ def _peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+KERNEL_OF = {"boundary_demand": "k_demand_tc", "compress_hold": "k_compress"}
+
+
+def _sources_sha() -> str:
+    """sha256 over the kernel sources (file name and bytes, sorted by name)."""
+    import hashlib
+    d = os.path.join(ROOT, "paged_kv_cache_step_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        h.update(f.encode())
+        h.update(b"\0")
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _traffic(kernel: str, bytes_per_launch: float):
+    """DRAM bytes per launch from the committed ncu capture, scaled by the
+    launch's algorithmic bytes; None when the kernel sources have changed
+    since the capture or no capture exists."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(KERNEL_OF.get(kernel, ""), None)
+    except Exception:
+        return None
+    if not rec or rec.get("source_sha256") != _sources_sha():
+        return None
+    ratio = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["algorithmic_bytes"]
+    return ratio * bytes_per_launch
 
 
 def _dist():
@@ -218,8 +250,8 @@ def run_gpu(args, world, rank, local):
     moved0 = _moved(gp, s.ctx)
     if world > 1:
         torch.distributed.barrier()
-    clocks = Clocks(local, os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv")
-                    if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clock_file = os.path.join(tempfile.gettempdir(), f"growpage_bench_clocks_{os.getpid()}_r{rank}.csv")
+    clocks = Clocks(local, clock_file)
     times = []
     scan_bytes = 0
     for _ in range(args.steps):
@@ -309,7 +341,8 @@ def run_gpu(args, world, rank, local):
         "kv_frac": kv_gbs / peak,
         "scan_bytes": scan_bytes, "compaction_bytes": comp_bytes,
         "actions": s.actions,
-        "roofline": dict(rl[dom], kernel=dom, peak_source=peak_src, traffic=None) if dom else None,
+        "roofline": dict(rl[dom], kernel=dom, peak_source=peak_src,
+                         traffic=_traffic(dom, rl[dom]["bytes_per_launch"])) if dom else None,
         "kernels": {k: dict(v, **({"frac": rl[k]["frac"], "achieved_gbs": rl[k]["achieved"]}
                                   if k in rl else {})) for k, v in kern.items()},
         "gpu_launches": launches,

@@ -202,13 +202,13 @@ gp_status gp_boundary_demand(gp_ctx* ctx, int32_t n, const gp_request* reqs,
  * out-of-memory error and no cudaMalloc/cudaFree synchronises the device
  * mid-flight.  The paper has no counterpart to this call.
  * It calls no cudaMalloc, cudaFree or other allocating routine: every
- * temporary (request descriptors, block tables, calibrated summaries,
- * importance values, per-unit D_p and their sums) lives in one file-scope
- * device array of 64 MiB that every GPU loading the library holds until the
- * process exits.  A call needing more (roughly: the sum over requests of
- * L * Hkv * (P * b - R) * 4 bytes, plus about 1 MiB per request) is
- * rejected with GP_ERR_INVALID and a message naming the size; n is at most
- * 512.  On the first call on a device, with that device current, the
+ * temporary (request descriptors, block tables, calibrated summaries and
+ * their tensor-core operands, importance values, a-values, arrival tickets,
+ * per-unit D_p and their sums) lives in one file-scope device array of
+ * 64 MiB that every GPU loading the library holds until the process exits.
+ * A call needing more (roughly: the sum over requests of
+ * 12 * L * Hkv * P * b bytes plus L * Hkv * 9 KiB) is rejected with
+ * GP_ERR_INVALID and a message naming the size; n is at most 512.  On the first call on a device, with that device current, the
  * array's address is looked up once (cudaGetSymbolAddress); make that first
  * call before any stream capture.  All calls share the array and its host
  * staging, which keep the last call's contents: calls that overlap on the

@@ -11,8 +11,7 @@ arXiv 2609.03494), in float64, with no blocking, fusion or reordering beyond
 what the definition states.  Library primitives used as single steps: matrix
 products (numpy), a sort (numpy), cumulative sums (numpy).
 
-Readings of the paper where it is silent or ambiguous (each also listed in
-DESIGN.md):
+Readings of the paper where it is silent or ambiguous:
 
 * EMA convention: the stored beta is the decay, the weight on the previous
   summary (Sec. 3.2, Eq. 6); beta_S = 0.9 < beta_L = 0.999, so the short

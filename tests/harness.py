@@ -145,7 +145,7 @@ def oracle_unit(qt, pages_f64, table, layer, h, G, p=0.99, recent=16):
 # ---------------------------------------------------------------------------
 
 def dp_ok(gpu_k: int, a_oracle: np.ndarray, p: float):
-    """D_p within the benchmark spec's tolerance.  Returns (ok, detail)."""
+    """D_p within the stated tolerance.  Returns (ok, detail)."""
     k, before, at = og.coverage_demand_detail(a_oracle, p)
     if gpu_k == k:
         return True, ""
