@@ -330,6 +330,12 @@ __device__ __forceinline__ unsigned long long bin_mass(const DpSmem* sm, int x, 
 // as zero.
 __device__ __forceinline__ unsigned sel_bits(unsigned u) { return u >= 0x40000000u ? 0u : u; }
 
+// Values below 2^-41 (biased exponent <= 85) have exactly zero fixed-point
+// mass.  They lie in first-digit bins strictly below any bin holding a value
+// of positive mass, and the threshold bin always holds one, so they never
+// reach the count or mass above the threshold: the histograms skip them.
+constexpr unsigned MIN_MASS_BITS = 86u << 23;
+
 template <int NTH>
 __device__ __forceinline__ void clear_hist(DpSmem* sm, int tid) {
   for (int k = tid; k < 2 * SEL_BINS; k += NTH) {
@@ -470,6 +476,7 @@ __device__ __forceinline__ bool sel_bar_try(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void warp_append4(const unsigned (&v)[4], const bool (&keep)[4], unsigned* dst,
                                              unsigned* count, int lane) {
   const unsigned c = (unsigned)keep[0] + keep[1] + keep[2] + keep[3];
+  if (!__any_sync(FULL, c != 0u)) return;
   unsigned incl = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -572,7 +579,8 @@ __device__ __forceinline__ unsigned coverage_demand(const float* av, int ndem, d
         const unsigned w[4] = {sel_bits(v[j].x), sel_bits(v[j].y), sel_bits(v[j].z), sel_bits(v[j].w)};
         if (i0 + j * NTH + tid < n4) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) hist_add(sm, x, (int)(w[k] >> 20), fixed40(w[k]));
+          for (int k = 0; k < 4; ++k)
+            if (w[k] >= MIN_MASS_BITS) hist_add(sm, x, (int)(w[k] >> 20), fixed40(w[k]));
         }
       }
     }

@@ -94,9 +94,11 @@ inline cudaError_t launch_demand(const DemandArgs& a, cudaStream_t s) {
 }
 
 // How a request of P pages is split: kernel variant, pages per CTA (ppc) and
-// CTAs per cluster (C).  The tensor-core variant keeps a CTA's logits in
-// TMEM (32 columns per 128 keys, 512 columns per SM), so it takes up to 8
-// pages per CTA and 16 CTAs per cluster: P <= 128.
+// CTAs per cluster (C).  The tensor-core variant keeps two units of a CTA's
+// logits in TMEM (2G columns per 128 keys) beside its accumulator slots, so
+// it takes up to 8 pages per CTA and 16 CTAs per cluster: P <= 128.  Eight
+// pages per CTA keep clusters small, and small clusters fill the GPCs
+// (clusters of 4 occupy 144 of 152 SMs, clusters of 8 only 120).
 struct DemandPlan {
   int variant, ppc, C;
 };
@@ -104,7 +106,7 @@ inline DemandPlan demand_plan(int P, bool tc_ok) {
   DemandPlan pl;
   if (tc_ok && P <= 128) {
     pl.variant = DEMAND_TC;
-    pl.ppc = P <= 64 ? 4 : 8;
+    pl.ppc = 8;
   } else {
     pl.variant = DEMAND_FFMA;
     pl.ppc = P <= 128 ? 8 : 16;

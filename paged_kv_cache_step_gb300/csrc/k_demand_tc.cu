@@ -21,12 +21,17 @@
 //   warp 0      producer: per unit, the B operand (bulk copy) and the K tiles
 //               (128 keys x d, box 64 x 128 with the 128-byte swizzle)
 //               through an NSTAGE mbarrier ring, running ahead across units;
-//   warp 1      MMA issuer: tcgen05.mma into one of two TMEM buffers (a
-//               tile's accumulator is 128 lanes x N columns), so the next
-//               unit's scan proceeds while the epilogue reads the last one;
+//   warp 1      MMA issuer: tcgen05.mma into a ring of TMEM accumulator
+//               slots (a tile's accumulator is 128 lanes x N columns); a slot
+//               is reused once the epilogue has read it, so the scan runs on
+//               while the epilogue finishes the previous unit;
 //   warps 2..9  epilogue (warp w reads TMEM lane quadrant w % 4; two warps
-//               per quadrant split the tiles): online softmax statistics as
-//               tiles finish, a reduce-scatter butterfly over the warp, an
+//               per quadrant split the tiles): as tiles finish, it sums the
+//               three partial products into each key's 2G logits, stores
+//               them in a compact per-unit TMEM region (2G columns per 128
+//               keys, two units deep), releases the accumulator slot and
+//               folds online softmax statistics; then a reduce-scatter
+//               butterfly over the warp, an
 //               exchange with every rank (st.async into the peers' shared
 //               memory, completing on their mbarriers), the merge, then a^S,
 //               a^L and the importance of every key to global memory, and
@@ -67,7 +72,10 @@ struct TcCfg {
   static constexpr int BQ_BYTES = HALVES * NB * 128;
   static constexpr int KSTEPS = D / 16;
   static constexpr int NSTAGE = (96 * 1024) / TILE_BYTES;  // 96 KiB of K in flight per SM
-  static constexpr int MAX_READY = 512 / NB;             // tile slots of TMEM
+  static constexpr int TPU = 16;                         // tiles per unit and CTA at most (8 pages)
+  static constexpr int WSLOTS = (512 - 2 * TPU * ROWS) / NB;  // accumulator slots; the rest holds
+  static constexpr int CBASE = WSLOTS * NB;              // two units of compact logits from here
+  static_assert(CBASE + 2 * TPU * ROWS <= 512 && WSLOTS >= 4, "TMEM layout");
   static constexpr uint32_t IDESC = (1u << 4)        // D: f32
                                     | (1u << 7)      // A: bf16
                                     | (1u << 10)     // B: bf16
@@ -178,6 +186,48 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+template <int R>
+__device__ __forceinline__ void tmem_st_rows(uint32_t taddr, const float* z);
+template <>
+__device__ __forceinline__ void tmem_st_rows<8>(uint32_t taddr, const float* z) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(__float_as_uint(z[0])), "r"(__float_as_uint(z[1])), "r"(__float_as_uint(z[2])),
+               "r"(__float_as_uint(z[3])), "r"(__float_as_uint(z[4])), "r"(__float_as_uint(z[5])),
+               "r"(__float_as_uint(z[6])), "r"(__float_as_uint(z[7]))
+               : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_rows<4>(uint32_t taddr, const float* z) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+               "r"(__float_as_uint(z[0])), "r"(__float_as_uint(z[1])), "r"(__float_as_uint(z[2])),
+               "r"(__float_as_uint(z[3]))
+               : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+template <int R>
+__device__ __forceinline__ void tmem_ld_rows(uint32_t taddr, float* z);
+template <>
+__device__ __forceinline__ void tmem_ld_rows<8>(uint32_t taddr, float* z) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) z[i] = __uint_as_float(r[i]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_rows<4>(uint32_t taddr, float* z) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) z[i] = __uint_as_float(r[i]);
+}
+
 // Logits of the key in this thread's lane of the tile at TMEM column `col`.
 template <int NB, int ROWS>
 __device__ __forceinline__ void tile_logits(uint32_t tmem, int quad, int col, float* z) {
@@ -221,8 +271,8 @@ struct TcSmem {
   static constexpr size_t BQ = STAGE + (size_t)T::NSTAGE * T::TILE_BYTES;  // 2 buffers
   static constexpr size_t XG = BQ + 2 * (size_t)T::BQ_BYTES;               // XStat [2][16][16]
   static constexpr size_t BARS = XG + sizeof(XStat) * 2 * 16 * 16;
-  // full[NSTAGE], empty[NSTAGE], bqfull[2], bqempty[2], tfree[2], xbar[2], mmadone, sel, ready[MAX_READY]
-  static constexpr int NBARS = 2 * T::NSTAGE + 10 + T::MAX_READY;
+  // full[NSTAGE], empty[NSTAGE], bqfull[2], bqempty[2], xbar[2], mmadone, sel, ready[W], wfree[W]
+  static constexpr int NBARS = 2 * T::NSTAGE + 8 + 2 * T::WSLOTS;
   static constexpr size_t PART = BARS + 8 * (size_t)NBARS;                 // [EPI_NW][16] XStat
   static constexpr size_t LSE = PART + sizeof(XStat) * EPI_NW * 16;        // lse_dem[8], lse_cmp[8]
   static constexpr size_t MISC = LSE + sizeof(float) * 16;                 // ints, see kernel
@@ -265,11 +315,11 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
   const uint32_t bar_empty = bar_full + 8 * T::NSTAGE;
   const uint32_t bar_bqfull = bar_empty + 8 * T::NSTAGE;
   const uint32_t bar_bqempty = bar_bqfull + 16;
-  const uint32_t bar_tfree = bar_bqempty + 16;
-  const uint32_t bar_xg = bar_tfree + 16;
+  const uint32_t bar_xg = bar_bqempty + 16;
   const uint32_t bar_mmadone = bar_xg + 16;
   const uint32_t bar_sel = bar_mmadone + 8;
   const uint32_t bar_ready = bar_sel + 8;
+  const uint32_t bar_wfree = bar_ready + 8 * T::WSLOTS;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = a.C;
@@ -277,8 +327,6 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
   const int g0 = (int)(blockIdx.x / (unsigned)C);
   const int nclus = (int)(gridDim.x / (unsigned)C);
   const int units = a.L * a.Hkv;
-  const int TPB = 2 * a.ppc;                                  // tiles per unit and TMEM buffer
-  const int NBUF = (2 * TPB * T::NB <= 512) ? 2 : 1;
 
   if (tid == 0) {
     for (int s = 0; s < T::NSTAGE; ++s) {
@@ -288,12 +336,14 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_bqfull + 8 * b, 1);
       mbar_init(bar_bqempty + 8 * b, 1);
-      mbar_init(bar_tfree + 8 * b, 1);
       mbar_init(bar_xg + 8 * b, 1);
     }
     mbar_init(bar_mmadone, 1);
     mbar_init(bar_sel, 1);
-    for (int t = 0; t < T::MAX_READY; ++t) mbar_init(bar_ready + 8 * t, 1);
+    for (int t = 0; t < T::WSLOTS; ++t) {
+      mbar_init(bar_ready + 8 * t, 1);
+      mbar_init(bar_wfree + 8 * t, 4);  // the four quadrant warps that read the slot
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *abort = 0;
     *q_head = 0;
@@ -310,6 +360,50 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
   cluster_sync_all();  // barriers of every rank initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+
+  // The next queued unit whose D_p this rank computes, once every rank of the
+  // cluster has written its a-values; -1 when the queue is empty and the
+  // epilogue has finished (or stop_at_done and the epilogue has finished),
+  // or on abort.  Called by one thread.
+  auto take_item = [&](bool stop_at_done) -> int {
+    int item = -1;
+    const long long t0 = clock64();
+    while (true) {
+      const int h = *q_head, tl = *q_tail;
+      if (*q_done && stop_at_done) break;
+      if (h != tl) {
+        item = queue[tl % QLEN];
+        break;
+      }
+      if (*q_done) {
+        __threadfence_block();
+        if (*q_head == tl) break;
+        continue;
+      }
+      if (*abort) break;
+      if (clock64() - t0 > kWaitLimit) {
+        atomicOr(a.err, ERR_TIMEOUT);
+        *abort = 1;
+        break;
+      }
+      __nanosleep(200);
+    }
+    if (item >= 0) {
+      const UnitInfo u = unit_info(a, item, 0);
+      const unsigned* tk = a.tickets + (size_t)u.r * units + u.unit;
+      const long long t1 = clock64();
+      while (ld_acquire(tk) < (unsigned)C) {
+        if (*abort || clock64() - t1 > kWaitLimit) {
+          atomicOr(a.err, ERR_TIMEOUT);
+          *abort = 1;
+          item = -1;
+          break;
+        }
+        __nanosleep(100);
+      }
+    }
+    return item;
+  };
 
   if (warp == 0) {
     // ---- producer --------------------------------------------------------
@@ -369,16 +463,16 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
         const int w = g0 + kk * nclus;
         if (w >= total_units) break;
         const UnitInfo u = unit_info(a, w, crank);
-        const int b = kk % NBUF, b2 = kk & 1;
-        if (kk >= NBUF && !(ok = mbar_wait(bar_tfree + 8 * b, ((kk / NBUF) - 1) & 1, abort))) break;
+        const int b2 = kk & 1;
         if (!(ok = mbar_wait(bar_bqfull + 8 * b2, (kk >> 1) & 1, abort))) break;
         const uint32_t b0 = sbase + (uint32_t)(S::BQ + (size_t)b2 * T::BQ_BYTES);
         for (int t = 0; t < 2 * u.npg; ++t, ++gt) {
-          const int s = gt % T::NSTAGE;
+          const int s = gt % T::NSTAGE, ws = gt % T::WSLOTS;
+          if (gt >= T::WSLOTS && !(ok = mbar_wait(bar_wfree + 8 * ws, ((gt / T::WSLOTS) - 1) & 1, abort))) break;
           if (!(ok = mbar_wait(bar_full + 8 * s, (gt / T::NSTAGE) & 1, abort))) break;
           tc_fence_after();
           const uint32_t a0 = sbase + (uint32_t)(S::STAGE + (size_t)s * T::TILE_BYTES);
-          const uint32_t col = (uint32_t)((b * TPB + t) * T::NB);
+          const uint32_t col = (uint32_t)(ws * T::NB);
 #pragma unroll
           for (int k = 0; k < T::KSTEPS; ++k) {
             const uint32_t ad = a0 + (k >> 2) * T::HALF_BYTES + (k & 3) * 32;
@@ -386,7 +480,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
             mma_f16(tmem + col, sw128_desc(ad), sw128_desc(bd), T::IDESC, k > 0 ? 1u : 0u);
           }
           mma_commit(bar_empty + 8 * s);
-          mma_commit(bar_ready + 8 * (b * TPB + t));
+          mma_commit(bar_ready + 8 * ws);
         }
         if (ok) mma_commit(bar_bqempty + 8 * b2);
       }
@@ -406,16 +500,15 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     const int half = (warp - EPI_W0) >> 2;      // tiles t with t % 2 == half
     const int ew = warp - EPI_W0;               // 0..7
     const int et = tid - 32 * EPI_W0;           // 0..255
-    // Phase parity of each ready barrier (TMEM tile slot).  A unit's last
-    // rank may score fewer pages than the others, so slots are not used
-    // once per unit: follow every use, in the MMA issuer's order.
-    uint32_t ready_par = 0u;
+    int gt0 = 0;  // global index of the unit's first tile, in the MMA issuer's order
     for (int kk = 0;; ++kk) {
       const int w = g0 + kk * nclus;
       if (w >= total_units || *abort) break;
       const UnitInfo u = unit_info(a, w, crank);
-      const int b = kk % NBUF, p = kk & 1;
+      const int p = kk & 1;
       const int ntiles = 2 * u.npg;
+      const uint32_t lanes = (uint32_t)(32 * quad) << 16;
+      const uint32_t cbase = tmem + lanes + (uint32_t)(T::CBASE + p * T::TPU * ROWS);  // compact logits
       // online softmax statistics (stat = set * ROWS + row) of this warp's tiles
       float m[NSTAT], sm[NSTAT];
 #pragma unroll
@@ -426,11 +519,16 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
       bool ok = true;
       for (int t = half; t < ntiles; t += 2) {
         // warp-uniform outcome: the TMEM load below is warp-collective
-        const int slot = b * TPB + t;
-        if (!(ok = __all_sync(FULL, mbar_wait(bar_ready + 8 * slot, (ready_par >> slot) & 1u, abort)))) break;
+        const int gt = gt0 + t, ws = gt % T::WSLOTS;
+        if (!(ok = __all_sync(FULL, mbar_wait(bar_ready + 8 * ws, (gt / T::WSLOTS) & 1, abort)))) break;
         tc_fence_after();
         float z[ROWS];
-        tile_logits<T::NB, ROWS>(tmem, quad, slot * T::NB, z);
+        tile_logits<T::NB, ROWS>(tmem, quad, ws * T::NB, z);
+        // keep the logits, hand the accumulator slot back to the MMA issuer
+        tmem_st_rows<ROWS>(cbase + (uint32_t)(t * ROWS), z);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_wfree + 8 * ws);
         const int i = u.j0 * PAGE + t * 128 + 32 * quad + lane;
         if (i < u.ndem) {
 #pragma unroll
@@ -440,7 +538,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
           for (int r = 0; r < ROWS; ++r) online(m[ROWS + r], sm[ROWS + r], z[r]);
         }
       }
-      ready_par ^= ((1u << ntiles) - 1u) << (b * TPB);
+      gt0 += ntiles;
       if (!ok) {
         if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
         *abort = 1;
@@ -483,14 +581,13 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
         float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
         for (int t = half; t < ntiles; t += 2) {
           float z[ROWS];
-          tile_logits<T::NB, ROWS>(tmem, quad, (b * TPB + t) * T::NB, z);
+          tmem_ld_rows<ROWS>(cbase + (uint32_t)(t * ROWS), z);
           key_values<ROWS>(z, u.j0 * PAGE + t * 128 + 32 * quad + lane, u.ndem, u.ncmp, lse_dem, lse_cmp, av, sc);
         }
       }
       tc_fence_before();
       epi_sync();
       if (et == 0) {
-        mbar_arrive(bar_tfree + 8 * b);  // TMEM buffer b may take the unit after next
         // the CTA's a-values (ordered by the barrier above) before its ticket
         __threadfence();
         atomicAdd(a.tickets + (size_t)u.r * units + u.unit, 1u);
@@ -505,6 +602,12 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
             }
           }
           if (!*abort) {
+            // the cluster's last unit: no scan is left to hide its select behind,
+            // so the selector warps stop here and the whole CTA drains it
+            if (w + nclus >= total_units) {
+              *q_done = 1;
+              __threadfence_block();
+            }
             queue[*q_head % QLEN] = w;
             __threadfence_block();
             *q_head = *q_head + 1;
@@ -518,48 +621,12 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     }
   } else if (warp >= SEL_W0) {
     // ---- selector ------------------------------------------------------------
+    // Runs queued selects while the scan goes on; the ones still queued when
+    // the epilogue finishes are left to the whole CTA (drain below).
     const int st = tid - 32 * SEL_W0;
     uint32_t sel_par = 0u;  // phase of the staging barrier
     while (true) {
-      if (st == 0) {
-        int item = -1;
-        const long long t0 = clock64();
-        while (true) {
-          const int h = *q_head, tl = *q_tail;
-          if (h != tl) {
-            item = queue[tl % QLEN];
-            break;
-          }
-          if (*q_done) {
-            __threadfence_block();
-            if (*q_head == tl) break;
-            continue;
-          }
-          if (*abort) break;
-          if (clock64() - t0 > kWaitLimit) {
-            atomicOr(a.err, ERR_TIMEOUT);
-            *abort = 1;
-            break;
-          }
-          __nanosleep(200);
-        }
-        if (item >= 0) {
-          // wait until every rank of the cluster has written its a-values
-          const UnitInfo u = unit_info(a, item, 0);
-          const unsigned* tk = a.tickets + (size_t)u.r * units + u.unit;
-          const long long t1 = clock64();
-          while (ld_acquire(tk) < (unsigned)C) {
-            if (*abort || clock64() - t1 > kWaitLimit) {
-              atomicOr(a.err, ERR_TIMEOUT);
-              *abort = 1;
-              item = -1;
-              break;
-            }
-            __nanosleep(100);
-          }
-        }
-        *sel_item = item;
-      }
+      if (st == 0) *sel_item = take_item(true);
       sel_sync<SEL_NTH, BAR_SEL>();
       const int w = *sel_item;
       if (w < 0) break;
@@ -574,13 +641,35 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
       sel_sync<SEL_NTH, BAR_SEL>();
       if (st == 0) *q_tail = *q_tail + 1;
     }
+    if (st == 0) misc[7] = (int)sel_par;
   }
   (void)flag;
   (void)phys;
 
-  // ---- teardown ----------------------------------------------------------------
+  // ---- drain: selects still queued when the scan ended, with the whole CTA --
   tc_fence_before();
   __syncthreads();
+  {
+    uint32_t par = (uint32_t)misc[7];
+    while (true) {
+      if (tid == 0) *sel_item = take_item(false);
+      __syncthreads();
+      const int w = *sel_item;
+      if (w < 0) break;
+      const UnitInfo u = unit_info(a, w, 0);
+      unsigned k = 0;
+      if (u.ndem > 0) {
+        const float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
+        k = coverage_demand<NTHR, 0>(av, u.ndem, a.p, selbuf, sel_cap, dps, a.err, tid, bar_sel, par);
+        if (2 * u.ndem <= sel_cap) par ^= 1u;
+      }
+      write_demand(a, u.r, u.unit, tid, k);
+      __syncthreads();
+      if (tid == 0) *q_tail = *q_tail + 1;
+    }
+  }
+
+  // ---- teardown ----------------------------------------------------------------
   cluster_sync_all();  // no rank leaves while a peer may still write into it
   if (warp == 1) {
     tc_fence_after();
@@ -614,7 +703,7 @@ template <int D, int ROWS>
 cudaError_t launch_t(const DemandArgs& a, cudaStream_t s) {
   using T = TcCfg<D, ROWS>;
   using S = TcSmem<D, ROWS>;
-  if (2 * a.ppc * T::NB > 512) return cudaErrorInvalidValue;  // one unit's tiles must fit TMEM
+  if (2 * a.ppc > T::TPU) return cudaErrorInvalidValue;  // a unit's compact logits must fit TMEM
   int dev = 0, max_optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
