@@ -274,74 +274,113 @@ __device__ __forceinline__ void key_values(const float* z, int i, int ndem, int 
 }
 
 // ---- p-coverage demand D_p (Eq. 2) ----------------------------------------
-// Exact on the fp32 a-values: masses are fixed point with 40 fractional bits,
-// so every sum is an integer sum and the threshold test is exact.  A radix
-// select on the fp32 bit pattern (a >= 0, so the bits order like the values)
-// walks three 10-bit digits from the top -- bits [29:20] (exponent and 3
-// mantissa bits), [19:10], [9:0] -- keeping the bin where the cumulative
-// mass, counted from the largest values down, reaches ceil(p * total).  Then
-// D_p = #(a > t) + ceil((target - mass(a > t)) / mass(t)).
-// A bin holds its count and its mass split in two 32-bit sums (mass >> 16,
-// mass & 0xffff), each fed by a native 32-bit shared atomic; the first digit
-// reaches into the mantissa, so even a flat distribution spreads over many
-// bins and the atomics rarely collide.
+// Exact on the fp32 a-values of one summary: a value's mass is its product
+// with 2^40 rounded to the nearest integer (ties to even), so every sum is an
+// integer sum and the threshold test is exact.  With T the total mass and
+// target = ceil(p T) (p a 64-bit binary fraction), D_p is the number of the
+// largest values whose mass first reaches the target:
+//   D_p = #(a > t) + ceil((target - mass(a > t)) / mass(t))
+// for the threshold value t.  The values are non-negative, so their fp32 bit
+// patterns order like the values and t is found by digits of the pattern.
+//
+//   1. One pass over the values: the exact total T, and a histogram over the
+//      first digit (bits [29:20]: exponent and 3 mantissa bits) of each
+//      value's mass >> 9, one 32-bit shared atomic per value of non-zero
+//      approximate mass.  A block scan from the top picks the bin b where
+//      that approximate mass reaches the target.
+//   2. A second pass sums exactly the mass and count of the values above b
+//      and the mass of b, and compacts b's members.  If the exact sums place
+//      the target inside b, b is the threshold bin; if not (the truncated
+//      masses can move the crossing across a bin edge), the first digit is
+//      redone with exact histograms.
+//   3. Within the bin, a few hundred members at most: every member counts
+//      the members above it and their mass, and the member where the
+//      cumulative mass reaches the target is t.  More members than that: two
+//      more 10-bit digits ([19:10], [9:0]) with exact histograms of count and
+//      mass (mass split in two 32-bit sums, mass >> 16 and mass & 0xffff).
+// All of it in 32-bit integer and fp32 arithmetic: GB300 runs 64-bit
+// conversions and divisions on its slow FP64 path.
 
-__device__ __forceinline__ unsigned long long fixed40(unsigned u) {
-  const int e = (int)(u >> 23) & 255;
-  if (e == 0 || e > 128) return 0ull;  // zero, or not a probability (inf / NaN)
-  const unsigned long long m = (u & 0x7FFFFFu) | 0x800000u;
-  const int sh = e - 110;  // value * 2^40 = m * 2^(e - 110)
-  if (sh >= 0) return m << sh;
-  const int s = -sh;
-  if (s >= 25) return 0ull;  // below one half
-  const unsigned long long q = m >> s, r = m & ((1ull << s) - 1), half = 1ull << (s - 1);
-  return q + ((r > half || (r == half && (q & 1ull))) ? 1ull : 0ull);
+// The bits of a value that take part: values >= 2 (not probabilities, or
+// negative, inf, NaN) count as zero.
+__device__ __forceinline__ unsigned sel_bits(unsigned u) { return u >= 0x40000000u ? 0u : u; }
+
+// The mass of a value (bits u, 0 <= a < 2) as hi 2^23 + lo, 0 <= lo <= 2^23:
+// hi = floor(a 2^17) and lo = the rest of a 2^40 rounded to nearest even.
+// a 2^40 is exact, so is the remainder r = a 2^40 - hi 2^23 < 2^23 (a
+// multiple of ulp(a 2^40) below 2^23), and adding 2^23 (ulp 1 on [2^23,
+// 2^24)) rounds r to an integer with ties to even; floor(a 2^17) < 2^18 is
+// taken the same way with round-toward-zero.
+__device__ __forceinline__ void mass40(unsigned u, unsigned& hi, unsigned& lo) {
+  const float a = __uint_as_float(u);
+  const float t = __fadd_rz(__fmul_rn(a, 131072.0f), 8388608.0f);  // 2^23 + floor(a 2^17)
+  hi = __float_as_uint(t) - 0x4B000000u;
+  const float r = __fmaf_rn(-(t - 8388608.0f), 8388608.0f, __fmul_rn(a, 1099511627776.0f));
+  lo = __float_as_uint(__fadd_rn(r, 8388608.0f)) - 0x4B000000u;
+}
+__device__ __forceinline__ unsigned long long mass40(unsigned u) {
+  unsigned hi, lo;
+  mass40(u, hi, lo);
+  return ((unsigned long long)hi << 23) + lo;
+}
+
+// ceil(t * f / 2^64), at least 1: the target mass for the fraction f.
+__device__ __forceinline__ unsigned long long coverage_target(unsigned long long t, unsigned long long f) {
+  const unsigned long long hi = __umul64hi(t, f), lo = t * f;
+  const unsigned long long g = hi + (lo != 0ull ? 1ull : 0ull);
+  return g < 1ull ? 1ull : g;
+}
+
+// min(cap, ceil(need / f)) for f >= 1, need >= 1, without a 64-bit division:
+// a float estimate, good to well under one unit when the result is at most
+// cap + 2 < 2^20, then exact integer steps.
+__device__ __forceinline__ unsigned ceil_div_capped(unsigned long long need, unsigned long long f, unsigned cap) {
+  const float q = __fdiv_rn((float)need, (float)f);
+  if (!(q <= (float)cap + 2.0f)) return cap;
+  unsigned j = (unsigned)q;
+  while (j > 0u && (unsigned long long)(j - 1u) * f >= need) --j;
+  while ((unsigned long long)j * f < need) ++j;
+  return j < cap ? j : cap;
 }
 
 constexpr int SEL_BINS = 1024;  // every digit
+constexpr int APPROX_SHIFT = 9;  // first-digit histogram: mass >> 9 (sums stay below 2^32)
 
 struct DpState {
   unsigned prefix, cnt_above, cnt_eq;
   unsigned long long mass_above, target;
-  int bad, done;
+  int bad;
 };
 
 struct DpSmem {
-  unsigned cnt[2][SEL_BINS];
-  unsigned mhi[2][SEL_BINS];             // sum of mass >> 16
-  unsigned mlo[2][SEL_BINS];             // sum of mass & 0xffff
-  unsigned long long wm[2][32];          // per-warp scan totals: mass
-  unsigned wc[2][32];                    //                       count
-  DpState st[2];
-  unsigned ncomp[2];
-  int compact;
+  unsigned am[SEL_BINS];   // first digit: approximate mass
+  unsigned cnt[SEL_BINS];  // exact digits: count,
+  unsigned mhi[SEL_BINS];  //   mass >> 16,
+  unsigned mlo[SEL_BINS];  //   mass & 0xffff
+  unsigned long long wm[32], we[32];  // per-warp partial sums
+  unsigned wc[32];
+  DpState st;
+  unsigned ncomp;          // members of the threshold bin appended so far
+  unsigned res;            // D_p once found (~0u before)
 };
 
-__device__ __forceinline__ void hist_add(DpSmem* sm, int x, int bin, unsigned long long w) {
-  atomicAdd(&sm->cnt[x][bin], 1u);
-  atomicAdd(&sm->mhi[x][bin], (unsigned)(w >> 16));
-  atomicAdd(&sm->mlo[x][bin], (unsigned)(w & 0xFFFFull));
+__device__ __forceinline__ void hist_add(DpSmem* sm, int bin, unsigned u) {
+  unsigned hi, lo;
+  mass40(u, hi, lo);
+  atomicAdd(&sm->cnt[bin], 1u);
+  atomicAdd(&sm->mhi[bin], (hi << 7) + (lo >> 16));
+  atomicAdd(&sm->mlo[bin], lo & 0xFFFFu);
 }
-__device__ __forceinline__ unsigned long long bin_mass(const DpSmem* sm, int x, int bin) {
-  return ((unsigned long long)sm->mhi[x][bin] << 16) + sm->mlo[x][bin];
+__device__ __forceinline__ unsigned long long bin_mass(const DpSmem* sm, int bin) {
+  return ((unsigned long long)sm->mhi[bin] << 16) + sm->mlo[bin];
 }
-
-// The bits of a value that take part: values >= 2 (not probabilities) count
-// as zero.
-__device__ __forceinline__ unsigned sel_bits(unsigned u) { return u >= 0x40000000u ? 0u : u; }
-
-// Values below 2^-41 (biased exponent <= 85) have exactly zero fixed-point
-// mass.  They lie in first-digit bins strictly below any bin holding a value
-// of positive mass, and the threshold bin always holds one, so they never
-// reach the count or mass above the threshold: the histograms skip them.
-constexpr unsigned MIN_MASS_BITS = 86u << 23;
 
 template <int NTH>
-__device__ __forceinline__ void clear_hist(DpSmem* sm, int tid) {
-  for (int k = tid; k < 2 * SEL_BINS; k += NTH) {
-    (&sm->cnt[0][0])[k] = 0u;
-    (&sm->mhi[0][0])[k] = 0u;
-    (&sm->mlo[0][0])[k] = 0u;
+__device__ __forceinline__ void clear_exact_hist(DpSmem* sm, int tid) {
+  for (int k = tid; k < SEL_BINS; k += NTH) {
+    sm->cnt[k] = 0u;
+    sm->mhi[k] = 0u;
+    sm->mlo[k] = 0u;
   }
 }
 
@@ -355,108 +394,81 @@ __device__ __forceinline__ void sel_sync() {
   }
 }
 
-// One digit for both summaries: scan the bins from the top (a block-wide
-// prefix sum over thread-owned runs of bins), fix the target on the first
-// digit, and record the bin where the mass reaches it.
-template <int NTH, int BAR>
-__device__ __forceinline__ void pick_digit(DpSmem* sm, int shift, bool first, double p, int tid) {
-  constexpr int nbins = SEL_BINS;
-  constexpr int NWS = NTH / 32;
-  const int lane = tid & 31, wid = tid >> 5;
-  const int per = (nbins + NTH - 1) / NTH;
-  const int q0 = tid * per, q1 = min(nbins, q0 + per);  // positions from the top
-  unsigned long long lm[2] = {0ull, 0ull};
-  unsigned lc[2] = {0u, 0u};
-  for (int q = q0; q < q1; ++q) {
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      lm[x] += bin_mass(sm, x, nbins - 1 - q);
-      lc[x] += sm->cnt[x][nbins - 1 - q];
-    }
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+__device__ __forceinline__ unsigned warp_sum_u32(unsigned v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+// One exact digit: scan the bins from the top (a block-wide prefix sum over
+// thread-owned runs of bins) and record the bin where the cumulative mass
+// reaches the target.  need = target - mass above the bins, read by every
+// thread before the barrier inside, so the crossing thread may update st.
+template <int NTH, int BAR>
+__device__ __forceinline__ void pick_digit(DpSmem* sm, int shift, unsigned long long need, int tid) {
+  constexpr int NWS = NTH / 32;
+  constexpr int PER = (SEL_BINS + NTH - 1) / NTH;
+  const int lane = tid & 31, wid = tid >> 5;
+  const int q0 = tid * PER, q1 = min(SEL_BINS, q0 + PER);  // positions from the top
+  unsigned long long lm = 0ull;
+  unsigned lc = 0u;
+  for (int q = q0; q < q1; ++q) {
+    lm += bin_mass(sm, SEL_BINS - 1 - q);
+    lc += sm->cnt[SEL_BINS - 1 - q];
   }
-  unsigned long long im[2] = {lm[0], lm[1]};
-  unsigned ic[2] = {lc[0], lc[1]};
+  unsigned long long im = lm;
+  unsigned ic = lc;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const unsigned long long om = __shfl_up_sync(FULL, im[x], o);
-      const unsigned oc = __shfl_up_sync(FULL, ic[x], o);
-      if (lane >= o) {
-        im[x] += om;
-        ic[x] += oc;
-      }
+    const unsigned long long om = __shfl_up_sync(FULL, im, o);
+    const unsigned oc = __shfl_up_sync(FULL, ic, o);
+    if (lane >= o) {
+      im += om;
+      ic += oc;
     }
   }
   if (lane == 31) {
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      sm->wm[x][wid] = im[x];
-      sm->wc[x][wid] = ic[x];
-    }
+    sm->wm[wid] = im;
+    sm->wc[wid] = ic;
   }
   sel_sync<NTH, BAR>();
-  unsigned long long base_m[2] = {0ull, 0ull}, tot[2] = {0ull, 0ull};
-  unsigned base_c[2] = {0u, 0u};
+  unsigned long long base_m = 0ull;
+  unsigned base_c = 0u;
 #pragma unroll
-  for (int x = 0; x < 2; ++x)
-    for (int w = 0; w < NWS; ++w) {
-      if (w < wid) {
-        base_m[x] += sm->wm[x][w];
-        base_c[x] += sm->wc[x][w];
-      }
-      tot[x] += sm->wm[x][w];
-    }
-  if (first && tid < 2) {
-    DpState& st = sm->st[tid];
-    if (tot[tid] == 0ull) {
-      st.done = 1;
-    } else {
-      unsigned long long tg = (unsigned long long)ceil(p * (double)tot[tid]);
-      if (tg < 1ull) tg = 1ull;
-      if (tg > tot[tid]) tg = tot[tid];
-      st.target = tg;
+  for (int w = 0; w < NWS; ++w) {
+    if (w < wid) {
+      base_m += sm->wm[w];
+      base_c += sm->wc[w];
     }
   }
-  if (first) sel_sync<NTH, BAR>();
-  // Every thread reads the state before the crossing thread updates it.
-  unsigned long long needs[2];
-  bool dones[2];
-#pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    dones[x] = sm->st[x].done != 0;
-    needs[x] = sm->st[x].target - sm->st[x].mass_above;
-  }
-  sel_sync<NTH, BAR>();
-#pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    DpState& st = sm->st[x];
-    if (dones[x]) continue;
-    const unsigned long long need = needs[x];
-    const unsigned long long incl = base_m[x] + im[x], excl = incl - lm[x];
-    const bool last = tid == NTH - 1;
-    if ((excl < need && need <= incl) || (last && incl < need)) {
-      unsigned long long cum = excl;
-      unsigned cnt = base_c[x] + ic[x] - lc[x];
-      int chosen = -1;
-      for (int q = q0; q < q1; ++q) {
-        const unsigned long long mb = bin_mass(sm, x, nbins - 1 - q);
-        if (cum + mb >= need) {
-          chosen = nbins - 1 - q;
-          break;
-        }
-        cum += mb;
-        cnt += sm->cnt[x][nbins - 1 - q];
+  const unsigned long long incl = base_m + im, excl = incl - lm;
+  if ((excl < need && need <= incl) || (tid == NTH - 1 && incl < need)) {
+    DpState& st = sm->st;
+    unsigned long long cum = excl;
+    unsigned cnt = base_c + ic - lc;
+    int chosen = -1;
+    for (int q = q0; q < q1; ++q) {
+      const unsigned long long mb = bin_mass(sm, SEL_BINS - 1 - q);
+      if (cum + mb >= need) {
+        chosen = SEL_BINS - 1 - q;
+        break;
       }
-      if (chosen < 0) {  // the target lies beyond all mass: inconsistent input
-        st.bad = 1;
-        chosen = 0;
-      }
-      st.prefix |= (unsigned)chosen << shift;
-      st.mass_above += cum;
-      st.cnt_above += cnt;
-      st.cnt_eq = sm->cnt[x][chosen];
+      cum += mb;
+      cnt += sm->cnt[SEL_BINS - 1 - q];
     }
+    if (chosen < 0) {  // the target lies beyond all mass: inconsistent input
+      st.bad = 1;
+      chosen = 0;
+    }
+    st.prefix |= (unsigned)chosen << shift;
+    st.mass_above += cum;
+    st.cnt_above += cnt;
+    st.cnt_eq = sm->cnt[chosen];
   }
 }
 
@@ -473,8 +485,9 @@ __device__ __forceinline__ bool sel_bar_try(uint32_t bar, uint32_t parity) {
 
 // Append the kept values among v[0..3] of every lane of the warp to
 // dst[*count ...] with one shared atomic per warp (order is irrelevant).
+// Positions at or beyond `room` are counted but not written.
 __device__ __forceinline__ void warp_append4(const unsigned (&v)[4], const bool (&keep)[4], unsigned* dst,
-                                             unsigned* count, int lane) {
+                                             unsigned* count, unsigned room, int lane) {
   const unsigned c = (unsigned)keep[0] + keep[1] + keep[2] + keep[3];
   if (!__any_sync(FULL, c != 0u)) return;
   unsigned incl = c;
@@ -484,58 +497,64 @@ __device__ __forceinline__ void warp_append4(const unsigned (&v)[4], const bool 
     if (lane >= o) incl += t;
   }
   const unsigned tot = __shfl_sync(FULL, incl, 31);
-  if (tot == 0u) return;
   unsigned base = 0u;
   if (lane == 31) base = atomicAdd(count, tot);
   base = __shfl_sync(FULL, base, 31);
   unsigned pos = base + incl - c;
 #pragma unroll
   for (int k = 0; k < 4; ++k)
-    if (keep[k]) dst[pos++] = v[k];
+    if (keep[k]) {
+      if (pos < room) dst[pos] = v[k];
+      ++pos;
+    }
 }
 
-// D_p of both summaries of one unit from its a-values av[2][ndem] (global,
-// written by the unit's CTAs, 16-byte aligned, ndem a multiple of 256).
-// Called by NTH threads (tid in [0, NTH), whole warps) that synchronise on
-// named barrier BAR.  sm: shared DpSmem; buf: shared scratch of `cap` words.
-//   * 2 ndem <= cap: the a-values are staged in buf -- by one bulk async
-//     copy completing on the initialised mbarrier `bar` (phase `parity`) when
-//     bar != 0, else by 16-byte loads -- and the first digit reads them there;
-//   * otherwise the first digit reads global memory (four 16-byte loads in
-//     flight per thread).
-// Then the members of the first digit's bin are compacted behind the staged
-// values (or at the start of buf) when they fit, and the other two digits
-// run over them; if they do not fit, those digits re-scan every value.
-// Thread x < 2 returns D_p for summary x.
+// Whether coverage_demand stages the n values in its scratch of cap words
+// (and so uses its staging barrier, whose phase the caller then flips).
+__host__ __device__ __forceinline__ bool sel_resident(int n, int cap) { return n <= cap; }
+
+// D_p of one summary from its n a-values av[n] (global, written by the
+// unit's CTAs, 16-byte aligned, n a multiple of 256), for the target
+// fraction pfix / 2^64.  Called by NTH threads (tid in [0, NTH), whole warps)
+// that synchronise on named barrier BAR.  sm: shared DpSmem; buf: shared
+// scratch of `cap` words, 16-byte aligned.
+//   * n <= cap: the values are staged in buf -- by one bulk async copy
+//     completing on the initialised mbarrier `bar` (phase `parity`) when
+//     bar != 0, else by 16-byte loads -- and every pass reads them there;
+//   * otherwise the passes read global memory.
+// The threshold bin's members are compacted behind the staged values (or at
+// the start of buf) when they fit.  Every thread returns D_p.
 template <int NTH, int BAR>
-__device__ __forceinline__ unsigned coverage_demand(const float* av, int ndem, double p, unsigned* buf, int cap,
-                                                    DpSmem* sm, int* err, int tid, uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ unsigned coverage_demand(const float* av, int n, unsigned long long pfix, unsigned* buf,
+                                                    int cap, DpSmem* sm, int* err, int tid, uint32_t bar,
+                                                    uint32_t parity) {
   static_assert(NTH % 32 == 0 && NTH <= 1024, "whole warps");
-  const int lane = tid & 31;
-  const bool resident = 2 * ndem <= cap;
-  if (tid < 2) {
-    DpState& s = sm->st[tid];
+  constexpr int NWS = NTH / 32;
+  const int lane = tid & 31, wid = tid >> 5;
+  const bool resident = sel_resident(n, cap);
+  if (tid == 0) {
+    DpState& s = sm->st;
     s.prefix = 0u;
     s.cnt_above = 0u;
     s.cnt_eq = 0u;
     s.mass_above = 0ull;
     s.target = 0ull;
     s.bad = 0;
-    s.done = 0;
-    sm->ncomp[tid] = 0u;
+    sm->ncomp = 0u;
+    sm->res = ~0u;
   }
   const uint4* src4 = reinterpret_cast<const uint4*>(av);
-  const int n4 = ndem / 4;  // 16-byte groups per summary
+  const int n4 = n / 4;  // 16-byte groups
   if (resident && bar != 0u && tid == 0) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // buf was last read by ordinary loads
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"((uint32_t)(8 * ndem))
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"((uint32_t)(4 * n))
                  : "memory");
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(buf)),
-                 "l"(av), "r"((uint32_t)(8 * ndem)), "r"(bar)
+                 "l"(av), "r"((uint32_t)(4 * n)), "r"(bar)
                  : "memory");
   }
-  clear_hist<NTH>(sm, tid);
+  for (int k = tid; k < SEL_BINS; k += NTH) sm->am[k] = 0u;
   if (resident) {
     if (bar != 0u) {
       bool ok = sel_bar_try(bar, parity);
@@ -548,7 +567,7 @@ __device__ __forceinline__ unsigned coverage_demand(const float* av, int ndem, d
     } else {
       uint4* d4 = reinterpret_cast<uint4*>(buf);
       int i = tid;
-      for (; i + 3 * NTH < 2 * n4; i += 4 * NTH) {
+      for (; i + 3 * NTH < n4; i += 4 * NTH) {
         const uint4 v0 = __ldcg(src4 + i), v1 = __ldcg(src4 + i + NTH), v2 = __ldcg(src4 + i + 2 * NTH),
                     v3 = __ldcg(src4 + i + 3 * NTH);
         d4[i] = v0;
@@ -556,124 +575,257 @@ __device__ __forceinline__ unsigned coverage_demand(const float* av, int ndem, d
         d4[i + 2 * NTH] = v2;
         d4[i + 3 * NTH] = v3;
       }
-      for (; i < 2 * n4; i += NTH) d4[i] = __ldcg(src4 + i);
+      for (; i < n4; i += NTH) d4[i] = __ldcg(src4 + i);
     }
   }
   sel_sync<NTH, BAR>();
-  // The a-values of summary x, 16 bytes at a time, from buf or global memory.
-  auto group = [&](int x, int i) -> uint4 {
-    return resident ? reinterpret_cast<const uint4*>(buf)[(size_t)x * n4 + i] : __ldcg(src4 + (size_t)x * n4 + i);
-  };
-  // digit 1: bits [29:20]
-#pragma unroll
-  for (int x = 0; x < 2; ++x) {
+  // Visit every value as f(bits[4], in range), four 16-byte groups in flight
+  // per thread; bits already through sel_bits, zero out of range.
+  auto each_value = [&](auto&& f) {
     for (int i0 = 0; i0 < n4; i0 += 4 * NTH) {
       uint4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int i = i0 + j * NTH + tid;
-        v[j] = i < n4 ? group(x, i) : make_uint4(0u, 0u, 0u, 0u);
+        v[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < n4) v[j] = resident ? reinterpret_cast<const uint4*>(buf)[i] : __ldcg(src4 + i);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const unsigned w[4] = {sel_bits(v[j].x), sel_bits(v[j].y), sel_bits(v[j].z), sel_bits(v[j].w)};
-        if (i0 + j * NTH + tid < n4) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (w[k] >= MIN_MASS_BITS) hist_add(sm, x, (int)(w[k] >> 20), fixed40(w[k]));
-        }
+        f(w);
       }
+    }
+  };
+
+  // 1. exact total, approximate first-digit histogram
+  {
+    unsigned thi = 0u, tlo = 0u;  // sums of hi (< 2^18 each) and lo (<= 2^23 each)
+    each_value([&](const unsigned (&w)[4]) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        unsigned hi, lo;
+        mass40(w[k], hi, lo);
+        thi += hi;
+        tlo += lo;
+        const unsigned h = (hi << (23 - APPROX_SHIFT)) + (lo >> APPROX_SHIFT);
+        if (h != 0u) atomicAdd(&sm->am[w[k] >> 20], h);
+      }
+    });
+    const unsigned long long tot = warp_sum_u64(((unsigned long long)thi << 23) + tlo);
+    if (lane == 0) sm->wm[wid] = tot;
+  }
+  sel_sync<NTH, BAR>();
+  unsigned long long tot = 0ull;
+#pragma unroll
+  for (int w = 0; w < NWS; ++w) tot += sm->wm[w];
+  if (tot == 0ull) return 0u;  // no mass at all: nothing to cover
+  const unsigned long long target = coverage_target(tot, pfix);
+  {
+    constexpr int PER = (SEL_BINS + NTH - 1) / NTH;
+    const int q0 = tid * PER, q1 = min(SEL_BINS, q0 + PER);
+    unsigned ls = 0u;
+    for (int q = q0; q < q1; ++q) ls += sm->am[SEL_BINS - 1 - q];
+    unsigned is = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned t = __shfl_up_sync(FULL, is, o);
+      if (lane >= o) is += t;
+    }
+    if (lane == 31) sm->wc[wid] = is;
+    sel_sync<NTH, BAR>();
+    unsigned base = 0u;
+#pragma unroll
+    for (int w = 0; w < NWS; ++w)
+      if (w < wid) base += sm->wc[w];
+    const unsigned long long incl = (unsigned long long)(base + is) << APPROX_SHIFT;
+    const unsigned long long excl = (unsigned long long)(base + is - ls) << APPROX_SHIFT;
+    if ((excl < target && target <= incl) || (tid == NTH - 1 && incl < target)) {
+      unsigned long long cum = excl;
+      int chosen = 0;
+      for (int q = q0; q < q1; ++q) {
+        const unsigned long long mb = (unsigned long long)sm->am[SEL_BINS - 1 - q] << APPROX_SHIFT;
+        if (cum + mb >= target) {
+          chosen = SEL_BINS - 1 - q;
+          break;
+        }
+        cum += mb;
+      }
+      sm->st.prefix = (unsigned)chosen;  // the candidate bin, checked below
+    }
+    sel_sync<NTH, BAR>();
+  }
+
+  // 2. exact mass and count above the candidate bin, its mass and members
+  const unsigned bsel = sm->st.prefix;
+  const unsigned cbase = resident ? (unsigned)n : 0u;
+  const unsigned space = (unsigned)cap > cbase ? (unsigned)cap - cbase : 0u;
+  unsigned* memb = buf + cbase;
+  {
+    unsigned ahi = 0u, alo = 0u, ehi = 0u, elo = 0u, ca = 0u;
+    each_value([&](const unsigned (&w)[4]) {
+      bool keep[4], above[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const unsigned b = w[k] >> 20;
+        keep[k] = w[k] != 0u && b == bsel;
+        above[k] = b > bsel;
+      }
+      const bool any_above = above[0] || above[1] || above[2] || above[3];
+      const bool any_keep = keep[0] || keep[1] || keep[2] || keep[3];
+      if (__any_sync(FULL, any_above || any_keep)) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          unsigned hi, lo;
+          mass40(w[k], hi, lo);
+          if (above[k]) {
+            ahi += hi;
+            alo += lo;
+            ++ca;
+          }
+          if (keep[k]) {
+            ehi += hi;
+            elo += lo;
+          }
+        }
+        warp_append4(w, keep, memb, &sm->ncomp, space, lane);
+      }
+    });
+    const unsigned long long ma = warp_sum_u64(((unsigned long long)ahi << 23) + alo);
+    const unsigned long long me = warp_sum_u64(((unsigned long long)ehi << 23) + elo);
+    ca = warp_sum_u32(ca);
+    if (lane == 0) {
+      sm->wm[wid] = ma;
+      sm->we[wid] = me;
+      sm->wc[wid] = ca;
     }
   }
   sel_sync<NTH, BAR>();
-  pick_digit<NTH, BAR>(sm, 20, true, p, tid);
-  sel_sync<NTH, BAR>();
-  // stream compaction of the first digit's bin
-  const unsigned cbase = resident ? (unsigned)(2 * ndem) : 0u;
-  const bool compact = cbase + sm->st[0].cnt_eq + sm->st[1].cnt_eq <= (unsigned)cap;
-  const unsigned off1 = cbase + sm->st[0].cnt_eq;
-  if (compact) {
+  unsigned long long above = 0ull, in_bin = 0ull;
+  unsigned cnt_above = 0u;
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      if (sm->st[x].done) continue;
-      const unsigned want = sm->st[x].prefix >> 20;
-      unsigned* dst = buf + (x ? off1 : cbase);
-      for (int i0 = 0; i0 < n4; i0 += 4 * NTH) {
-        uint4 v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = i0 + j * NTH + tid;
-          v[j] = i < n4 ? group(x, i) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const bool in = i0 + j * NTH + tid < n4;
-          const unsigned w[4] = {sel_bits(v[j].x), sel_bits(v[j].y), sel_bits(v[j].z), sel_bits(v[j].w)};
-          const bool keep[4] = {in && (w[0] >> 20) == want, in && (w[1] >> 20) == want,
-                                in && (w[2] >> 20) == want, in && (w[3] >> 20) == want};
-          warp_append4(w, keep, dst, &sm->ncomp[x], lane);
+  for (int w = 0; w < NWS; ++w) {
+    above += sm->wm[w];
+    in_bin += sm->we[w];
+    cnt_above += sm->wc[w];
+  }
+  const unsigned m = sm->ncomp;
+  const bool first_ok = above < target && target <= above + in_bin;
+  // 3a layout: members padded with zeros (mass 0, never above or equal to a
+  // member of positive mass) to tpc chunks of a multiple of 4, then their
+  // masses; tpc threads share a member.
+  unsigned tpc = 1u;
+  while (tpc < 32u && m * tpc * 2u <= (unsigned)NTH) tpc <<= 1;
+  const unsigned chunk = ((m + tpc - 1u) / tpc + 3u) & ~3u, mpad = chunk * tpc;
+  bool compacted = first_ok && m <= space;
+
+  if (first_ok && 3u * mpad <= space && m * m <= 128u * NTH) {
+    // 3a. rank every member among the members
+    unsigned long long* fm = reinterpret_cast<unsigned long long*>(memb + mpad);  // 16-byte aligned
+    for (unsigned i = tid; i < mpad; i += NTH) {
+      const unsigned u = i < m ? memb[i] : 0u;
+      if (i >= m) memb[i] = 0u;
+      fm[i] = mass40(u);
+    }
+    sel_sync<NTH, BAR>();
+    const unsigned long long need = target - above;
+    const unsigned per_pass = NTH / tpc, part = (unsigned)tid % tpc;
+    for (unsigned i0 = 0; i0 < m; i0 += per_pass) {
+      const unsigned i = i0 + (unsigned)tid / tpc;
+      const unsigned v = i < m ? memb[i] : 0u;
+      unsigned long long g_mass = 0ull;
+      unsigned g_cnt = 0u, e_cnt = 0u;
+      if (i < m) {
+        const uint4* c4 = reinterpret_cast<const uint4*>(memb + part * chunk);
+        const ulonglong2* f2 = reinterpret_cast<const ulonglong2*>(fm + part * chunk);
+        for (int q = 0; q < (int)(chunk / 4u); ++q) {
+          const uint4 c = c4[q];
+          const ulonglong2 fa = f2[2 * q], fb = f2[2 * q + 1];
+          g_mass += (c.x > v ? fa.x : 0ull) + (c.y > v ? fa.y : 0ull) + (c.z > v ? fb.x : 0ull) +
+                    (c.w > v ? fb.y : 0ull);
+          g_cnt += (unsigned)(c.x > v) + (unsigned)(c.y > v) + (unsigned)(c.z > v) + (unsigned)(c.w > v);
+          e_cnt += (unsigned)(c.x == v) + (unsigned)(c.y == v) + (unsigned)(c.z == v) + (unsigned)(c.w == v);
         }
       }
+      for (unsigned o = 1; o < tpc; o <<= 1) {
+        g_mass += __shfl_xor_sync(FULL, g_mass, o);
+        g_cnt += __shfl_xor_sync(FULL, g_cnt, o);
+        e_cnt += __shfl_xor_sync(FULL, e_cnt, o);
+      }
+      if (i < m && part == 0u) {
+        const unsigned long long fv = fm[i];
+        if (g_mass < need && fv > 0ull && need - g_mass <= fv * e_cnt)  // the same for every member equal to t
+          sm->res = cnt_above + g_cnt + ceil_div_capped(need - g_mass, fv, e_cnt);
+      }
+    }
+    sel_sync<NTH, BAR>();
+    const unsigned r = sm->res;
+    sel_sync<NTH, BAR>();  // the scratch may be reused once every thread is done
+    if (r != ~0u) return r;
+    if (tid == 0) atomicOr(err, ERR_BAD_COUNT);  // unreachable for consistent sums
+    return 0u;
+  }
+
+  // 3b. exact digits
+  if (tid == 0) {
+    DpState& s = sm->st;
+    s.target = target;
+    if (first_ok) {
+      s.prefix = bsel << 20;
+      s.mass_above = above;
+      s.cnt_above = cnt_above;
+      s.cnt_eq = m;
+    } else {
+      s.prefix = 0u;
+      s.mass_above = 0ull;
+      s.cnt_above = 0u;
     }
   }
-  // digits 2 and 3: bits [19:10] and [9:0] of the values matching the prefix
+  clear_exact_hist<NTH>(sm, tid);
+  sel_sync<NTH, BAR>();
+  if (!first_ok) {
+    compacted = false;
+    each_value([&](const unsigned (&w)[4]) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (w[k] != 0u) hist_add(sm, (int)(w[k] >> 20), w[k]);
+    });
+    sel_sync<NTH, BAR>();
+    pick_digit<NTH, BAR>(sm, 20, target, tid);
+  }
 #pragma unroll
   for (int ro = 0; ro < 2; ++ro) {
     const int sh = ro == 0 ? 10 : 0;
     const unsigned hi_mask = ro == 0 ? 0x3FF00000u : 0x3FFFFC00u;  // bits already fixed
     sel_sync<NTH, BAR>();
-    clear_hist<NTH>(sm, tid);
-    sel_sync<NTH, BAR>();
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      if (sm->st[x].done) continue;
-      const unsigned pf = sm->st[x].prefix;
-      if (compact) {
-        const unsigned n = sm->ncomp[x];
-        const unsigned* bb = buf + (x ? off1 : cbase);
-        for (unsigned i = tid; i < n; i += NTH) {
-          const unsigned u = bb[i];
-          if ((u & hi_mask) == pf) hist_add(sm, x, (int)((u >> sh) & (SEL_BINS - 1)), fixed40(u));
-        }
-      } else {
-        for (int i0 = 0; i0 < n4; i0 += 4 * NTH) {
-          uint4 v[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int i = i0 + j * NTH + tid;
-            v[j] = i < n4 ? group(x, i) : make_uint4(0u, 0u, 0u, 0u);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (i0 + j * NTH + tid >= n4) continue;
-            const unsigned w[4] = {sel_bits(v[j].x), sel_bits(v[j].y), sel_bits(v[j].z), sel_bits(v[j].w)};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if ((w[k] & hi_mask) == pf) hist_add(sm, x, (int)((w[k] >> sh) & (SEL_BINS - 1)), fixed40(w[k]));
-          }
-        }
+    const unsigned pf = sm->st.prefix;
+    const unsigned long long need = target - sm->st.mass_above;
+    if (ro == 1 || !first_ok) {  // the histograms of the previous digit are done with
+      clear_exact_hist<NTH>(sm, tid);
+      sel_sync<NTH, BAR>();
+    }
+    if (compacted) {
+      for (unsigned i = tid; i < m; i += NTH) {
+        const unsigned u = memb[i];
+        if ((u & hi_mask) == pf) hist_add(sm, (int)((u >> sh) & (SEL_BINS - 1)), u);
       }
+    } else {
+      each_value([&](const unsigned (&w)[4]) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (w[k] != 0u && (w[k] & hi_mask) == pf) hist_add(sm, (int)((w[k] >> sh) & (SEL_BINS - 1)), w[k]);
+      });
     }
     sel_sync<NTH, BAR>();
-    pick_digit<NTH, BAR>(sm, sh, false, p, tid);
+    pick_digit<NTH, BAR>(sm, sh, need, tid);
   }
   sel_sync<NTH, BAR>();
-  unsigned res = 0;
-  if (tid < 2) {
-    const DpState& s = sm->st[tid];
-    if (!s.done) {
-      const unsigned long long tf = fixed40(s.prefix);
-      const unsigned long long need = s.target - s.mass_above;
-      unsigned j = s.cnt_eq;
-      if (tf > 0) {
-        const unsigned long long q = (need + tf - 1) / tf;
-        if (q < j) j = (unsigned)q;
-      }
-      if (j < 1) j = 1;
-      res = s.cnt_above + j;
-      if (s.bad) atomicOr(err, ERR_BAD_COUNT);
-    }
-  }
+  const DpState& s = sm->st;
+  const unsigned long long tf = mass40(s.prefix);
+  const unsigned long long need = s.target - s.mass_above;
+  const unsigned j = tf > 0ull ? ceil_div_capped(need, tf, s.cnt_eq) : s.cnt_eq;
+  const unsigned res = s.cnt_above + (j < 1u ? 1u : j);
+  if (s.bad && tid == 0) atomicOr(err, ERR_BAD_COUNT);
   sel_sync<NTH, BAR>();  // the scratch may be reused once every thread is done
   return res;
 }
@@ -694,13 +846,11 @@ __device__ __forceinline__ bool last_of_unit(const DemandArgs& a, const Unit& u,
   return *flag_smem != 0;
 }
 
-// Thread x < 2 of the select stores D_p of summary x and adds it to the sums.
+// Stores D_p of summary x of a unit and adds it to the request's sum (one thread).
 __device__ __forceinline__ void write_demand(const DemandArgs& a, int r, int unit, int x, unsigned k) {
-  if (x < 2) {
-    const int units = a.L * a.Hkv;
-    a.kout[((size_t)r * units + unit) * 2 + x] = (int32_t)k;
-    atomicAdd(a.ksum + (size_t)r * 2 + x, (unsigned long long)k);
-  }
+  const int units = a.L * a.Hkv;
+  a.kout[((size_t)r * units + unit) * 2 + x] = (int32_t)k;
+  atomicAdd(a.ksum + (size_t)r * 2 + x, (unsigned long long)k);
 }
 
 // Launch with a cluster of a.C CTAs along x.

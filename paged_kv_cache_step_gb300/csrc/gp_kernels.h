@@ -2,6 +2,7 @@
 // kernels.  Plain structs of device pointers and sizes; no torch types.
 #pragma once
 
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 
@@ -62,6 +63,10 @@ __host__ __device__ inline size_t bq_bytes(int D, int G) { return (size_t)(D / 6
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 
 // ---- A3-A5: score scan, softmax, GQA mean, a-values, importance cache, D_p --
+// The coverage level p of D_p (0 < p < 1) as a 64-bit binary fraction,
+// floor(p 2^64): the select's target mass is ceil(T f / 2^64) in integers.
+inline unsigned long long coverage_fraction(double p) { return (unsigned long long)std::ldexp(p, 64); }
+
 struct DemandArgs {
   CUtensorMap kmap;        // K cache as [rows][D] bf16, box 64 x 128, 128-byte swizzle
   int variant;             // DEMAND_FFMA or DEMAND_TC
@@ -70,7 +75,7 @@ struct DemandArgs {
   int num_pages_total;
   int L, Hkv, D, G;
   int b, R;
-  double p;
+  unsigned long long pfix; // coverage p as a binary fraction, floor(p 2^64)
   const float* qt;
   const unsigned char* bq; // tensor-core operand per unit (prep kernel output)
   const DevReq* reqs;

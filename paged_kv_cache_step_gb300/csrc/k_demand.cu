@@ -248,13 +248,15 @@ __global__ void __launch_bounds__(NT, 2) k_demand_ffma(const __grid_constant__ D
 
   // ---- 4. D_p, by the unit's last CTA -------------------------------------
   if (!last_of_unit(a, u, flag)) return;
-  unsigned k = 0;
-  if (u.ndem > 0) {
-    const float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
-    k = coverage_demand<NT, 0>(av, u.ndem, a.p, reinterpret_cast<unsigned*>(zb), a.ppc * PAGE * ROWS, dps, a.err, tid,
-                               0u, 0u);
+  for (int x = 0; x < 2; ++x) {
+    unsigned k = 0;
+    if (u.ndem > 0) {
+      const float* av = a.aval + u.rq.aval_off + ((size_t)u.unit * 2 + x) * u.ndem;
+      k = coverage_demand<NT, 0>(av, u.ndem, a.pfix, reinterpret_cast<unsigned*>(zb), a.ppc * PAGE * ROWS, dps, a.err,
+                                 tid, 0u, 0u);
+    }
+    if (tid == 0) write_demand(a, u.r, u.unit, x, k);
   }
-  write_demand(a, u.r, u.unit, tid, k);
 }
 
 template <bool BF16, int D, int ROWS>

@@ -36,9 +36,11 @@
 //               memory, completing on their mbarriers), the merge, then a^S,
 //               a^L and the importance of every key to global memory, and
 //               a ticket per unit in global memory;
-//   warps 10..15 selector: rank k mod C computes the D_p of the cluster's
-//               k-th unit once all C tickets are in -- the exact radix select
-//               of demand_common.cuh, on the SM's otherwise idle issue slots.
+//   warps 10..15 selector: rank (k + x) mod C computes D_p of summary x of
+//               the cluster's k-th unit once all C tickets are in -- the
+//               exact select of demand_common.cuh, on the SM's otherwise idle
+//               issue slots; each cluster's last unit is left to the whole
+//               CTA once its scan is over (nothing is left to hide it behind).
 // Every wait is bounded; on expiry the CTA records ERR_TIMEOUT, raises a
 // shared abort flag that ends every role's loop, drains its copies in
 // flight and finishes with garbage rather than hanging.
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
       __nanosleep(200);
     }
     if (item >= 0) {
-      const UnitInfo u = unit_info(a, item, 0);
+      const UnitInfo u = unit_info(a, item >> 1, 0);
       const unsigned* tk = a.tickets + (size_t)u.r * units + u.unit;
       const long long t1 = clock64();
       while (ld_acquire(tk) < (unsigned)C) {
@@ -591,8 +593,10 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
         // the CTA's a-values (ordered by the barrier above) before its ticket
         __threadfence();
         atomicAdd(a.tickets + (size_t)u.r * units + u.unit, 1u);
-        if (kk % C == crank) {
-          // this rank computes the unit's D_p: queue it for the selector warps
+        // D_p of summary x is computed by rank (kk + x) mod C: queue it for
+        // this rank's selector warps
+        for (int x = 0; x < 2; ++x) {
+          if ((kk + x) % C != crank) continue;
           const long long t0 = clock64();
           while (*q_head - *q_tail >= QLEN) {
             if (*abort || clock64() - t0 > kWaitLimit) {
@@ -601,17 +605,16 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
               break;
             }
           }
-          if (!*abort) {
-            // the cluster's last unit: no scan is left to hide its select behind,
-            // so the selector warps stop here and the whole CTA drains it
-            if (w + nclus >= total_units) {
-              *q_done = 1;
-              __threadfence_block();
-            }
-            queue[*q_head % QLEN] = w;
+          if (*abort) break;
+          // the cluster's last unit: no scan is left to hide its select behind,
+          // so the selector warps stop here and the whole CTA drains it
+          if (w + nclus >= total_units) {
+            *q_done = 1;
             __threadfence_block();
-            *q_head = *q_head + 1;
           }
+          queue[*q_head % QLEN] = 2 * w + x;
+          __threadfence_block();
+          *q_head = *q_head + 1;
         }
       }
     }
@@ -628,16 +631,17 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     while (true) {
       if (st == 0) *sel_item = take_item(true);
       sel_sync<SEL_NTH, BAR_SEL>();
-      const int w = *sel_item;
-      if (w < 0) break;
-      const UnitInfo u = unit_info(a, w, 0);
+      const int item = *sel_item;
+      if (item < 0) break;
+      const int x = item & 1;
+      const UnitInfo u = unit_info(a, item >> 1, 0);
       unsigned k = 0;
       if (u.ndem > 0) {
-        const float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
-        k = coverage_demand<SEL_NTH, BAR_SEL>(av, u.ndem, a.p, selbuf, sel_cap, dps, a.err, st, bar_sel, sel_par);
-        if (2 * u.ndem <= sel_cap) sel_par ^= 1u;
+        const float* av = a.aval + u.rq.aval_off + ((size_t)u.unit * 2 + x) * u.ndem;
+        k = coverage_demand<SEL_NTH, BAR_SEL>(av, u.ndem, a.pfix, selbuf, sel_cap, dps, a.err, st, bar_sel, sel_par);
+        if (sel_resident(u.ndem, sel_cap)) sel_par ^= 1u;
       }
-      write_demand(a, u.r, u.unit, st, k);
+      if (st == 0) write_demand(a, u.r, u.unit, x, k);
       sel_sync<SEL_NTH, BAR_SEL>();
       if (st == 0) *q_tail = *q_tail + 1;
     }
@@ -654,16 +658,17 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     while (true) {
       if (tid == 0) *sel_item = take_item(false);
       __syncthreads();
-      const int w = *sel_item;
-      if (w < 0) break;
-      const UnitInfo u = unit_info(a, w, 0);
+      const int item = *sel_item;
+      if (item < 0) break;
+      const int x = item & 1;
+      const UnitInfo u = unit_info(a, item >> 1, 0);
       unsigned k = 0;
       if (u.ndem > 0) {
-        const float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
-        k = coverage_demand<NTHR, 0>(av, u.ndem, a.p, selbuf, sel_cap, dps, a.err, tid, bar_sel, par);
-        if (2 * u.ndem <= sel_cap) par ^= 1u;
+        const float* av = a.aval + u.rq.aval_off + ((size_t)u.unit * 2 + x) * u.ndem;
+        k = coverage_demand<NTHR, 0>(av, u.ndem, a.pfix, selbuf, sel_cap, dps, a.err, tid, bar_sel, par);
+        if (sel_resident(u.ndem, sel_cap)) par ^= 1u;
       }
-      write_demand(a, u.r, u.unit, tid, k);
+      if (tid == 0) write_demand(a, u.r, u.unit, x, k);
       __syncthreads();
       if (tid == 0) *q_tail = *q_tail + 1;
     }

@@ -226,7 +226,7 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
       da.G = G;
       da.b = kPage;
       da.R = g.recent_window;
-      da.p = g.p;
+      da.pfix = gp::coverage_fraction(g.p);
       da.qt = pa.qt;
       da.bq = pa.bq;
       da.reqs = pa.reqs;
