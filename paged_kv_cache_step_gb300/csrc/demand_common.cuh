@@ -59,8 +59,8 @@ __device__ __forceinline__ Unit make_unit(const DemandArgs& a) {
   u.P = u.rq.num_pages;
   u.ndem = (u.P - 1) * PAGE;
   u.ncmp = u.P * PAGE - a.R;
-  u.j0 = u.crank * a.ppc;
-  u.npg = max(0, min(u.P, u.j0 + a.ppc) - u.j0);
+  u.j0 = (u.crank * u.P) / a.C;  // balanced range: at most ceil(P / C) <= ppc pages
+  u.npg = ((u.crank + 1) * u.P) / a.C - u.j0;
   return u;
 }
 

@@ -98,25 +98,57 @@ inline cudaError_t launch_demand(const DemandArgs& a, cudaStream_t s) {
   return a.variant == DEMAND_TC ? launch_demand_tc(a, s) : launch_demand_ffma(a, s);
 }
 
-// How a request of P pages is split: kernel variant, pages per CTA (ppc) and
-// CTAs per cluster (C).  The tensor-core variant keeps two units of a CTA's
-// logits in TMEM (2G columns per 128 keys) beside its accumulator slots, so
-// it takes up to 8 pages per CTA and 16 CTAs per cluster: P <= 128.  Eight
-// pages per CTA keep clusters small, and small clusters fill the GPCs
-// (clusters of 4 occupy 144 of 152 SMs, clusters of 8 only 120).
+// Clusters of C CTAs of the tensor-core demand kernel (head dim D, GQA
+// group G) that the current device runs at once; at least 1.
+int demand_tc_cluster_fit(int D, int G, int C);
+
+// How a request of P pages is split: kernel variant, CTAs per cluster (C)
+// and the most pages one CTA scores (ppc).  CTA c of a unit's cluster scores
+// the balanced range of logical pages [c P / C, (c + 1) P / C), so no rank
+// idles on a short remainder.
+//
+// The tensor-core variant keeps two units of a CTA's logits in TMEM (2G
+// columns per 128 keys) beside its accumulator slots: at most TC_MAX_PPC
+// pages per CTA and 16 CTAs per cluster, so P <= 128 (it needs C >= P / 10).
+// Its C minimises a makespan model of the launch: a cluster takes units in
+// turn, so U units run ceil(U / fit(C)) rounds, each of ceil(P / C) pages
+// per CTA plus about one page's worth of per-unit epilogue.  fit(C) is how
+// many clusters of C CTAs the device holds at once (clusters stay inside a
+// GPC, so for some C a good part of the 152 SMs stays empty).  Ties go to
+// the smaller cluster (a cheaper statistics exchange).
+//
+// The CUDA-core variant keeps its logits in shared memory: 8 pages per CTA
+// up to 128 pages, 16 beyond (P <= 256).
+constexpr int TC_MAX_PPC = 10;
 struct DemandPlan {
   int variant, ppc, C;
 };
-inline DemandPlan demand_plan(int P, bool tc_ok) {
+inline DemandPlan demand_plan(int P, bool tc_ok, int D, int G, long long units) {
   DemandPlan pl;
   if (tc_ok && P <= 128) {
     pl.variant = DEMAND_TC;
-    pl.ppc = 8;
+    const int c_lo = P <= 1 ? 1 : (P + TC_MAX_PPC - 1) / TC_MAX_PPC;
+    const int c_hi = P < 16 ? (P < 1 ? 1 : P) : 16;
+    long long best = -1;
+    pl.C = c_lo;
+    for (int C = c_lo; C <= c_hi; ++C) {
+      const long long fit = demand_tc_cluster_fit(D, G, C);
+      if (fit < 1) continue;
+      const long long rounds = (units + fit - 1) / fit;
+      const long long cost = rounds * ((P + C - 1) / C + 1);
+      if (best < 0 || cost < best) {
+        best = cost;
+        pl.C = C;
+      }
+    }
   } else {
     pl.variant = DEMAND_FFMA;
-    pl.ppc = P <= 128 ? 8 : 16;
+    const int ppc = P <= 128 ? 8 : 16;
+    pl.C = (P + ppc - 1) / ppc;
+    if (pl.C < 1) pl.C = 1;
   }
-  pl.C = (P + pl.ppc - 1) / pl.ppc;
+  pl.ppc = (P + pl.C - 1) / pl.C;
+  if (pl.ppc < 1) pl.ppc = 1;
   return pl;
 }
 

@@ -539,15 +539,19 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   if ((st = ensure(c, c->kout, sizeof(int32_t) * (size_t)n * units * 2)) != GP_OK) return st;
   if ((st = ensure(c, c->ksum, sizeof(unsigned long long) * (size_t)n * 2)) != GP_OK) return st;
 
-  // work buckets: (variant, cluster size C, pages per CTA), one launch each
+  // work buckets: (variant, cluster size C), one launch each; a launch's
+  // ppc bounds the pages any CTA of it scores
   const bool tc = c->tc_ok && c->scan_kernel != GP_SCAN_CUDA_CORE;
-  std::map<std::tuple<int, int, int>, std::vector<int32_t>> buckets;
+  std::map<std::tuple<int, int>, std::vector<int32_t>> buckets;
+  std::map<std::tuple<int, int>, int> bucket_ppc;
   for (int r = 0; r < n; ++r) {
-    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, tc);
+    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, tc, g.head_dim, G, units);
     if (c->scan_kernel == GP_SCAN_TENSOR_CORE && pl.variant != gp::DEMAND_TC)
       return fail(c, GP_ERR_UNSUPPORTED, "request %d: the tensor-core scan needs a bf16 cache and at most 128 pages",
                   r);
-    buckets[{pl.variant, pl.C, pl.ppc}].push_back(r);
+    buckets[{pl.variant, pl.C}].push_back(r);
+    int& mp = bucket_ppc[{pl.variant, pl.C}];
+    mp = std::max(mp, pl.ppc);
   }
   for (int r = 0; r < n; ++r) {
     gp::DevReq& d = s.reqs[r];
@@ -567,7 +571,7 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   std::vector<Launch> launches;
   int wpos = 0;
   for (auto it = buckets.rbegin(); it != buckets.rend(); ++it) {  // largest clusters first
-    launches.push_back({std::get<0>(it->first), std::get<1>(it->first), std::get<2>(it->first), wpos,
+    launches.push_back({std::get<0>(it->first), std::get<1>(it->first), bucket_ppc[it->first], wpos,
                         (int)it->second.size()});
     for (int32_t r : it->second) s.work[wpos++] = r;
   }

@@ -4,8 +4,8 @@
 // caches up to 128 pages take the tcgen05 variant (k_demand_tc.cu).
 //
 // Work unit: one (request, layer, KV head), owned by a cluster of C CTAs;
-// CTA c scores logical pages [c*ppc, (c+1)*ppc) and keeps its logits in
-// shared memory, so K is read from HBM once:
+// CTA c scores the balanced page range [c P / C, (c+1) P / C) (at most ppc
+// pages) and keeps its logits in shared memory, so K is read from HBM once:
 //   1. scan     -- 16-byte streaming loads of K rows (a lane pair per key,
 //                  each lane half of the row's 16-byte chunks, so a warp load
 //                  covers whole 32-byte sectors), fp32 FMA against the 2G

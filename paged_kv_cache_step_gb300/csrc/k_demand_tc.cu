@@ -17,7 +17,7 @@
 //
 // Persistent and warp-specialised.  A cluster of C CTAs (one CTA per SM)
 // takes units (request, layer, KV head) g, g + #clusters, ...; in each, CTA
-// rank c scores logical pages [c*ppc, (c+1)*ppc).  Roles:
+// rank c scores the balanced page range [c P / C, (c+1) P / C).  Roles:
 //   warp 0      producer: per unit, the B operand (bulk copy) and the K tiles
 //               (128 keys x d, box 64 x 128 with the 128-byte swizzle)
 //               through an NSTAGE mbarrier ring, running ahead across units;
@@ -64,6 +64,9 @@ constexpr int BAR_EPI = 1;      // named barriers
 constexpr int BAR_SEL = 2;
 constexpr int QLEN = 32;        // select queue
 constexpr long long kWaitLimit = 1ll << 31;  // clock cycles (about one second)
+#ifndef GP_TC_STAGE_BYTES
+#define GP_TC_STAGE_BYTES (96 * 1024)  // bytes of K tiles in flight per CTA (one CTA per SM)
+#endif
 
 template <int D, int ROWS>
 struct TcCfg {
@@ -73,8 +76,8 @@ struct TcCfg {
   static constexpr int HALF_BYTES = 128 * 128;           // one 64-element span of 128 keys
   static constexpr int BQ_BYTES = HALVES * NB * 128;
   static constexpr int KSTEPS = D / 16;
-  static constexpr int NSTAGE = (96 * 1024) / TILE_BYTES;  // 96 KiB of K in flight per SM
-  static constexpr int TPU = 16;                         // tiles per unit and CTA at most (8 pages)
+  static constexpr int NSTAGE = GP_TC_STAGE_BYTES / TILE_BYTES;  // K in flight per SM
+  static constexpr int TPU = 2 * TC_MAX_PPC;             // tiles per unit and CTA at most (10 pages)
   static constexpr int WSLOTS = (512 - 2 * TPU * ROWS) / NB;  // accumulator slots; the rest holds
   static constexpr int CBASE = WSLOTS * NB;              // two units of compact logits from here
   static_assert(CBASE + 2 * TPU * ROWS <= 512 && WSLOTS >= 4, "TMEM layout");
@@ -255,8 +258,8 @@ __device__ __forceinline__ UnitInfo unit_info(const DemandArgs& a, int w, int cr
   u.P = u.rq.num_pages;
   u.ndem = (u.P - 1) * PAGE;
   u.ncmp = u.P * PAGE - a.R;
-  u.j0 = crank * a.ppc;
-  u.npg = max(0, min(u.P, u.j0 + a.ppc) - u.j0);
+  u.j0 = (crank * u.P) / a.C;
+  u.npg = ((crank + 1) * u.P) / a.C - u.j0;
   return u;
 }
 
@@ -682,7 +685,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
   }
 }
 
-// Clusters of this shape that fit on the GPU at once.
+// Clusters of this shape that fit on the GPU at once; 0 if none does.
 template <typename K>
 int max_clusters(K kern, int C, size_t smem) {
   cudaLaunchConfig_t cfg = {};
@@ -699,35 +702,59 @@ int max_clusters(K kern, int C, size_t smem) {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
-    n = 1;
+    n = 0;
   }
   return n;
+}
+
+// The kernel's launch attributes (set once) and its dynamic shared memory:
+// the whole opt-in amount, so that one CTA owns an SM, its TMEM (512
+// columns) and the select buffer.  0 if the device cannot hold the layout.
+template <int D, int ROWS>
+size_t prepare_t() {
+  using S = TcSmem<D, ROWS>;
+  static size_t smem = 0;
+  if (smem) return smem;
+  int dev = 0, max_optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      (size_t)max_optin < S::MIN_BYTES) {
+    cudaGetLastError();
+    return 0;
+  }
+  auto kern = k_demand_tc<D, ROWS>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  smem = (size_t)max_optin;
+  return smem;
+}
+
+template <int D, int ROWS>
+int fit_t(int C) {
+  static int fit_cache[17] = {};  // per kernel instantiation and cluster size
+  if (C < 1 || C > 16) return 0;
+  if (!fit_cache[C]) {
+    const size_t smem = prepare_t<D, ROWS>();
+    if (!smem) return 0;
+    fit_cache[C] = max_clusters(k_demand_tc<D, ROWS>, C, smem);
+  }
+  return fit_cache[C];
 }
 
 template <int D, int ROWS>
 cudaError_t launch_t(const DemandArgs& a, cudaStream_t s) {
   using T = TcCfg<D, ROWS>;
-  using S = TcSmem<D, ROWS>;
   if (2 * a.ppc > T::TPU) return cudaErrorInvalidValue;  // a unit's compact logits must fit TMEM
-  int dev = 0, max_optin = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e != cudaSuccess) return e;
-  // the whole opt-in shared memory: one CTA per SM, so TMEM (512 columns)
-  // and the select buffer are the CTA's alone
-  const size_t smem = (size_t)max_optin;
-  if (smem < S::MIN_BYTES) return cudaErrorInvalidValue;
+  if (a.ppc * a.C < 1) return cudaErrorInvalidValue;
+  const size_t smem = prepare_t<D, ROWS>();
+  if (!smem) return cudaErrorInvalidValue;
   auto kern = k_demand_tc<D, ROWS>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (a.C > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
   const int total = a.n_work * a.L * a.Hkv;
-  static int fit_cache[17] = {};  // per kernel instantiation and cluster size
-  if (!fit_cache[a.C]) fit_cache[a.C] = max_clusters(kern, a.C, smem);
-  int nclus = fit_cache[a.C];
+  int nclus = fit_t<D, ROWS>(a.C);
+  if (nclus < 1) return cudaErrorInvalidValue;
   if (nclus > total) nclus = total;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.C * nclus), 1, 1);
@@ -745,6 +772,14 @@ cudaError_t launch_t(const DemandArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+int demand_tc_cluster_fit(int D, int G, int C) {
+  if (D == 128 && G == 4) return fit_t<128, 8>(C);
+  if (D == 128 && G == 2) return fit_t<128, 4>(C);
+  if (D == 64 && G == 4) return fit_t<64, 8>(C);
+  if (D == 64 && G == 2) return fit_t<64, 4>(C);
+  return 0;
+}
 
 cudaError_t launch_demand_tc(const DemandArgs& a, cudaStream_t s) {
   if (a.n_work == 0) return cudaSuccess;

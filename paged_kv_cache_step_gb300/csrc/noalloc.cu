@@ -154,30 +154,30 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   }
   unsigned char* base = g_scratch_addr[dev];
 
-  // ---- work buckets (scan variant, pages per CTA, cluster size C) ----------
-  // Key k = 2 * variant + wide: demand_plan gives each variant two CTA widths
-  // (tensor core 4 or 8 pages, CUDA core 8 or 16).
-  const int ppc_of[4] = {8, 16, 4, 8};
-  int bucket_count[4][17] = {};
-  auto key_of = [&](const gp::DemandPlan& pl) { return 2 * pl.variant + (pl.ppc == ppc_of[2 * pl.variant + 1]); };
+  // ---- work buckets (scan variant, cluster size C), as gp_boundary_demand --
+  // forms them; a bucket's ppc bounds the pages any CTA of its launch scores.
+  int bucket_count[2][17] = {};
+  int bucket_ppc[2][17] = {};
   for (int r = 0; r < n; ++r) {
-    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok);
+    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok, g.head_dim, G, units);
     if (v.scan_kernel == GP_SCAN_TENSOR_CORE && pl.variant != gp::DEMAND_TC)
       return fail(c, GP_ERR_UNSUPPORTED, "request %lld: the tensor-core scan cannot serve it", r);
-    bucket_count[key_of(pl)][pl.C] += 1;
+    if (pl.C < 1 || pl.C > 16) return fail(c, GP_ERR_UNSUPPORTED, "request %lld: cluster size %lld", r, pl.C);
+    bucket_count[pl.variant][pl.C] += 1;
+    if (pl.ppc > bucket_ppc[pl.variant][pl.C]) bucket_ppc[pl.variant][pl.C] = pl.ppc;
   }
-  int bucket_start[4][17];
+  int bucket_start[2][17];
   int pos = 0;
-  for (int k = 3; k >= 0; --k)
+  for (int k = 1; k >= 0; --k)
     for (int C = 16; C >= 1; --C) {
       bucket_start[k][C] = pos;
       pos += bucket_count[k][C];
     }
-  int fill[4][17];
+  int fill[2][17];
   memcpy(fill, bucket_start, sizeof(fill));
   for (int r = 0; r < n; ++r) {
-    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok);
-    g_work[fill[key_of(pl)][pl.C]++] = r;
+    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok, g.head_dim, G, units);
+    g_work[fill[pl.variant][pl.C]++] = r;
   }
 
   // ---- uploads (from the caller's / static host memory; no staging buffers) --
@@ -210,10 +210,10 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   e = gp::launch_prep(pa, s);
   if (e != cudaSuccess) return cuda_fail(c, "prep_queries launch", e);
 
-  for (int k = 3; k >= 0; --k)
+  for (int k = 1; k >= 0; --k)
     for (int C = 16; C >= 1; --C) {
       if (!bucket_count[k][C]) continue;
-      const int var = k / 2;
+      const int var = k;
       gp::DemandArgs da{};
       if (var == gp::DEMAND_TC) da.kmap = *v.kmap;
       da.variant = var;
@@ -234,7 +234,7 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
       da.work = reinterpret_cast<const int32_t*>(base + off_work) + bucket_start[k][C];
       da.n_work = bucket_count[k][C];
       da.C = C;
-      da.ppc = ppc_of[k];
+      da.ppc = bucket_ppc[k][C];
       da.scores = reinterpret_cast<float*>(base + off_sc);
       da.aval = reinterpret_cast<float*>(base + off_sc);
       da.tickets = reinterpret_cast<unsigned*>(base + off_tk);

@@ -17,6 +17,17 @@ Recipe (the same for every configuration; sizes per configuration below):
 * Physical pages are a seeded permutation of the pool; block tables take
   consecutive runs of it.
 
+* Continuous-batching stream (``stream256``): 256 seats in 32 prefix groups
+  of 8.  A group's members share a 32-page prefix (one reference per
+  member) and a direction u (their queries follow one topic); each request
+  adds a private part of lognormal length (median 2048 tokens, sigma 1.0,
+  clipped to 512..16384, rounded up to whole pages) and finishes after a
+  geometric number of boundary events (mean 12).  A seat's queries
+  alternate 64-step concentrated and diffuse phases from a seeded offset.
+  The free pool holds a bounded number of spare pages beyond the initial
+  allocation (256).  The request lifecycle that uses these draws lives in
+  synth/stream.py.
+
 Seeds: ``0x47505047 ^ config_id``.
 """
 
@@ -313,6 +324,74 @@ def _batch(device, name="batch64", shape=LLAMA8B, n=64, p_lo=4, p_hi=128,
     return w
 
 
+STREAM_DEFAULTS = dict(seats=256, group=8, prefix_pages=32, spare_pages=256, median_tokens=2048,
+                       sigma=1.0, min_tokens=512, max_tokens=16384, mean_events=12, phase_len=64,
+                       max_pages=128)
+
+
+def private_pages(hgen, n: int, median_tokens=2048, sigma=1.0, min_tokens=512, max_tokens=16384,
+                  page_size=256) -> list:
+    """Private-part lengths in pages: lognormal tokens, clipped, rounded up."""
+    z = torch.randn(n, generator=hgen, dtype=torch.float64)
+    tok = torch.exp(math.log(median_tokens) + sigma * z).clamp(min_tokens, max_tokens)
+    return torch.ceil(tok / page_size).to(torch.int64).tolist()
+
+
+def event_counts(hgen, n: int, mean: float = 12.0) -> list:
+    """Boundary events before a request finishes: geometric on {1, 2, ...}."""
+    u = torch.rand(n, generator=hgen, dtype=torch.float64).clamp_min(1e-300)
+    q = 1.0 - 1.0 / mean
+    return (torch.floor(torch.log(u) / math.log(q)) + 1).to(torch.int64).tolist()
+
+
+def _stream(device, shape=LLAMA8B, **kw):
+    """Initial state of the continuous-batching stream (config 5).
+
+    Pages [0, G * prefix) are the groups' prefixes, then each seat's private
+    pages in seat order, then the spare pages.  ``extra`` holds the recipe
+    parameters, the groups' prefix pages and the seeded per-seat draws the
+    lifecycle consumes (phase offsets, event counts).
+    """
+    p = dict(STREAM_DEFAULTS)
+    p.update({k: v for k, v in kw.items() if k in STREAM_DEFAULTS})
+    sh = shape
+    b = 256
+    gen, hgen = _gens(device, config_seed("stream256") ^ kw.get("seed_xor", 0))
+    seats, group, npre = p["seats"], p["group"], p["prefix_pages"]
+    ngroups = (seats + group - 1) // group
+    priv = private_pages(hgen, seats, p["median_tokens"], p["sigma"], p["min_tokens"], p["max_tokens"], b)
+    priv = [min(x, p["max_pages"] - npre - 1) for x in priv]
+    prefixes = [list(range(g * npre, (g + 1) * npre)) for g in range(ngroups)]
+    nxt = ngroups * npre
+    bts = []
+    for s_ in range(seats):
+        bts.append(prefixes[s_ // group] + list(range(nxt, nxt + priv[s_])))
+        nxt += priv[s_]
+    num_pages = nxt + p["spare_pages"]
+    k = _random_cache(sh, num_pages, b, gen, device)
+    v = _random_cache(sh, num_pages, b, gen, device)
+    ug = low_freq_directions((ngroups, sh.num_layers, sh.num_kv_heads), sh.head_dim, gen, device)
+    u = ug.repeat_interleave(group, dim=0)[:seats].contiguous()
+    conc = torch.ones(seats, sh.num_layers, sh.num_kv_heads, dtype=torch.bool, device=device)
+    w = Workload("stream256", sh, b, num_pages, k, v, bts, [len(t) * b for t in bts], u, conc, gen, hgen,
+                 phase_len=p["phase_len"])
+    for g in range(ngroups):
+        _plant(w, g * group, prefixes[g])
+    for s_ in range(seats):
+        _plant(w, s_, bts[s_][npre:])
+    w.extra.update(p)
+    w.extra["prefixes"] = prefixes
+    w.extra["phase_offset"] = torch.randint(0, 2 * p["phase_len"], (seats,), generator=hgen).tolist()
+    w.extra["events"] = event_counts(hgen, seats, p["mean_events"])
+    return w
+
+
+def stream_kinds(w: Workload, step: int) -> list:
+    """Per seat: True if its query at this step is a concentrated one."""
+    L = w.extra["phase_len"]
+    return [((step + off) // L) % 2 == 0 for off in w.extra["phase_offset"]]
+
+
 def make_workload(name: str, device="cpu", **kw) -> Workload:
     """Build configuration ``name`` on ``device`` (see CONFIGS)."""
     if name == "tiny":
@@ -328,6 +407,8 @@ def make_workload(name: str, device="cpu", **kw) -> Workload:
         kw.setdefault("spare_per_req", 1)
         return _batch(device, name="qwen3_8b", shape=QWEN3_8B, conc_prob=0.3,
                       **kw)
+    if name == "stream256":
+        return _stream(device, **kw)
     if name == "custom":
         # explicit shape and request sizes: kw shape=ModelShape, sizes=[P, ...]
         return _batch(device, name="custom", **kw)
