@@ -216,15 +216,24 @@ def query_step(w: Workload, kinds) -> torch.Tensor:
 
 def fill_page(w: Workload, req: int, phys_page: int):
     """Write a fresh page of tokens (N(0,1), planted like the rest)."""
+    fill_pages(w, req, [phys_page])
+
+
+def fill_pages(w: Workload, req: int, phys_pages):
+    """Write fresh tokens into several pages of request ``req`` at once."""
     sh = w.shape
     dev = w.device
+    pages = list(phys_pages)
+    if not pages:
+        return
+    idx = torch.as_tensor(pages, device=dev, dtype=torch.long)
     for cache in (w.k_cache, w.v_cache):
-        blk = torch.randn(sh.num_layers, sh.num_kv_heads, w.page_size,
+        blk = torch.randn(sh.num_layers, len(pages), sh.num_kv_heads, w.page_size,
                           sh.head_dim, generator=w.gen, device=dev)
         if sh.qk_norm:
             blk = _unit_rms(blk)
-        cache[:, phys_page] = blk.to(cache.dtype)
-    _plant(w, req, [phys_page])
+        cache.index_copy_(1, idx, blk.to(cache.dtype))
+    _plant(w, req, pages)
 
 
 # ---------------------------------------------------------------------------
