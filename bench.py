@@ -356,6 +356,175 @@ def run_gpu(args, world, rank, local):
 
 
 # ---------------------------------------------------------------------------
+# the other configurations (one JSON line each; not the default line)
+# ---------------------------------------------------------------------------
+
+def _engine_over(gp, w, stream, max_slots, max_pages, policy):
+    sh = w.shape
+    cfg = gp.gp_config_default(
+        num_layers=sh.num_layers, num_q_heads=sh.num_q_heads, num_kv_heads=sh.num_kv_heads,
+        head_dim=sh.head_dim, kv_dtype=gp.GP_DTYPE_BF16, q_dtype=gp.GP_DTYPE_BF16,
+        max_slots=max_slots, num_pages=w.num_pages, max_pages_per_req=max_pages, rope_theta=sh.rope_theta)
+    if policy == "fixed":
+        cfg.policy = gp.GP_POLICY_FIXED
+    return cfg, gp.gp_create(cfg, w.k_cache, w.v_cache, stream)
+
+
+def _kernel_report(gp, ctx, peak, scan_bytes, comp_bytes):
+    kern, rl = {}, {}
+    for k, name in gp.KERNEL_NAMES.items():
+        ms, n = gp.gp_kernel_time(ctx, k)
+        kern[name] = {"ms": ms, "launches": n}
+    for name, nbytes in (("boundary_demand", scan_bytes), ("compress_hold", comp_bytes)):
+        k = kern[name]
+        if k["launches"] and k["ms"] > 0:
+            a = nbytes / (k["ms"] / 1e3) / 1e9
+            rl[name] = {"bound": "hbm", "achieved": a, "peak": peak, "unit": "GB/s", "frac": a / peak,
+                        "bytes_per_launch": nbytes / k["launches"], "ms_per_launch": k["ms"] / k["launches"]}
+            k.update(frac=a / peak, achieved_gbs=a)
+    dom = max(rl, key=lambda n: kern[n]["ms"]) if rl else None
+    return kern, rl, dom
+
+
+def run_batch(args, device):
+    """64 requests (or 16 Qwen3-like ones) all at a boundary: per step the
+    summary update, one demand call over every request, the decision and
+    the actions (Grow, or Compress & Hold of every compressing request)."""
+    import paged_kv_cache_step_gb300 as gp
+    peak, peak_src = _peaks()
+    w = synth.make_workload(args.workload, device=device)
+    sh = w.shape
+    ts = torch.cuda.Stream(device=device)
+    cfg, ctx = _engine_over(gp, w, ts, max(4, w.n), 256, args.policy)
+    used = set(p for t in w.block_tables for p in t)
+    for _ in range(w.num_pages):
+        gp.gp_page_alloc(ctx)
+    for pg in range(w.num_pages):
+        if pg not in used:
+            gp.gp_page_unref(ctx, pg)
+    reqs = [gp.Request(gp.gp_slot_acquire(ctx), t, w.positions[r], 256) for r, t in enumerate(w.block_tables)]
+    slots = torch.tensor([q.slot for q in reqs], dtype=torch.int32, device=device)
+    first = torch.ones(w.n, dtype=torch.uint8, device=device)
+    notfirst = torch.zeros(w.n, dtype=torch.uint8, device=device)
+    units = sh.num_layers * sh.num_kv_heads
+    row = sh.head_dim * 2
+    for t, q in enumerate(w.history):
+        with torch.cuda.stream(ts):
+            ts.wait_stream(torch.cuda.current_stream())
+            gp.gp_update_summaries(ctx, w.n, slots, q, first if t == 0 else notfirst)
+    torch.cuda.synchronize()
+
+    def one_step(q):
+        with torch.cuda.stream(ts):
+            gp.gp_update_summaries(ctx, w.n, slots, q, notfirst)
+        scan = sum((r.num_pages * PAGE - 16) * units * row for r in reqs)
+        dem = gp.gp_boundary_demand(ctx, reqs, q)
+        acts = gp.gp_decide(ctx, reqs, dem)
+        comp = []
+        for r, a in zip(reqs, acts):
+            if a.kind == gp.GP_ACT_GROW:
+                gp.gp_grow_page(ctx, r)
+            else:
+                comp.append(r)
+        if comp:
+            gp.gp_compress_hold(ctx, comp)
+        return scan, len(comp)
+
+    qs = [synth.query_step(w, [True] * w.n) for _ in range(args.warmup + args.steps)]
+    for i in range(args.warmup):
+        one_step(qs[i])
+    torch.cuda.synchronize()
+    gp.gp_reset_timing(ctx)
+    gp.gp_set_timing(ctx, 1)
+    moved0 = gp.gp_stats(ctx)["moved_rows"]
+    clocks = Clocks(device.index or 0, os.path.join(tempfile.gettempdir(), f"growpage_clk_{os.getpid()}.csv"))
+    times, scan_bytes, ncomp = [], 0, 0
+    for i in range(args.steps):
+        q = qs[args.warmup + i]
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(ts)
+        sb, nc = one_step(q)
+        ev1.record(ts)
+        torch.cuda.synchronize()
+        times.append(ev0.elapsed_time(ev1))
+        scan_bytes += sb
+        ncomp += nc
+    clk = clocks.stop()
+    gp.gp_set_timing(ctx, 0)
+    comp_bytes = (gp.gp_stats(ctx)["moved_rows"] - moved0) * row * 4
+    kern, rl, dom = _kernel_report(gp, ctx, peak, scan_bytes, comp_bytes)
+    gp.gp_destroy(ctx)
+    total = sum(times)
+    launches = sum(k["launches"] for k in kern.values())
+    return {
+        "metric": METRIC, "value": args.steps * w.n / (total / 1e3), "unit": "events/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {synth.CONFIGS[args.workload][2]}; policy {args.policy}",
+                   "l2": "inputs larger than L2"},
+        "kv_gbs": (scan_bytes + comp_bytes) / (total / 1e3) / 1e9,
+        "scan_bytes": scan_bytes, "compaction_bytes": comp_bytes, "compress_events": ncomp,
+        "roofline": dict(rl[dom], kernel=dom, peak_source=peak_src, traffic=None) if dom else None,
+        "kernels": kern, "gpu_launches": launches, "clocks": clk}
+
+
+def run_stream(args, device):
+    """The continuous-batching stream: value = boundary events per second of
+    engine device time (every engine kernel, timed per launch on its stream);
+    the loop's synthetic page fills and host bookkeeping are not engine work."""
+    import paged_kv_cache_step_gb300 as gp
+    from synth.stream import ContinuousBatch
+    peak, peak_src = _peaks()
+    w = synth.make_workload("stream256", device=device)
+    ts = torch.cuda.Stream(device=device)
+    cfg, ctx = _engine_over(gp, w, ts, 256, 128, "growpage")
+    drv = ContinuousBatch(gp, ctx, w, 128)
+    units = cfg.num_layers * cfg.num_kv_heads
+    row = cfg.head_dim * 2
+    scan = [0]
+
+    class Hooks:
+        def post_demand(self, d, t, bseats, q_b, dem, acts):
+            scan[0] += sum((d.seats[s].req.num_pages * PAGE - 16) * units * row for s in bseats)
+
+    with torch.cuda.stream(ts):
+        for t in range(args.warmup):
+            drv.step(t)
+        torch.cuda.synchronize()
+        gp.gp_reset_timing(ctx)
+        gp.gp_set_timing(ctx, 1)
+        b0, moved0 = drv.counts["boundary"], gp.gp_stats(ctx)["moved_rows"]
+        clocks = Clocks(device.index or 0, os.path.join(tempfile.gettempdir(), f"growpage_clk_{os.getpid()}.csv"))
+        t0 = time.perf_counter()
+        for t in range(args.warmup, args.warmup + args.steps):
+            drv.step(t, hooks=Hooks())
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        clk = clocks.stop()
+    gp.gp_set_timing(ctx, 0)
+    events = drv.counts["boundary"] - b0
+    comp_bytes = (gp.gp_stats(ctx)["moved_rows"] - moved0) * row * 4
+    kern, rl, dom = _kernel_report(gp, ctx, peak, scan[0], comp_bytes)
+    dev_ms = sum(k["ms"] for k in kern.values())
+    counts = dict(drv.counts)
+    gp.gp_destroy(ctx)
+    return {
+        "metric": METRIC, "value": events / (dev_ms / 1e3), "unit": "events/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dev_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "stream256: " + synth.CONFIGS["stream256"][2],
+                   "timing": "engine device time (sum of per-launch CUDA events); step wall time separate"},
+        "boundary_events": events, "wall_s": wall, "kv_gbs": (scan[0] + comp_bytes) / (dev_ms / 1e3) / 1e9,
+        "scan_bytes": scan[0], "compaction_bytes": comp_bytes, "counts": counts,
+        "mean_live": drv.live_sum / (args.warmup + args.steps),
+        "roofline": dict(rl[dom], kernel=dom, peak_source=peak_src, traffic=None) if dom else None,
+        "kernels": kern, "gpu_launches": sum(k["launches"] for k in kern.values()), "clocks": clk}
+
+
+# ---------------------------------------------------------------------------
 # oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
@@ -458,6 +627,9 @@ def main():
     ap.add_argument("--ref-units", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="llama8b_single",
+                    choices=["llama8b_single", "batch64", "qwen3_8b", "stream256"])
+    ap.add_argument("--policy", default="growpage", choices=["growpage", "fixed"])
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = _dist()
@@ -469,6 +641,14 @@ def main():
     if world > 1:
         torch.distributed.init_process_group(
             backend="nccl" if torch.cuda.is_available() else "gloo")
+    if args.workload != "llama8b_single":
+        if world > 1 or rank != 0:
+            raise SystemExit("--workload other than the default runs on one GPU")
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        out = run_stream(args, dev) if args.workload == "stream256" else run_batch(args, dev)
+        print(json.dumps(out), flush=True)
+        return
     out = run_gpu(args, world, rank, local)
     if rank == 0:
         print(json.dumps(out), flush=True)

@@ -276,7 +276,7 @@ gp_status gp_debug_keep_mask(gp_ctx* ctx, int32_t req_idx, uint32_t* out);
 gp_status gp_read_summaries(gp_ctx* ctx, int32_t slot, double* out);
 
 /* Which kernel scans the cache in gp_boundary_demand.  AUTO (default): the
- * tensor-core (tcgen05) scan for bf16 caches and requests of at most 128
+ * tensor-core (tcgen05) scan for bf16 caches and requests of at most 160
  * pages, the CUDA-core (fp32 FMA) scan otherwise.  CUDA_CORE forces the
  * latter everywhere; TENSOR_CORE makes requests it cannot serve fail with
  * GP_ERR_UNSUPPORTED.  Both give the same results within the tolerances of

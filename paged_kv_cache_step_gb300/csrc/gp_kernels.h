@@ -82,8 +82,14 @@ struct DemandArgs {
   const int32_t* bt;       // packed block tables
   const int32_t* work;     // request indices handled by this launch
   int n_work;
-  int C;                   // cluster size (CTAs per unit)
-  int ppc;                 // pages per CTA
+  int C;                   // CUDA-core scan: cluster size (CTAs per unit)
+  int ppc;                 // CUDA-core scan: most pages one CTA scores
+  // tensor-core scan: units split into parts (tc_parts), parts numbered in
+  // work order; request work[i] owns parts [part_base[i], part_base[i+1])
+  const int32_t* part_base;// [n_work + 1]
+  int n_parts;
+  float2* xstat;           // per unit and part: softmax statistics [n][units][16][16]
+  unsigned* xcount;        // per unit: parts whose statistics are in, zero between calls
   float* scores;           // importance cache, log2 domain
   float* aval;             // a^S, a^L over C_t: per unit [2][(P-1) b]
   unsigned* tickets;       // [n][units] arrival counters, zero between calls
@@ -98,56 +104,46 @@ inline cudaError_t launch_demand(const DemandArgs& a, cudaStream_t s) {
   return a.variant == DEMAND_TC ? launch_demand_tc(a, s) : launch_demand_ffma(a, s);
 }
 
-// Clusters of C CTAs of the tensor-core demand kernel (head dim D, GQA
-// group G) that the current device runs at once; at least 1.
-int demand_tc_cluster_fit(int D, int G, int C);
+// CTAs of the tensor-core demand kernel (head dim D, GQA group G) that the
+// current device holds at once (one per SM); 0 if it cannot run.
+int demand_tc_resident(int D, int G);
 
-// How a request of P pages is split: kernel variant, CTAs per cluster (C)
-// and the most pages one CTA scores (ppc).  CTA c of a unit's cluster scores
-// the balanced range of logical pages [c P / C, (c + 1) P / C), so no rank
-// idles on a short remainder.
+// How a request of P pages is scanned.
 //
-// The tensor-core variant keeps two units of a CTA's logits in TMEM (2G
-// columns per 128 keys) beside its accumulator slots: at most TC_MAX_PPC
-// pages per CTA and 16 CTAs per cluster, so P <= 128 (it needs C >= P / 10).
-// Its C minimises a makespan model of the launch: a cluster takes units in
-// turn, so U units run ceil(U / fit(C)) rounds, each of ceil(P / C) pages
-// per CTA plus about one page's worth of per-unit epilogue.  fit(C) is how
-// many clusters of C CTAs the device holds at once (clusters stay inside a
-// GPC, so for some C a good part of the 152 SMs stays empty).  Ties go to
-// the smaller cluster (a cheaper statistics exchange).
+// Tensor-core variant (bf16 caches, P <= TC_MAX_PAGES): a persistent
+// cooperative grid of one CTA per SM.  Each unit (request, layer, KV head)
+// is split into tc_parts(P) parts of balanced page ranges, at most
+// TC_MAX_PPC pages each (a CTA keeps two parts of logits in TMEM beside its
+// accumulator slots); CTA b takes parts b, b + grid, ... of the call's part
+// list, which runs in unit order, so every CTA meets its units in
+// increasing order and a unit's parts sit on different CTAs.  Within a unit
+// the parts are listed from a rotating start, so the larger ranges of
+// uneven splits spread over the CTAs.
 //
-// The CUDA-core variant keeps its logits in shared memory: 8 pages per CTA
-// up to 128 pages, 16 beyond (P <= 256).
+// CUDA-core variant (fp32 caches, or longer requests): a cluster of C CTAs
+// per unit keeps its logits in shared memory, 8 pages per CTA up to 128
+// pages, 16 beyond (P <= 256).
 constexpr int TC_MAX_PPC = 10;
+constexpr int TC_MAX_PARTS = 16;
+constexpr int TC_MAX_PAGES = TC_MAX_PARTS * TC_MAX_PPC;
+__host__ __device__ inline int tc_parts(int P) { return P <= TC_MAX_PPC ? 1 : (P + TC_MAX_PPC - 1) / TC_MAX_PPC; }
+
 struct DemandPlan {
   int variant, ppc, C;
 };
-inline DemandPlan demand_plan(int P, bool tc_ok, int D, int G, long long units) {
+inline DemandPlan demand_plan(int P, bool tc_ok) {
   DemandPlan pl;
-  if (tc_ok && P <= 128) {
+  if (tc_ok && P <= TC_MAX_PAGES) {
     pl.variant = DEMAND_TC;
-    const int c_lo = P <= 1 ? 1 : (P + TC_MAX_PPC - 1) / TC_MAX_PPC;
-    const int c_hi = P < 16 ? (P < 1 ? 1 : P) : 16;
-    long long best = -1;
-    pl.C = c_lo;
-    for (int C = c_lo; C <= c_hi; ++C) {
-      const long long fit = demand_tc_cluster_fit(D, G, C);
-      if (fit < 1) continue;
-      const long long rounds = (units + fit - 1) / fit;
-      const long long cost = rounds * ((P + C - 1) / C + 1);
-      if (best < 0 || cost < best) {
-        best = cost;
-        pl.C = C;
-      }
-    }
+    pl.C = 1;
+    pl.ppc = (P + tc_parts(P) - 1) / tc_parts(P);
   } else {
     pl.variant = DEMAND_FFMA;
     const int ppc = P <= 128 ? 8 : 16;
     pl.C = (P + ppc - 1) / ppc;
     if (pl.C < 1) pl.C = 1;
+    pl.ppc = (P + pl.C - 1) / pl.C;
   }
-  pl.ppc = (P + pl.C - 1) / pl.C;
   if (pl.ppc < 1) pl.ppc = 1;
   return pl;
 }

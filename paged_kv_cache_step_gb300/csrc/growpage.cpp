@@ -74,7 +74,7 @@ struct gp_ctx {
   double* pool = nullptr;          // [L][M][2][Hq][D]
   int* err_dev = nullptr;          // kernel error bits
   unsigned long long* moved_dev = nullptr;
-  DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks;
+  DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks, xstat;
   double* inv_freq = nullptr;      // [D/2] theta^(-2i/D) for RoPE
   CUtensorMap kmap;                // K cache as a 2-D bf16 tensor (tensor-core scan)
   bool tc_ok = false;              // kmap is valid
@@ -343,7 +343,7 @@ gp_status gp_destroy(gp_ctx* c) {
   if (!c->host_only) {
     cudaStreamSynchronize(c->stream);
     for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->bq, &c->scores, &c->aval, &c->tickets, &c->kout, &c->ksum,
-                      &c->masks})
+                      &c->masks, &c->xstat})
       if (b->p) cudaFree(b->p);
     if (c->inv_freq) cudaFree(c->inv_freq);
     if (c->pool) cudaFree(c->pool);
@@ -459,11 +459,13 @@ struct Staged {
   int32_t* bt;
   int32_t* bt_new;
   int32_t* work;
+  int32_t* part_base;
   size_t bytes;
-  size_t off_bt, off_bt_new, off_work;
+  size_t off_bt, off_bt_new, off_work, off_pb;
 };
 
-// Pinned layout [DevReq n][bt n*maxP][bt_new n*maxP][work n], mirrored in `upload`.
+// Pinned layout [DevReq n][bt n*maxP][bt_new n*maxP][work n][part_base n+1],
+// mirrored in `upload`.
 gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s) {
   const int maxp = c->cfg.max_pages_per_req;
   size_t o = 0;
@@ -472,6 +474,7 @@ gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s) {
   s->off_bt = take(sizeof(int32_t) * (size_t)n * maxp);
   s->off_bt_new = with_new ? take(sizeof(int32_t) * (size_t)n * maxp) : s->off_bt;
   s->off_work = take(sizeof(int32_t) * n);
+  s->off_pb = take(sizeof(int32_t) * (n + 1));
   s->bytes = o;
   gp_status st = ensure_pinned(c, o);
   if (st != GP_OK) return st;
@@ -482,6 +485,7 @@ gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s) {
   s->bt = reinterpret_cast<int32_t*>(p + s->off_bt);
   s->bt_new = reinterpret_cast<int32_t*>(p + s->off_bt_new);
   s->work = reinterpret_cast<int32_t*>(p + s->off_work);
+  s->part_base = reinterpret_cast<int32_t*>(p + s->off_pb);
   return GP_OK;
 }
 
@@ -535,23 +539,31 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   if ((st = ensure(c, c->bq, gp::bq_bytes(g.head_dim, G) * (size_t)n * units)) != GP_OK) return st;
   if ((st = ensure(c, c->scores, sizeof(float) * (size_t)std::max<int64_t>(score_total, 1))) != GP_OK) return st;
   if ((st = ensure(c, c->aval, sizeof(float) * (size_t)std::max<int64_t>(aval_total, 1))) != GP_OK) return st;
-  if ((st = ensure(c, c->tickets, sizeof(unsigned) * (size_t)n * units)) != GP_OK) return st;
+  // tickets [n][units] then the tensor-core scan's statistics counts [n][units]
+  if ((st = ensure(c, c->tickets, sizeof(unsigned) * 2 * (size_t)n * units)) != GP_OK) return st;
+  if ((st = ensure(c, c->xstat, sizeof(float2) * (size_t)n * units * gp::TC_MAX_PARTS * 16)) != GP_OK) return st;
   if ((st = ensure(c, c->kout, sizeof(int32_t) * (size_t)n * units * 2)) != GP_OK) return st;
   if ((st = ensure(c, c->ksum, sizeof(unsigned long long) * (size_t)n * 2)) != GP_OK) return st;
 
-  // work buckets: (variant, cluster size C), one launch each; a launch's
-  // ppc bounds the pages any CTA of it scores
+  // work: the tensor-core requests first (one launch, split into parts),
+  // then the CUDA-core requests in buckets of equal cluster size C (one
+  // launch each; a bucket's ppc bounds the pages any CTA of it scores)
   const bool tc = c->tc_ok && c->scan_kernel != GP_SCAN_CUDA_CORE;
-  std::map<std::tuple<int, int>, std::vector<int32_t>> buckets;
-  std::map<std::tuple<int, int>, int> bucket_ppc;
+  std::vector<int32_t> tc_work;
+  std::map<int, std::vector<int32_t>> buckets;
+  std::map<int, int> bucket_ppc;
   for (int r = 0; r < n; ++r) {
-    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, tc, g.head_dim, G, units);
+    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, tc);
     if (c->scan_kernel == GP_SCAN_TENSOR_CORE && pl.variant != gp::DEMAND_TC)
-      return fail(c, GP_ERR_UNSUPPORTED, "request %d: the tensor-core scan needs a bf16 cache and at most 128 pages",
+      return fail(c, GP_ERR_UNSUPPORTED, "request %d: the tensor-core scan needs a bf16 cache and at most 160 pages",
                   r);
-    buckets[{pl.variant, pl.C}].push_back(r);
-    int& mp = bucket_ppc[{pl.variant, pl.C}];
-    mp = std::max(mp, pl.ppc);
+    if (pl.variant == gp::DEMAND_TC) {
+      tc_work.push_back(r);
+    } else {
+      buckets[pl.C].push_back(r);
+      int& mp = bucket_ppc[pl.C];
+      mp = std::max(mp, pl.ppc);
+    }
   }
   for (int r = 0; r < n; ++r) {
     gp::DevReq& d = s.reqs[r];
@@ -570,14 +582,23 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   };
   std::vector<Launch> launches;
   int wpos = 0;
+  int n_parts = 0;
+  s.part_base[0] = 0;
+  if (!tc_work.empty()) {
+    launches.push_back({gp::DEMAND_TC, 1, gp::TC_MAX_PPC, 0, (int)tc_work.size()});
+    for (int32_t r : tc_work) {
+      s.work[wpos++] = r;
+      n_parts += units * gp::tc_parts(reqs[r].num_pages);
+      s.part_base[wpos] = n_parts;
+    }
+  }
   for (auto it = buckets.rbegin(); it != buckets.rend(); ++it) {  // largest clusters first
-    launches.push_back({std::get<0>(it->first), std::get<1>(it->first), bucket_ppc[it->first], wpos,
-                        (int)it->second.size()});
+    launches.push_back({gp::DEMAND_FFMA, it->first, bucket_ppc[it->first], wpos, (int)it->second.size()});
     for (int32_t r : it->second) s.work[wpos++] = r;
   }
   if ((st = upload(c, s)) != GP_OK) return st;
   GP_CUDA(c, cudaMemsetAsync(c->ksum.p, 0, sizeof(unsigned long long) * (size_t)n * 2, c->stream));
-  GP_CUDA(c, cudaMemsetAsync(c->tickets.p, 0, sizeof(unsigned) * (size_t)n * units, c->stream));
+  GP_CUDA(c, cudaMemsetAsync(c->tickets.p, 0, sizeof(unsigned) * 2 * (size_t)n * units, c->stream));
 
   gp::PrepArgs pa{};
   pa.pool = c->pool;
@@ -619,6 +640,10 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     da.n_work = l.count;
     da.C = l.C;
     da.ppc = l.ppc;
+    da.part_base = dev_at<int32_t>(c, s.off_pb);
+    da.n_parts = n_parts;
+    da.xstat = static_cast<float2*>(c->xstat.p);
+    da.xcount = static_cast<unsigned*>(c->tickets.p) + (size_t)n * units;
     da.scores = static_cast<float*>(c->scores.p);
     da.aval = static_cast<float*>(c->aval.p);
     da.tickets = static_cast<unsigned*>(c->tickets.p);

@@ -1,6 +1,6 @@
 // Boundary demand kernel, tensor-core variant (tcgen05, sm_103a): GrowPage
 // Sec. 3.2 Eqs. 2, 7 and App. E.1, plus the Eq. 9 importance cached for
-// Compress & Hold, for bf16 caches and requests of at most 128 pages.
+// Compress & Hold, for bf16 caches and requests of at most 160 pages.
 //
 // Why the tensor core on an HBM-bound scan: each key meets 2G = 8 summary
 // rows, 2 * 8 * d flops per 2 d bytes of K.  On CUDA cores that is 8 FMAs
@@ -15,35 +15,40 @@
 // in fp32, summed afterwards.  The prep kernel writes these parts already in
 // the 128-byte-swizzled K-major layout the MMA reads (one bulk copy).
 //
-// Persistent and warp-specialised.  A cluster of C CTAs (one CTA per SM)
-// takes units (request, layer, KV head) g, g + #clusters, ...; in each, CTA
-// rank c scores the balanced page range [c P / C, (c+1) P / C).  Roles:
-//   warp 0      producer: per unit, the B operand (bulk copy) and the K tiles
-//               (128 keys x d, box 64 x 128 with the 128-byte swizzle)
-//               through an NSTAGE mbarrier ring, running ahead across units;
+// Persistent and warp-specialised: a cooperative grid of one CTA per SM.
+// Each unit (request, layer, KV head) is split into parts of at most 10
+// pages (tc_parts); CTA b takes parts b, b + grid, ... of the call's part
+// list, which runs in unit order.  Roles:
+//   warp 0      producer: per part, the unit's B operand (bulk copy) and the
+//               part's K tiles (128 keys x d, box 64 x 128 with the 128-byte
+//               swizzle) through an NSTAGE mbarrier ring, running ahead
+//               across parts;
 //   warp 1      MMA issuer: tcgen05.mma into a ring of TMEM accumulator
 //               slots (a tile's accumulator is 128 lanes x N columns); a slot
 //               is reused once the epilogue has read it, so the scan runs on
-//               while the epilogue finishes the previous unit;
+//               while the epilogue finishes the previous part;
 //   warps 2..9  epilogue (warp w reads TMEM lane quadrant w % 4; two warps
 //               per quadrant split the tiles): as tiles finish, it sums the
 //               three partial products into each key's 2G logits, stores
-//               them in a compact per-unit TMEM region (2G columns per 128
-//               keys, two units deep), releases the accumulator slot and
+//               them in a compact per-part TMEM region (2G columns per 128
+//               keys, two parts deep), releases the accumulator slot and
 //               folds online softmax statistics; then a reduce-scatter
-//               butterfly over the warp, an
-//               exchange with every rank (st.async into the peers' shared
-//               memory, completing on their mbarriers), the merge, then a^S,
-//               a^L and the importance of every key to global memory, and
-//               a ticket per unit in global memory;
-//   warps 10..15 selector: rank (k + x) mod C computes D_p of summary x of
-//               the cluster's k-th unit once all C tickets are in -- the
-//               exact select of demand_common.cuh, on the SM's otherwise idle
-//               issue slots; each cluster's last unit is left to the whole
-//               CTA once its scan is over (nothing is left to hide it behind).
-// Every wait is bounded; on expiry the CTA records ERR_TIMEOUT, raises a
-// shared abort flag that ends every role's loop, drains its copies in
-// flight and finishes with garbage rather than hanging.
+//               butterfly over the warp, the part's statistics to global
+//               memory and a count per unit.  It runs one part ahead: once
+//               every part of the previous part's unit has counted in, the
+//               merge, then that part's a^S, a^L and the importance of every
+//               key to global memory, and a ticket per unit;
+//   warps 10..15 selector: the CTA of part (2 unit + x) mod parts computes D_p
+//               of summary x of the unit once all its parts' tickets are in
+//               -- the exact select of demand_common.cuh, on the SM's
+//               otherwise idle issue slots; a CTA's last part's selects are
+//               left to the whole CTA once its scan is over.
+// Progress: every CTA is resident (cooperative launch) and meets its units
+// in increasing order, so the lowest unfinished unit always has all its
+// parts' statistics on the way.  Every wait is bounded; on expiry the CTA
+// records ERR_TIMEOUT, raises a shared abort flag that ends every role's
+// loop, drains its copies in flight and finishes with garbage rather than
+// hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -125,15 +130,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-// 8 bytes into rank `rank`'s shared memory at the address that `local` has
-// here, completing on that rank's mbarrier at the address `local_bar` has here.
-__device__ __forceinline__ void st_async_b64(uint32_t local, uint32_t local_bar, int rank, uint64_t v) {
-  uint32_t ra, rb;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local), "r"(rank));
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(ra), "l"(v), "r"(rb)
                : "memory");
 }
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
@@ -242,24 +238,37 @@ __device__ __forceinline__ void tile_logits(uint32_t tmem, int quad, int col, fl
   for (int r = 0; r < ROWS; ++r) z[r] = v[r] + (v[ROWS + r] + v[2 * ROWS + r]);
 }
 
-// Per-unit facts every role derives from the unit index w.
+// Per-part facts every role derives from the part index p.
 struct UnitInfo {
   int r, unit, layer, h, P, ndem, ncmp, npg, j0;
+  int part, nparts;  // this part of the unit, and how many it has
+  int w;             // unit index within the launch (work slot * units + unit)
+  size_t g;          // unit index within the call: r * units + unit
   DevReq rq;
 };
-__device__ __forceinline__ UnitInfo unit_info(const DemandArgs& a, int w, int crank) {
+__device__ __forceinline__ UnitInfo unit_info(const DemandArgs& a, int p) {
   UnitInfo u;
   const int units = a.L * a.Hkv;
-  u.r = a.work[w / units];
-  u.unit = w % units;
-  u.layer = u.unit / a.Hkv;
-  u.h = u.unit % a.Hkv;
+  int lo = 0, hi = a.n_work;  // the work slot i with part_base[i] <= p < part_base[i + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a.part_base[mid] <= p) lo = mid; else hi = mid;
+  }
+  u.r = a.work[lo];
   u.rq = a.reqs[u.r];
   u.P = u.rq.num_pages;
+  u.nparts = tc_parts(u.P);
+  const int local = p - a.part_base[lo];
+  u.unit = local / u.nparts;
+  u.w = lo * units + u.unit;
+  u.part = (u.w + local % u.nparts) % u.nparts;
+  u.layer = u.unit / a.Hkv;
+  u.h = u.unit % a.Hkv;
+  u.g = (size_t)u.r * units + u.unit;
   u.ndem = (u.P - 1) * PAGE;
   u.ncmp = u.P * PAGE - a.R;
-  u.j0 = (crank * u.P) / a.C;
-  u.npg = ((crank + 1) * u.P) / a.C - u.j0;
+  u.j0 = (u.part * u.P) / u.nparts;
+  u.npg = ((u.part + 1) * u.P) / u.nparts - u.j0;
   return u;
 }
 
@@ -276,8 +285,8 @@ struct TcSmem {
   static constexpr size_t BQ = STAGE + (size_t)T::NSTAGE * T::TILE_BYTES;  // 2 buffers
   static constexpr size_t XG = BQ + 2 * (size_t)T::BQ_BYTES;               // XStat [2][16][16]
   static constexpr size_t BARS = XG + sizeof(XStat) * 2 * 16 * 16;
-  // full[NSTAGE], empty[NSTAGE], bqfull[2], bqempty[2], xbar[2], mmadone, sel, ready[W], wfree[W]
-  static constexpr int NBARS = 2 * T::NSTAGE + 8 + 2 * T::WSLOTS;
+  // full[NSTAGE], empty[NSTAGE], bqfull[2], bqempty[2], mmadone, sel, ready[W], wfree[W]
+  static constexpr int NBARS = 2 * T::NSTAGE + 6 + 2 * T::WSLOTS;
   static constexpr size_t PART = BARS + 8 * (size_t)NBARS;                 // [EPI_NW][16] XStat
   static constexpr size_t LSE = PART + sizeof(XStat) * EPI_NW * 16;        // lse_dem[8], lse_cmp[8]
   static constexpr size_t MISC = LSE + sizeof(float) * 16;                 // ints, see kernel
@@ -288,8 +297,7 @@ struct TcSmem {
 };
 
 template <int D, int ROWS>
-__global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ DemandArgs a, int total_units,
-                                                       int smem_bytes) {
+__global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ DemandArgs a, int smem_bytes) {
   using T = TcCfg<D, ROWS>;
   using S = TcSmem<D, ROWS>;
   constexpr int NSTAT = 2 * ROWS;
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  XStat* xg = reinterpret_cast<XStat*>(smem + S::XG);         // [parity][rank][stat]
+  XStat* xg = reinterpret_cast<XStat*>(smem + S::XG);         // [part][stat] of the unit being merged
   XStat* part = reinterpret_cast<XStat*>(smem + S::PART);
   float* lse_dem = reinterpret_cast<float*>(smem + S::LSE);
   float* lse_cmp = lse_dem + 8;
@@ -308,7 +316,8 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
   volatile int* q_tail = misc + 3;
   volatile int* q_done = misc + 4;
   volatile int* sel_item = misc + 5;
-  int* flag = misc + 6;
+  volatile int* flag = misc + 6;   // exchange outcome of the current part (epilogue)
+  volatile int* epi_fail = misc + 8;  // an epilogue warp's tile wait gave up (sticky)
   int* phys = misc + 16;                                      // [16]
   volatile int* queue = misc + 32;                            // [QLEN]
   DpSmem* dps = reinterpret_cast<DpSmem*>(smem + S::DPS);
@@ -320,18 +329,14 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
   const uint32_t bar_empty = bar_full + 8 * T::NSTAGE;
   const uint32_t bar_bqfull = bar_empty + 8 * T::NSTAGE;
   const uint32_t bar_bqempty = bar_bqfull + 16;
-  const uint32_t bar_xg = bar_bqempty + 16;
-  const uint32_t bar_mmadone = bar_xg + 16;
+  const uint32_t bar_mmadone = bar_bqempty + 16;
   const uint32_t bar_sel = bar_mmadone + 8;
   const uint32_t bar_ready = bar_sel + 8;
   const uint32_t bar_wfree = bar_ready + 8 * T::WSLOTS;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int C = a.C;
-  const int crank = (int)(blockIdx.x % (unsigned)C);
-  const int g0 = (int)(blockIdx.x / (unsigned)C);
-  const int nclus = (int)(gridDim.x / (unsigned)C);
-  const int units = a.L * a.Hkv;
+  const int cta = (int)blockIdx.x, ncta = (int)gridDim.x;  // CTA cta takes parts cta, cta + ncta, ...
+  const int total_parts = a.n_parts;
 
   if (tid == 0) {
     for (int s = 0; s < T::NSTAGE; ++s) {
@@ -341,7 +346,6 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_bqfull + 8 * b, 1);
       mbar_init(bar_bqempty + 8 * b, 1);
-      mbar_init(bar_xg + 8 * b, 1);
     }
     mbar_init(bar_mmadone, 1);
     mbar_init(bar_sel, 1);
@@ -354,6 +358,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     *q_head = 0;
     *q_tail = 0;
     *q_done = 0;
+    *epi_fail = 0;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
@@ -362,12 +367,13 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  cluster_sync_all();  // barriers of every rank initialised before any remote signal
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  // The next queued unit whose D_p this rank computes, once every rank of the
-  // cluster has written its a-values; -1 when the queue is empty and the
+  // The next queued select (2 p + x: summary x of part p's unit) this CTA
+  // computes, once every part of the unit has written its a-values; -1 when
+  // the queue is empty and the
   // epilogue has finished (or stop_at_done and the epilogue has finished),
   // or on abort.  Called by one thread.
   auto take_item = [&](bool stop_at_done) -> int {
@@ -394,10 +400,10 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
       __nanosleep(200);
     }
     if (item >= 0) {
-      const UnitInfo u = unit_info(a, item >> 1, 0);
-      const unsigned* tk = a.tickets + (size_t)u.r * units + u.unit;
+      const UnitInfo u = unit_info(a, item >> 1);
+      const unsigned* tk = a.tickets + u.g;
       const long long t1 = clock64();
-      while (ld_acquire(tk) < (unsigned)C) {
+      while (ld_acquire(tk) < (unsigned)u.nparts) {
         if (*abort || clock64() - t1 > kWaitLimit) {
           atomicOr(a.err, ERR_TIMEOUT);
           *abort = 1;
@@ -417,14 +423,14 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
       for (int s = 0; s < T::NSTAGE; ++s) last_gt[s] = -1;
       bool ok = true;
       for (int kk = 0; ok; ++kk) {
-        const int w = g0 + kk * nclus;
-        if (w >= total_units) break;
-        const UnitInfo u = unit_info(a, w, crank);
+        const int pi = cta + kk * ncta;
+        if (pi >= total_parts) break;
+        const UnitInfo u = unit_info(a, pi);
         const int b2 = kk & 1;
         if (kk >= 2 && !(ok = mbar_wait(bar_bqempty + 8 * b2, ((kk >> 1) - 1) & 1, abort))) break;
         mbar_expect_tx(bar_bqfull + 8 * b2, T::BQ_BYTES);
         bulk_load(sbase + (uint32_t)(S::BQ + (size_t)b2 * T::BQ_BYTES),
-                  a.bq + ((size_t)u.r * units + u.unit) * T::BQ_BYTES, T::BQ_BYTES, bar_bqfull + 8 * b2);
+                  a.bq + u.g * T::BQ_BYTES, T::BQ_BYTES, bar_bqfull + 8 * b2);
         last_bq[b2] = kk;
         for (int j = 0; j < u.npg; ++j) {
           int pg = a.bt[u.rq.bt_off + u.j0 + j];
@@ -465,9 +471,9 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
       int gt = 0;
       bool ok = true;
       for (int kk = 0; ok; ++kk) {
-        const int w = g0 + kk * nclus;
-        if (w >= total_units) break;
-        const UnitInfo u = unit_info(a, w, crank);
+        const int pi = cta + kk * ncta;
+        if (pi >= total_parts) break;
+        const UnitInfo u = unit_info(a, pi);
         const int b2 = kk & 1;
         if (!(ok = mbar_wait(bar_bqfull + 8 * b2, (kk >> 1) & 1, abort))) break;
         const uint32_t b0 = sbase + (uint32_t)(S::BQ + (size_t)b2 * T::BQ_BYTES);
@@ -501,20 +507,23 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     __syncwarp();
   } else if (warp >= EPI_W0 && warp < SEL_W0) {
     // ---- epilogue ------------------------------------------------------------
+    // Skewed by one part: part k+1's tiles are folded and its statistics
+    // published before part k's merge waits on the other CTAs, so the
+    // accumulator slots keep draining while the exchange completes.  Every
+    // early exit is decided from shared flags written before a barrier, so
+    // all epilogue threads leave together.
     const int quad = warp & 3;                  // TMEM lane quadrant of this warp
     const int half = (warp - EPI_W0) >> 2;      // tiles t with t % 2 == half
     const int ew = warp - EPI_W0;               // 0..7
     const int et = tid - 32 * EPI_W0;           // 0..255
-    int gt0 = 0;  // global index of the unit's first tile, in the MMA issuer's order
-    for (int kk = 0;; ++kk) {
-      const int w = g0 + kk * nclus;
-      if (w >= total_units || *abort) break;
-      const UnitInfo u = unit_info(a, w, crank);
-      const int p = kk & 1;
+    const uint32_t lanes = (uint32_t)(32 * quad) << 16;
+    int gt0 = 0;  // global index of the part's first tile, in the MMA issuer's order
+
+    // Fold part kk's tiles (compact logits into TMEM region kk & 1, online
+    // statistics), then publish its statistics and count it in.
+    auto fold_publish = [&](int kk, const UnitInfo& u) -> bool {
       const int ntiles = 2 * u.npg;
-      const uint32_t lanes = (uint32_t)(32 * quad) << 16;
-      const uint32_t cbase = tmem + lanes + (uint32_t)(T::CBASE + p * T::TPU * ROWS);  // compact logits
-      // online softmax statistics (stat = set * ROWS + row) of this warp's tiles
+      const uint32_t cbase = tmem + lanes + (uint32_t)(T::CBASE + (kk & 1) * T::TPU * ROWS);
       float m[NSTAT], sm[NSTAT];
 #pragma unroll
       for (int e = 0; e < NSTAT; ++e) {
@@ -544,10 +553,10 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
         }
       }
       gt0 += ntiles;
-      if (!ok) {
-        if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+      if (!ok && lane == 0) {
+        atomicOr(a.err, ERR_TIMEOUT);
         *abort = 1;
-        break;
+        *epi_fail = 1;
       }
       {
         float om, os;
@@ -556,35 +565,65 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
         if ((lane & (32 / NSTAT - 1)) == 0) part[ew * 16 + idx] = XStat{om, os};
       }
       epi_sync();
-      // exchange with every rank: 8 bytes per statistic per rank
+      if (*epi_fail) return false;  // written only before the barrier: every epilogue thread agrees
+      // the part's statistics to global memory (8 bytes each), then its count
       if (et < NSTAT) {
         float cm = NEG, cs = 0.f;
 #pragma unroll
         for (int q = 0; q < EPI_NW; ++q) combine(cm, cs, part[q * 16 + et].m, part[q * 16 + et].s);
-        const uint64_t v = ((uint64_t)__float_as_uint(cs) << 32) | __float_as_uint(cm);
-        const uint32_t dst = smem_u32(xg + (p * 16 + crank) * 16 + et);
-        for (int c = 0; c < C; ++c) st_async_b64(dst, bar_xg + 8 * p, c, v);
+        __stcg(a.xstat + u.g * (size_t)(TC_MAX_PARTS * 16) + u.part * 16 + et, make_float2(cm, cs));
       }
-      if (et == 0) mbar_expect_tx(bar_xg + 8 * p, (uint32_t)(C * NSTAT * 8));
-      if (!(ok = mbar_wait(bar_xg + 8 * p, (kk >> 1) & 1, abort))) {
-        if (et == 0) atomicOr(a.err, ERR_TIMEOUT);
-        *abort = 1;
-        break;
+      epi_sync();
+      if (et == 0) {
+        __threadfence();
+        atomicAdd(a.xcount + u.g, 1u);
       }
+      return true;
+    };
+
+    // Once every part of its unit has counted in: merge the statistics, write
+    // part kk's a^S, a^L and importance from TMEM region kk & 1, take a
+    // ticket and queue the selects this CTA owns.
+    auto finish = [&](int kk, int pi, const UnitInfo& u) -> bool {
+      if (et == 0) {
+        bool in = true;
+        const long long t0 = clock64();
+        while (ld_acquire(a.xcount + u.g) < (unsigned)u.nparts) {
+          if (*abort || clock64() - t0 > kWaitLimit) {
+            in = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (!in) {
+          atomicOr(a.err, ERR_TIMEOUT);
+          *abort = 1;
+        }
+        *flag = in ? 1 : 0;
+      }
+      epi_sync();
+      if (*flag == 0) return false;
+      // the unit's statistics through L2 (other CTAs wrote them), then the
       // merge into base-2 log-sum-exps over C_t and over C_cmp
+      const float2* xs_g = a.xstat + u.g * (size_t)(TC_MAX_PARTS * 16);
+      for (int i = et; i < u.nparts * NSTAT; i += EPI_NTH) {
+        const float2 v = __ldcg(xs_g + (i / NSTAT) * 16 + i % NSTAT);
+        xg[(i / NSTAT) * 16 + i % NSTAT] = XStat{v.x, v.y};
+      }
+      epi_sync();
       if (et < ROWS) {
-        const XStat* xs = xg + p * 16 * 16;
         float md, sd, mt, stl;
-        merge_ranks(&xs[et].m, &xs[et].s, C, 32, &md, &sd);
-        merge_ranks(&xs[ROWS + et].m, &xs[ROWS + et].s, C, 32, &mt, &stl);
+        merge_ranks(&xg[et].m, &xg[et].s, u.nparts, 32, &md, &sd);
+        merge_ranks(&xg[ROWS + et].m, &xg[ROWS + et].s, u.nparts, 32, &mt, &stl);
         lse_pair(md, sd, mt, stl, lse_dem + et, lse_cmp + et);
       }
       epi_sync();
       // a^S, a^L and the importance of every key of this warp's tiles
       {
+        const uint32_t cbase = tmem + lanes + (uint32_t)(T::CBASE + (kk & 1) * T::TPU * ROWS);
         float* sc = a.scores + u.rq.score_off + (size_t)u.unit * u.ncmp;
         float* av = a.aval + u.rq.aval_off + (size_t)u.unit * 2 * u.ndem;
-        for (int t = half; t < ntiles; t += 2) {
+        for (int t = half; t < 2 * u.npg; t += 2) {
           float z[ROWS];
           tmem_ld_rows<ROWS>(cbase + (uint32_t)(t * ROWS), z);
           key_values<ROWS>(z, u.j0 * PAGE + t * 128 + 32 * quad + lane, u.ndem, u.ncmp, lse_dem, lse_cmp, av, sc);
@@ -595,11 +634,12 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
       if (et == 0) {
         // the CTA's a-values (ordered by the barrier above) before its ticket
         __threadfence();
-        atomicAdd(a.tickets + (size_t)u.r * units + u.unit, 1u);
-        // D_p of summary x is computed by rank (kk + x) mod C: queue it for
-        // this rank's selector warps
+        atomicAdd(a.tickets + u.g, 1u);
+        // D_p of summary x is computed by the CTA of part (2 unit + x) mod
+        // parts, which spreads the selects over the CTAs: queue it for this
+        // CTA's selector warps
         for (int x = 0; x < 2; ++x) {
-          if ((kk + x) % C != crank) continue;
+          if ((2 * u.w + x) % u.nparts != u.part) continue;
           const long long t0 = clock64();
           while (*q_head - *q_tail >= QLEN) {
             if (*abort || clock64() - t0 > kWaitLimit) {
@@ -609,16 +649,36 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
             }
           }
           if (*abort) break;
-          // the cluster's last unit: no scan is left to hide its select behind,
+          // this CTA's last part: no scan is left to hide its select behind,
           // so the selector warps stop here and the whole CTA drains it
-          if (w + nclus >= total_units) {
+          if (pi + ncta >= total_parts) {
             *q_done = 1;
             __threadfence_block();
           }
-          queue[*q_head % QLEN] = 2 * w + x;
+          queue[*q_head % QLEN] = 2 * pi + x;
           __threadfence_block();
           *q_head = *q_head + 1;
         }
+      }
+      return true;
+    };
+
+    if (cta < total_parts) {
+      int pi = cta;
+      UnitInfo cur = unit_info(a, pi);
+      bool live = fold_publish(0, cur);
+      for (int kk = 0; live; ++kk) {
+        const int pn = pi + ncta;
+        UnitInfo nxt;
+        const bool more = pn < total_parts;
+        if (more) {
+          nxt = unit_info(a, pn);
+          if (!fold_publish(kk + 1, nxt)) break;
+        }
+        if (!finish(kk, pi, cur)) break;
+        if (!more) break;
+        cur = nxt;
+        pi = pn;
       }
     }
     if (et == 0) {
@@ -637,7 +697,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
       const int item = *sel_item;
       if (item < 0) break;
       const int x = item & 1;
-      const UnitInfo u = unit_info(a, item >> 1, 0);
+      const UnitInfo u = unit_info(a, item >> 1);
       unsigned k = 0;
       if (u.ndem > 0) {
         const float* av = a.aval + u.rq.aval_off + ((size_t)u.unit * 2 + x) * u.ndem;
@@ -650,7 +710,6 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
     }
     if (st == 0) misc[7] = (int)sel_par;
   }
-  (void)flag;
   (void)phys;
 
   // ---- drain: selects still queued when the scan ended, with the whole CTA --
@@ -664,7 +723,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
       const int item = *sel_item;
       if (item < 0) break;
       const int x = item & 1;
-      const UnitInfo u = unit_info(a, item >> 1, 0);
+      const UnitInfo u = unit_info(a, item >> 1);
       unsigned k = 0;
       if (u.ndem > 0) {
         const float* av = a.aval + u.rq.aval_off + ((size_t)u.unit * 2 + x) * u.ndem;
@@ -678,36 +737,14 @@ __global__ void __launch_bounds__(NTHR, 1) k_demand_tc(const __grid_constant__ D
   }
 
   // ---- teardown ----------------------------------------------------------------
-  cluster_sync_all();  // no rank leaves while a peer may still write into it
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
   }
 }
 
-// Clusters of this shape that fit on the GPU at once; 0 if none does.
-template <typename K>
-int max_clusters(K kern, int C, size_t smem) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)C * 152, 1, 1);
-  cfg.blockDim = dim3(NTHR, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
-    cudaGetLastError();
-    n = 0;
-  }
-  return n;
-}
-
-// The kernel's launch attributes (set once) and its dynamic shared memory:
+// The kernel's launch attribute (set once) and its dynamic shared memory:
 // the whole opt-in amount, so that one CTA owns an SM, its TMEM (512
 // columns) and the select buffer.  0 if the device cannot hold the layout.
 template <int D, int ROWS>
@@ -722,9 +759,8 @@ size_t prepare_t() {
     cudaGetLastError();
     return 0;
   }
-  auto kern = k_demand_tc<D, ROWS>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin) != cudaSuccess ||
-      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+  if (cudaFuncSetAttribute(k_demand_tc<D, ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -732,58 +768,57 @@ size_t prepare_t() {
   return smem;
 }
 
+// CTAs the device holds at once (one per SM at this shared-memory size).
 template <int D, int ROWS>
-int fit_t(int C) {
-  static int fit_cache[17] = {};  // per kernel instantiation and cluster size
-  if (C < 1 || C > 16) return 0;
-  if (!fit_cache[C]) {
-    const size_t smem = prepare_t<D, ROWS>();
-    if (!smem) return 0;
-    fit_cache[C] = max_clusters(k_demand_tc<D, ROWS>, C, smem);
+int resident_t() {
+  static int n = -1;
+  if (n >= 0) return n;
+  const size_t smem = prepare_t<D, ROWS>();
+  int dev = 0, sms = 0, per_sm = 0;
+  if (!smem || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_demand_tc<D, ROWS>, NTHR, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
   }
-  return fit_cache[C];
+  n = sms * per_sm;
+  return n;
 }
 
 template <int D, int ROWS>
 cudaError_t launch_t(const DemandArgs& a, cudaStream_t s) {
-  using T = TcCfg<D, ROWS>;
-  if (2 * a.ppc > T::TPU) return cudaErrorInvalidValue;  // a unit's compact logits must fit TMEM
-  if (a.ppc * a.C < 1) return cudaErrorInvalidValue;
+  if (a.n_parts < 1 || !a.part_base || !a.xstat || !a.xcount) return cudaErrorInvalidValue;
   const size_t smem = prepare_t<D, ROWS>();
-  if (!smem) return cudaErrorInvalidValue;
-  auto kern = k_demand_tc<D, ROWS>;
-  const int total = a.n_work * a.L * a.Hkv;
-  int nclus = fit_t<D, ROWS>(a.C);
-  if (nclus < 1) return cudaErrorInvalidValue;
-  if (nclus > total) nclus = total;
+  int grid = resident_t<D, ROWS>();
+  if (!smem || grid < 1) return cudaErrorInvalidValue;
+  if (grid > a.n_parts) grid = a.n_parts;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.C * nclus), 1, 1);
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(NTHR, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
+  // the parts of a unit wait on one another: every CTA must be resident
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, total, (int)smem);
+  return cudaLaunchKernelEx(&cfg, k_demand_tc<D, ROWS>, a, (int)smem);
 }
 
 }  // namespace
 
-int demand_tc_cluster_fit(int D, int G, int C) {
-  if (D == 128 && G == 4) return fit_t<128, 8>(C);
-  if (D == 128 && G == 2) return fit_t<128, 4>(C);
-  if (D == 64 && G == 4) return fit_t<64, 8>(C);
-  if (D == 64 && G == 2) return fit_t<64, 4>(C);
+int demand_tc_resident(int D, int G) {
+  if (D == 128 && G == 4) return resident_t<128, 8>();
+  if (D == 128 && G == 2) return resident_t<128, 4>();
+  if (D == 64 && G == 4) return resident_t<64, 8>();
+  if (D == 64 && G == 2) return resident_t<64, 4>();
   return 0;
 }
 
 cudaError_t launch_demand_tc(const DemandArgs& a, cudaStream_t s) {
   if (a.n_work == 0) return cudaSuccess;
-  if (a.b != PAGE || a.kv_f32 || a.C < 1 || a.C > 16 || a.ppc < 1 || !a.bq) return cudaErrorInvalidValue;
+  if (a.b != PAGE || a.kv_f32 || !a.bq) return cudaErrorInvalidValue;
   if (a.D == 128 && a.G == 4) return launch_t<128, 8>(a, s);
   if (a.D == 128 && a.G == 2) return launch_t<128, 4>(a, s);
   if (a.D == 64 && a.G == 4) return launch_t<64, 8>(a, s);

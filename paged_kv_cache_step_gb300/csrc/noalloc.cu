@@ -8,7 +8,8 @@
 // only the file-scope device array below for every temporary it needs: the
 // request descriptors and block tables, the calibrated summaries and their
 // tensor-core operands, the importance values, the a-values and arrival
-// tickets of the D_p select, the per-(layer, KV head) D_p and their sums.
+// tickets of the D_p select, the partial softmax statistics of the
+// tensor-core scan, the per-(layer, KV head) D_p and their sums.
 // It calls no cudaMalloc, cudaFree, cudaHostAlloc or other allocating routine;
 // host-side staging lives in fixed file-scope arrays.  Inputs (the caches,
 // the summaries in the engine's pool, the current queries) and outputs (the
@@ -19,7 +20,8 @@
 // library holds it until the process exits.  Every call shares it (and the
 // host staging arrays): calls whose work overlaps on the GPU, or that run on
 // several host threads at once, race.  It keeps the last call's contents;
-// the D_p sums and tickets that must start at zero are cleared by each call.
+// the D_p sums, tickets and counts that must start at zero are cleared by
+// each call.
 //
 // Set-up: on the first call on a device (with that device current) the
 // array's device address is looked up once with cudaGetSymbolAddress and
@@ -48,6 +50,7 @@ constexpr int kPage = 256;
 unsigned char* g_scratch_addr[GP_NOALLOC_MAX_DEVICES] = {};
 gp::DevReq g_reqs[GP_NOALLOC_MAX_REQ];
 int32_t g_work[GP_NOALLOC_MAX_REQ];
+int32_t g_part_base[GP_NOALLOC_MAX_REQ + 1];
 unsigned long long g_sums[2 * GP_NOALLOC_MAX_REQ];
 uint32_t g_seen[GP_NOALLOC_MAX_PAGES_BITS / 32];
 
@@ -116,11 +119,13 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   const size_t off_req = o;   o = align256(o + sizeof(gp::DevReq) * n);
   const size_t off_bt = o;    o = align256(o + sizeof(int32_t) * (size_t)n * maxp);
   const size_t off_work = o;  o = align256(o + sizeof(int32_t) * n);
+  const size_t off_pb = o;    o = align256(o + sizeof(int32_t) * (n + 1));
+  const size_t off_xs = o;    o = align256(o + sizeof(float2) * (size_t)n * units * gp::TC_MAX_PARTS * 16);
   const size_t off_qt = o;    o = align256(o + sizeof(float) * (size_t)n * units * 2 * G * g.head_dim);
   const size_t off_bq = o;    o = align256(o + gp::bq_bytes(g.head_dim, G) * (size_t)n * units);
   const size_t off_kout = o;  o = align256(o + sizeof(int32_t) * (size_t)n * units * 2);
   const size_t off_ksum = o;  o = align256(o + sizeof(unsigned long long) * (size_t)n * 2);
-  const size_t off_tk = o;    o = align256(o + sizeof(unsigned) * (size_t)n * units);
+  const size_t off_tk = o;    o = align256(o + sizeof(unsigned) * 2 * (size_t)n * units);  // tickets, counts
   // one float region: per request its importance values, then its a-values
   const size_t off_sc = o;
   for (int r = 0; r < n; ++r) {
@@ -154,30 +159,43 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   }
   unsigned char* base = g_scratch_addr[dev];
 
-  // ---- work buckets (scan variant, cluster size C), as gp_boundary_demand --
-  // forms them; a bucket's ppc bounds the pages any CTA of its launch scores.
-  int bucket_count[2][17] = {};
-  int bucket_ppc[2][17] = {};
+  // ---- work, as gp_boundary_demand forms it: the tensor-core requests first
+  // (one launch, split into parts), then the CUDA-core requests in buckets of
+  // equal cluster size C; a bucket's ppc bounds the pages any CTA scores.
+  int bucket_count[17] = {};
+  int bucket_ppc[17] = {};
+  int n_tc = 0;
   for (int r = 0; r < n; ++r) {
-    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok, g.head_dim, G, units);
+    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok);
     if (v.scan_kernel == GP_SCAN_TENSOR_CORE && pl.variant != gp::DEMAND_TC)
       return fail(c, GP_ERR_UNSUPPORTED, "request %lld: the tensor-core scan cannot serve it", r);
-    if (pl.C < 1 || pl.C > 16) return fail(c, GP_ERR_UNSUPPORTED, "request %lld: cluster size %lld", r, pl.C);
-    bucket_count[pl.variant][pl.C] += 1;
-    if (pl.ppc > bucket_ppc[pl.variant][pl.C]) bucket_ppc[pl.variant][pl.C] = pl.ppc;
-  }
-  int bucket_start[2][17];
-  int pos = 0;
-  for (int k = 1; k >= 0; --k)
-    for (int C = 16; C >= 1; --C) {
-      bucket_start[k][C] = pos;
-      pos += bucket_count[k][C];
+    if (pl.variant == gp::DEMAND_TC) {
+      ++n_tc;
+      continue;
     }
-  int fill[2][17];
+    if (pl.C < 1 || pl.C > 16) return fail(c, GP_ERR_UNSUPPORTED, "request %lld: cluster size %lld", r, pl.C);
+    bucket_count[pl.C] += 1;
+    if (pl.ppc > bucket_ppc[pl.C]) bucket_ppc[pl.C] = pl.ppc;
+  }
+  int bucket_start[17];
+  int pos = n_tc;
+  for (int C = 16; C >= 1; --C) {
+    bucket_start[C] = pos;
+    pos += bucket_count[C];
+  }
+  int fill[17];
   memcpy(fill, bucket_start, sizeof(fill));
+  int tc_pos = 0, n_parts = 0;
+  g_part_base[0] = 0;
   for (int r = 0; r < n; ++r) {
-    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok, g.head_dim, G, units);
-    g_work[fill[pl.variant][pl.C]++] = r;
+    const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, v.tc_ok);
+    if (pl.variant == gp::DEMAND_TC) {
+      g_work[tc_pos++] = r;
+      n_parts += units * gp::tc_parts(reqs[r].num_pages);
+      g_part_base[tc_pos] = n_parts;
+    } else {
+      g_work[fill[pl.C]++] = r;
+    }
   }
 
   // ---- uploads (from the caller's / static host memory; no staging buffers) --
@@ -188,8 +206,10 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
                         sizeof(int32_t) * reqs[r].num_pages, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + off_work, g_work, sizeof(int32_t) * n, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(base + off_pb, g_part_base, sizeof(int32_t) * (n_tc + 1), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(base + off_ksum, 0, sizeof(unsigned long long) * n * 2, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(base + off_tk, 0, sizeof(unsigned) * (size_t)n * units, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(base + off_tk, 0, sizeof(unsigned) * 2 * (size_t)n * units, s);
   if (e != cudaSuccess) return cuda_fail(c, "upload", e);
 
   gp::PrepArgs pa{};
@@ -210,40 +230,46 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   e = gp::launch_prep(pa, s);
   if (e != cudaSuccess) return cuda_fail(c, "prep_queries launch", e);
 
-  for (int k = 1; k >= 0; --k)
-    for (int C = 16; C >= 1; --C) {
-      if (!bucket_count[k][C]) continue;
-      const int var = k;
-      gp::DemandArgs da{};
-      if (var == gp::DEMAND_TC) da.kmap = *v.kmap;
-      da.variant = var;
-      da.k_cache = v.k_cache;
-      da.kv_f32 = g.kv_dtype == GP_DTYPE_F32;
-      da.num_pages_total = g.num_pages;
-      da.L = g.num_layers;
-      da.Hkv = g.num_kv_heads;
-      da.D = g.head_dim;
-      da.G = G;
-      da.b = kPage;
-      da.R = g.recent_window;
-      da.pfix = gp::coverage_fraction(g.p);
-      da.qt = pa.qt;
-      da.bq = pa.bq;
-      da.reqs = pa.reqs;
-      da.bt = reinterpret_cast<const int32_t*>(base + off_bt);
-      da.work = reinterpret_cast<const int32_t*>(base + off_work) + bucket_start[k][C];
-      da.n_work = bucket_count[k][C];
-      da.C = C;
-      da.ppc = bucket_ppc[k][C];
-      da.scores = reinterpret_cast<float*>(base + off_sc);
-      da.aval = reinterpret_cast<float*>(base + off_sc);
-      da.tickets = reinterpret_cast<unsigned*>(base + off_tk);
-      da.kout = reinterpret_cast<int32_t*>(base + off_kout);
-      da.ksum = reinterpret_cast<unsigned long long*>(base + off_ksum);
-      da.err = v.err_dev;
-      e = gp::launch_demand(da, s);
-      if (e != cudaSuccess) return cuda_fail(c, "boundary_demand launch", e);
-    }
+  for (int k = 0; k <= 16; ++k) {
+    // k = 0: the tensor-core launch; k = C: the CUDA-core bucket of cluster size C
+    const int C = k == 0 ? 1 : 17 - k;
+    const int count = k == 0 ? n_tc : bucket_count[C];
+    if (!count) continue;
+    const int var = k == 0 ? gp::DEMAND_TC : gp::DEMAND_FFMA;
+    gp::DemandArgs da{};
+    if (var == gp::DEMAND_TC) da.kmap = *v.kmap;
+    da.variant = var;
+    da.k_cache = v.k_cache;
+    da.kv_f32 = g.kv_dtype == GP_DTYPE_F32;
+    da.num_pages_total = g.num_pages;
+    da.L = g.num_layers;
+    da.Hkv = g.num_kv_heads;
+    da.D = g.head_dim;
+    da.G = G;
+    da.b = kPage;
+    da.R = g.recent_window;
+    da.pfix = gp::coverage_fraction(g.p);
+    da.qt = pa.qt;
+    da.bq = pa.bq;
+    da.reqs = pa.reqs;
+    da.bt = reinterpret_cast<const int32_t*>(base + off_bt);
+    da.work = reinterpret_cast<const int32_t*>(base + off_work) + (k == 0 ? 0 : bucket_start[C]);
+    da.n_work = count;
+    da.C = C;
+    da.ppc = k == 0 ? gp::TC_MAX_PPC : bucket_ppc[C];
+    da.part_base = reinterpret_cast<const int32_t*>(base + off_pb);
+    da.n_parts = n_parts;
+    da.xstat = reinterpret_cast<float2*>(base + off_xs);
+    da.xcount = reinterpret_cast<unsigned*>(base + off_tk) + (size_t)n * units;
+    da.scores = reinterpret_cast<float*>(base + off_sc);
+    da.aval = reinterpret_cast<float*>(base + off_sc);
+    da.tickets = reinterpret_cast<unsigned*>(base + off_tk);
+    da.kout = reinterpret_cast<int32_t*>(base + off_kout);
+    da.ksum = reinterpret_cast<unsigned long long*>(base + off_ksum);
+    da.err = v.err_dev;
+    e = gp::launch_demand(da, s);
+    if (e != cudaSuccess) return cuda_fail(c, "boundary_demand launch", e);
+  }
 
   // ---- results -------------------------------------------------------------
   int kerr = 0;

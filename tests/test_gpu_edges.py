@@ -3,8 +3,8 @@
 Small model shapes (2 layers, 2 KV heads) that reach every kernel variant:
 bf16 caches with head_dim 64 / 128 and GQA group 2 / 4 (the tensor-core scan
 and, when forced, the CUDA-core scan), an fp32 cache (CUDA-core only), and
-requests of 1, 2, 5, 33, 64, 65, 128 pages (tensor-core range, every
-cluster shape) and 129, 256 pages (beyond it: the CUDA-core scan, the
+requests of 1, 2, 5, 33, 64, 65, 128, 129, 160 pages (tensor-core range,
+every cluster shape) and 161, 256 pages (beyond it: the CUDA-core scan, the
 largest block table).  Against the fp64 oracle: D_p within the tie
 tolerance, the demand distributions within 1e-4, the importance, the
 decision (forced Grow at P = 1), the Eq. 10 keep masks and the compacted
@@ -27,7 +27,7 @@ import harness as hz
 pytestmark = pytest.mark.gpu
 
 PAGE = 256
-SIZES = [1, 2, 5, 33, 64, 65, 128, 129, 256]
+SIZES = [1, 2, 5, 33, 64, 65, 128, 129, 160, 161, 256]
 SHAPES = {
     "bf16_g4_d128": ModelShape(2, 8, 2, 128, "bf16", "bf16", 5.0e5),
     "bf16_g2_d128": ModelShape(2, 4, 2, 128, "bf16", "bf16", 5.0e5),
