@@ -57,14 +57,17 @@ def _peaks():
 
 
 KERNEL_OF = {"boundary_demand": "k_demand_tc", "compress_hold": "k_compress"}
+# the sources each kernel is built from (its capture is void once they change)
+KERNEL_SOURCES = {"k_demand_tc": ["k_demand_tc.cu", "demand_common.cuh", "gp_kernels.h"],
+                  "k_compress": ["k_compress.cu", "gp_kernels.h"]}
 
 
-def _sources_sha() -> str:
-    """sha256 over the kernel sources (file name and bytes, sorted by name)."""
+def _sources_sha(kernel: str) -> str:
+    """sha256 over a kernel's source files (file name and bytes, in order)."""
     import hashlib
     d = os.path.join(ROOT, "paged_kv_cache_step_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(f.encode())
         h.update(b"\0")
         with open(os.path.join(d, f), "rb") as fh:
@@ -74,14 +77,15 @@ def _sources_sha() -> str:
 
 def _traffic(kernel: str, bytes_per_launch: float):
     """DRAM bytes per launch from the committed ncu capture, scaled by the
-    launch's algorithmic bytes; None when the kernel sources have changed
+    launch's algorithmic bytes; None when the kernel's sources have changed
     since the capture or no capture exists."""
+    name = KERNEL_OF.get(kernel, "")
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f).get(KERNEL_OF.get(kernel, ""), None)
+            rec = json.load(f).get(name, None)
     except Exception:
         return None
-    if not rec or rec.get("source_sha256") != _sources_sha():
+    if not rec or rec.get("source_sha256") != _sources_sha(name):
         return None
     ratio = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["algorithmic_bytes"]
     return ratio * bytes_per_launch
@@ -296,13 +300,30 @@ def run_gpu(args, world, rank, local):
                                "ms_per_launch": cmp_["ms"] / cmp_["launches"]}
     dom = max(rl, key=lambda k: kern[k]["ms"]) if rl else None
 
-    # e2e: the boundary query copied from pinned host memory each step
+    actions = dict(s.actions)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(s, args.cpu_seconds)
+    gp.gp_destroy(s.ctx)
+    del s
+    torch.cuda.empty_cache()
+
+    # e2e: the same event sequence on a fresh, identical stream, with the
+    # boundary query copied from pinned host memory and the D_p sums read
+    # back every step, inside the timed region
     e2e = None
     if not args.no_e2e:
-        host_qs = [s._query().cpu().pin_memory() for _ in range(args.steps)]
-        dev_q = torch.empty_like(host_qs[0], device=device)
+        s = Stream(device)
+        s.advance(EVENT_STRIDE - 1)
+        for _ in range(args.warmup):
+            q = s._query()
+            one_event(q)
+            s.advance(EVENT_STRIDE - 1)
+        torch.cuda.synchronize()
+        dev_q = torch.empty_like(s._query(), device=device)
         e2e_times = []
-        for hq in host_qs:
+        for _ in range(args.steps):
+            hq = s._query().cpu().pin_memory()
             torch.cuda.synchronize()
             ev0 = torch.cuda.Event(enable_timing=True)
             ev1 = torch.cuda.Event(enable_timing=True)
@@ -318,7 +339,9 @@ def run_gpu(args, world, rank, local):
         h2d = s.q_bytes + 48 + 4 * maxp * 2 + 4
         d2h = 16 + 4
         e2e = {"value": len(e2e_times) / (sum(e2e_times) / 1e3), "unit": "events/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "events": "the timed events of the value line, replayed on an identical fresh stream"}
+        gp.gp_destroy(s.ctx)
 
     # aggregate over ranks (replicas): max time, summed events
     t_tot = torch.tensor([total_ms], dtype=torch.float64)
@@ -340,7 +363,7 @@ def run_gpu(args, world, rank, local):
         "kv_gbs": kv_gbs,
         "kv_frac": kv_gbs / peak,
         "scan_bytes": scan_bytes, "compaction_bytes": comp_bytes,
-        "actions": s.actions,
+        "actions": actions,
         "roofline": dict(rl[dom], kernel=dom, peak_source=peak_src,
                          traffic=_traffic(dom, rl[dom]["bytes_per_launch"])) if dom else None,
         "kernels": {k: dict(v, **({"frac": rl[k]["frac"], "achieved_gbs": rl[k]["achieved"]}
@@ -349,9 +372,8 @@ def run_gpu(args, world, rank, local):
         "clocks": clk,
         "e2e": e2e,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(s, args.cpu_seconds)
-    gp.gp_destroy(s.ctx)
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
     return out
 
 

@@ -56,6 +56,12 @@ struct PrepArgs {
   float* qt;               // [n][L][Hkv][2G][D], scaled by log2(e)/sqrt(D)
   unsigned char* bq;       // optional tensor-core operand per unit (bq_bytes each)
   int* err;
+  // counters the demand launches that follow need at zero (cleared here, so
+  // the call needs no separate memset operations)
+  unsigned* zero32;        // [n_zero32]
+  size_t n_zero32;
+  unsigned long long* zero64;  // [n_zero64]
+  int n_zero64;
 };
 // Bytes of the tensor-core B operand of one unit: D/64 swizzle halves of NB
 // rows x 128 B, NB = 3 x 2G rounded up to 16 (three bf16 parts per row).

@@ -597,8 +597,6 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     for (int32_t r : it->second) s.work[wpos++] = r;
   }
   if ((st = upload(c, s)) != GP_OK) return st;
-  GP_CUDA(c, cudaMemsetAsync(c->ksum.p, 0, sizeof(unsigned long long) * (size_t)n * 2, c->stream));
-  GP_CUDA(c, cudaMemsetAsync(c->tickets.p, 0, sizeof(unsigned) * 2 * (size_t)n * units, c->stream));
 
   gp::PrepArgs pa{};
   pa.pool = c->pool;
@@ -615,6 +613,10 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   pa.qt = static_cast<float*>(c->qt.p);
   pa.bq = static_cast<unsigned char*>(c->bq.p);
   pa.err = c->err_dev;
+  pa.zero32 = static_cast<unsigned*>(c->tickets.p);   // tickets and statistics counts
+  pa.n_zero32 = 2 * (size_t)n * units;
+  pa.zero64 = static_cast<unsigned long long*>(c->ksum.p);
+  pa.n_zero64 = n * 2;
   st = timed_launch(c, GP_KERNEL_PREP, "prep_queries", [&] { return gp::launch_prep(pa, c->stream); });
   if (st != GP_OK) return st;
 

@@ -91,6 +91,9 @@ __global__ void __launch_bounds__(256) k_prep_queries(PrepArgs a) {
   const int l = (blockIdx.x / hblocks) % a.L;
   const int r = blockIdx.x / (hblocks * a.L);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.n_zero32; i += (size_t)gridDim.x * blockDim.x)
+    a.zero32[i] = 0u;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_zero64; i += gridDim.x * blockDim.x) a.zero64[i] = 0ull;
   const DevReq rq = a.reqs[r];
   if (threadIdx.x < D / 2) {
     const double ang = (double)rq.pos * a.inv_freq[threadIdx.x];

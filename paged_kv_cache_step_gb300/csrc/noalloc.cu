@@ -208,8 +208,6 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
     e = cudaMemcpyAsync(base + off_work, g_work, sizeof(int32_t) * n, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + off_pb, g_part_base, sizeof(int32_t) * (n_tc + 1), cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(base + off_ksum, 0, sizeof(unsigned long long) * n * 2, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(base + off_tk, 0, sizeof(unsigned) * 2 * (size_t)n * units, s);
   if (e != cudaSuccess) return cuda_fail(c, "upload", e);
 
   gp::PrepArgs pa{};
@@ -227,6 +225,10 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   pa.qt = reinterpret_cast<float*>(base + off_qt);
   pa.bq = base + off_bq;
   pa.err = v.err_dev;
+  pa.zero32 = reinterpret_cast<unsigned*>(base + off_tk);  // tickets and statistics counts
+  pa.n_zero32 = 2 * (size_t)n * units;
+  pa.zero64 = reinterpret_cast<unsigned long long*>(base + off_ksum);
+  pa.n_zero64 = n * 2;
   e = gp::launch_prep(pa, s);
   if (e != cudaSuccess) return cuda_fail(c, "prep_queries launch", e);
 
