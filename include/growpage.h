@@ -69,8 +69,26 @@ typedef enum {
 } gp_status;
 
 typedef enum { GP_DTYPE_BF16 = 0, GP_DTYPE_F32 = 1 } gp_dtype;
-typedef enum { GP_POLICY_GROWPAGE = 0, GP_POLICY_FIXED = 1 } gp_policy;
-typedef enum { GP_ACT_GROW = 0, GP_ACT_COMPRESS = 1 } gp_action_kind;
+/* Capacity-control policies (GrowPage Sec. 3.2; the alternatives of App. H.1):
+ * GROWPAGE  Grow iff Delta > tau, else Compress & Hold;
+ * FIXED     never Grow (GrowPage-Fixed);
+ * RANDOM    Compress & Hold with probability random_compress, else Grow,
+ *           whatever Delta (GrowPage-Random); the draw of the engine's k-th
+ *           decision (k = 0, 1, ... since gp_create) is
+ *           u_k = (splitmix64(random_seed * 2^32 + k) >> 11) * 2^-53;
+ * INVERSE   Grow iff Delta <= tau, else Compress & Hold (GrowPage-Inverse);
+ * SHRINK    Eq. 13: Shrink iff Delta < shrink_threshold, Grow iff Delta > tau,
+ *           else Compress & Hold; Shrink only while the request holds more
+ *           than shrink_floor_pages pages (App. H.1: 1024 tokens), else
+ *           Compress & Hold. */
+typedef enum {
+  GP_POLICY_GROWPAGE = 0,
+  GP_POLICY_FIXED = 1,
+  GP_POLICY_RANDOM = 2,
+  GP_POLICY_INVERSE = 3,
+  GP_POLICY_SHRINK = 4
+} gp_policy;
+typedef enum { GP_ACT_GROW = 0, GP_ACT_COMPRESS = 1, GP_ACT_SHRINK = 2 } gp_action_kind;
 
 /* Engine configuration.  Defaults (gp_config_default) follow the paper:
  * page_size 256, recent_window 16, k_loc 64, beta_s 0.9, beta_l 0.999,
@@ -95,6 +113,11 @@ typedef struct gp_config {
   double p;                  /* coverage target of D_p, 0 < p < 1 */
   double tau;                /* decision threshold on Delta */
   double rope_theta;         /* rotate-half RoPE base */
+  /* policy variants (App. H.1); defaults 0.7, -0.005, 4 pages, 0 */
+  double random_compress;    /* RANDOM: probability of Compress & Hold */
+  double shrink_threshold;   /* SHRINK: Shrink iff Delta < this */
+  int32_t shrink_floor_pages;/* SHRINK: no Shrink at or below this many pages */
+  uint32_t random_seed;      /* RANDOM: seed of the counter-based draws */
 } gp_config;
 
 /* One request as the caller's scheduler sees it.  block_table is a HOST
@@ -136,6 +159,7 @@ typedef struct gp_stats_t {
   int64_t forced_grow;
   int64_t cow_pages;       /* shared pages replaced by copy-on-write */
   int64_t moved_rows;      /* (layer, head, token) rows moved by compaction */
+  int64_t shrink;          /* Shrink decisions (policy SHRINK) */
 } gp_stats_t;
 
 typedef struct gp_ctx gp_ctx;
@@ -221,10 +245,13 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* ctx, int32_t n, const gp_request* r
                                      const void* q_cur_dev, gp_demand* out,
                                      int32_t* k_units);
 
-/* gp_decide: Grow iff Delta > tau, else Compress & Hold (Sec. 3.2); P == 1
+/* gp_decide: per the configured policy (gp_policy above; GROWPAGE: Grow iff
+ * Delta > tau, else Compress & Hold, Sec. 3.2).  Delta is compared as
+ * delta = (sum_k_short - sum_k_long) / (num_candidates * num_units) in
+ * double (for tau == 0 the Grow test is the exact integer one).  P == 1
  * forces Grow; a Grow that would leave the pool at or below reserve_pages
  * (counting earlier grants of this call) becomes a fallback Compress
- * (Sec. 4.2).  policy FIXED never grows except when forced.  Host only. */
+ * (Sec. 4.2, App. H.2).  Host only. */
 gp_status gp_decide(gp_ctx* ctx, int32_t n, const gp_request* reqs,
                     const gp_demand* demand, gp_action* out);
 
@@ -247,6 +274,29 @@ gp_status gp_grow_page(gp_ctx* ctx, gp_request* req);
  * GP_ERR_NO_PAGES (not enough fresh pages for copy-on-write) changes
  * nothing.  Asynchronous on the stream. */
 gp_status gp_compress_hold(gp_ctx* ctx, int32_t n, gp_request* reqs);
+
+/* gp_shrink: Shrink (App. H.1, Eq. 13) for n requests prepared like those of
+ * gp_compress_hold (a gp_boundary_demand on the same slot, pages and block
+ * table): the same selection and copy-on-write as Compress & Hold, but with
+ * K_t = (P-2) b - R, so two pages' worth of history is compacted into
+ * logical slots [0, (P-2) b); the last page of the (new) block table is
+ * then returned to the pool (its reference dropped) and num_pages becomes
+ * P - 1, which leaves one page of free slots [(P-2) b, (P-1) b).  Needs
+ * P >= 3 (else GP_ERR_INVALID).  GP_ERR_NO_PAGES (copy-on-write) changes
+ * nothing.  Asynchronous on the stream. */
+gp_status gp_shrink(gp_ctx* ctx, int32_t n, gp_request* reqs);
+
+/* gp_compress_fill: Compress & Hold with hole-fill compaction -- NOT the
+ * paper's compaction, an order-destroying variant that moves far fewer
+ * bytes.  Selection and copy-on-write as gp_compress_hold (same keep
+ * masks), but the kept slots of the first P-1 logical pages stay where they
+ * are and the kept slots of the last page fill the holes (dropped slots of
+ * the first P-1 pages): the k-th kept slot of the last page (ascending) goes
+ * to the k-th hole (ascending).  Logical order and block locality are not
+ * preserved; num_pages is unchanged and logical slots [(P-1) b, P b) become
+ * free.  At most one page of rows moves per (layer, KV head).
+ * Asynchronous on the stream. */
+gp_status gp_compress_fill(gp_ctx* ctx, int32_t n, gp_request* reqs);
 
 /* gp_compact_kv: the compaction step of Compress & Hold for a caller-given
  * index set (App. E.2), with the same copy-on-write handling.

@@ -48,6 +48,7 @@ import numpy as np
 
 GROW = 0
 COMPRESS = 1
+SHRINK = 2
 
 
 # ---------------------------------------------------------------------------
@@ -284,22 +285,63 @@ class Action:
 
 
 def decide(delta: float, num_pages: int, free_pages: int, reserve: int,
-           tau: float, policy: str = "growpage") -> Action:
-    """Grow iff Delta > tau, else Compress & Hold (Sec. 3.2, after Eq. 8).
+           tau: float, policy: str = "growpage", draw: float = 0.0,
+           random_compress: float = 0.7, shrink_threshold: float = -0.005,
+           shrink_floor_pages: int = 4) -> Action:
+    """The capacity decision for one request at a boundary.
 
-    P = 1 forces Grow (there is no history to compress).  A Grow the free
-    pool cannot grant above ``reserve`` pages falls back to Compress
-    (Sec. 4.2; App. H.2 defines a fallback).  Policy "fixed" never grows
-    (GrowPage-Fixed, App. H.1) except when P = 1.
+    GrowPage (Sec. 3.2, after Eq. 8): Grow iff Delta > tau, else Compress &
+    Hold.  P = 1 forces Grow (there is no history to compress).  A Grow the
+    free pool cannot grant above ``reserve`` pages falls back to Compress
+    (Sec. 4.2; App. H.2 defines a fallback).  The alternatives of App. H.1:
+    "fixed" never grows; "random" compresses with probability
+    ``random_compress`` (the uniform ``draw`` decides), whatever Delta;
+    "inverse" grows iff Delta <= tau; "shrink" follows Eq. 13: Shrink if
+    Delta < -0.005, Compress & Hold if -0.005 <= Delta <= 0, Grow if
+    Delta > 0, with no Shrink at or below the 1024-token floor.
     """
     if num_pages <= 1:
         return Action(GROW, forced=True)
-    want_grow = (policy == "growpage") and (delta > tau)
+    shrink = False
+    if policy == "growpage":
+        want_grow = delta > tau
+    elif policy == "fixed":
+        want_grow = False
+    elif policy == "random":
+        want_grow = not (draw < random_compress)
+    elif policy == "inverse":
+        want_grow = not (delta > tau)
+    elif policy == "shrink":
+        want_grow = delta > tau
+        shrink = (not want_grow) and delta < shrink_threshold and num_pages > shrink_floor_pages
+    else:
+        raise ValueError(policy)
     if want_grow:
         if free_pages > reserve:
             return Action(GROW)
         return Action(COMPRESS, fallback=True)
+    if shrink:
+        return Action(SHRINK)
     return Action(COMPRESS)
+
+
+# SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+# generators", OOPSLA 2014): one output of the generator whose state is x,
+# i.e. x advanced by the golden-ratio increment and then mixed.
+_M64 = (1 << 64) - 1
+
+
+def splitmix64(x: int) -> int:
+    z = (x + 0x9E3779B97F4A7C15) & _M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)
+
+
+def policy_draw(seed: int, k: int) -> float:
+    """Uniform [0, 1) draw of the k-th decision for the random policy:
+    the top 53 bits of splitmix64(seed * 2^32 + k), scaled by 2^-53."""
+    return (splitmix64(((seed << 32) + k) & _M64) >> 11) / float(1 << 53)
 
 
 # ---------------------------------------------------------------------------
@@ -319,24 +361,26 @@ def _top_by_score(cands: np.ndarray, s: np.ndarray, k: int) -> np.ndarray:
     return cands[order[:k]]
 
 
-def retention_budget(num_pages: int, page_size: int, recent: int) -> int:
-    """K_t: historical tokens kept so that (P-1) b slots stay occupied."""
-    return (num_pages - 1) * page_size - recent
+def retention_budget(num_pages: int, page_size: int, recent: int, drop: int = 1) -> int:
+    """K_t: historical tokens kept so that (P - drop) b slots stay occupied
+    (drop = 1 for Compress & Hold, 2 for Shrink, App. H.1)."""
+    return (num_pages - drop) * page_size - recent
 
 
 def select_retained(s, num_pages: int, page_size: int, recent: int,
-                    k_loc: int) -> np.ndarray:
+                    k_loc: int, drop: int = 1) -> np.ndarray:
     """Keep mask over the P*b slots of one (layer, KV head) (Eq. 10).
 
     S_loc = union over blocks j of TopK_{k_loc'}(B_j; s);
     S = S_loc  union  TopK_{K_t - |S_loc|}(Ccmp minus S_loc; s);
     the protected recent window [P b - R, P b) is always kept (Sec. 3.3,
-    Sec. 5.1).  Exactly (P-1) b slots are kept, freeing one page.
+    Sec. 5.1).  Exactly (P - drop) b slots are kept: one page freed by
+    Compress & Hold, two pages' worth by Shrink (App. H.1).
     """
     s = np.asarray(s, np.float64)
     n = num_pages * page_size
     n_cmp = n - recent
-    k_t = retention_budget(num_pages, page_size, recent)
+    k_t = retention_budget(num_pages, page_size, recent, drop)
     keep = np.zeros(n, dtype=bool)
     keep[n_cmp:] = True
     quota = min(k_loc, k_t // num_pages) if num_pages > 0 else 0
@@ -422,6 +466,31 @@ def release_replaced(replaced, pool: PagePool):
     """After compaction the request drops its references to replaced pages."""
     for pg in replaced:
         pool.unref(pg)
+
+
+def shrink_release(new_table, pool: PagePool) -> list:
+    """Shrink (App. H.1): after two pages' worth of history has been
+    compacted into logical slots [0, (P-2) b), the emptied last page of the
+    block table goes back to the pool; the request keeps P - 1 pages, the
+    last of them with b free slots."""
+    pool.unref(new_table[-1])
+    return list(new_table[:-1])
+
+
+def hole_fill_unit(rows, keep, num_pages: int, page_size: int):
+    """Hole-fill variant of the compaction (order-destroying; not the
+    paper's): kept rows of the first P-1 pages stay in their slots, and the
+    k-th kept row of the last page (ascending) fills the k-th dropped slot of
+    the first P-1 pages (ascending).  Returns rows [(P-1) b][d]."""
+    rows = np.asarray(rows)
+    keep = np.asarray(keep, dtype=bool)
+    lastp = (num_pages - 1) * page_size
+    out = rows[:lastp].copy()
+    holes = np.nonzero(~keep[:lastp])[0]
+    fillers = np.nonzero(keep[lastp:num_pages * page_size])[0] + lastp
+    assert holes.size == fillers.size
+    out[holes] = rows[fillers]
+    return out
 
 
 def compact_unit(rows, keep):

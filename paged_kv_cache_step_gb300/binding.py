@@ -23,8 +23,8 @@ from . import _build_lib
 GP_OK, GP_ERR_INVALID, GP_ERR_NO_PAGES, GP_ERR_NO_SLOTS = 0, 1, 2, 3
 GP_ERR_CUDA, GP_ERR_TIMEOUT, GP_ERR_STATE, GP_ERR_UNSUPPORTED = 4, 5, 6, 7
 GP_DTYPE_BF16, GP_DTYPE_F32 = 0, 1
-GP_POLICY_GROWPAGE, GP_POLICY_FIXED = 0, 1
-GP_ACT_GROW, GP_ACT_COMPRESS = 0, 1
+GP_POLICY_GROWPAGE, GP_POLICY_FIXED, GP_POLICY_RANDOM, GP_POLICY_INVERSE, GP_POLICY_SHRINK = 0, 1, 2, 3, 4
+GP_ACT_GROW, GP_ACT_COMPRESS, GP_ACT_SHRINK = 0, 1, 2
 GP_SCAN_AUTO, GP_SCAN_CUDA_CORE, GP_SCAN_TENSOR_CORE = 0, 1, 2
 GP_KERNEL_EMA, GP_KERNEL_PREP, GP_KERNEL_DEMAND, GP_KERNEL_COMPRESS = 0, 1, 2, 3
 KERNEL_NAMES = {0: "ema_update", 1: "prep_queries", 2: "boundary_demand", 3: "compress_hold"}
@@ -34,7 +34,8 @@ EXPORTS = [
     "gp_page_alloc", "gp_page_ref", "gp_page_unref", "gp_page_refcount", "gp_free_page_count",
     "gp_slot_acquire", "gp_slot_release", "gp_update_summaries", "gp_boundary_demand",
     "gp_boundary_demand_noalloc",
-    "gp_decide", "gp_grow_page", "gp_compress_hold", "gp_compact_kv", "gp_debug_demand_k",
+    "gp_decide", "gp_grow_page", "gp_compress_hold", "gp_shrink", "gp_compress_fill", "gp_compact_kv",
+    "gp_debug_demand_k",
     "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
     "gp_set_scan_kernel", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
 ]
@@ -49,6 +50,8 @@ class GpConfig(C.Structure):
         ("reserve_pages", C.c_int32), ("policy", C.c_int32),
         ("beta_s", C.c_double), ("beta_l", C.c_double), ("p", C.c_double), ("tau", C.c_double),
         ("rope_theta", C.c_double),
+        ("random_compress", C.c_double), ("shrink_threshold", C.c_double),
+        ("shrink_floor_pages", C.c_int32), ("random_seed", C.c_uint32),
     ]
 
 
@@ -68,7 +71,8 @@ class GpAction(C.Structure):
 
 class GpStats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("demand_calls", "demand_requests", "grow", "compress",
-                                          "fallback", "forced_grow", "cow_pages", "moved_rows")]
+                                          "fallback", "forced_grow", "cow_pages", "moved_rows",
+                                          "shrink")]
 
 
 class GrowPageError(RuntimeError):
@@ -116,6 +120,8 @@ def load(build_if_missing: bool = True):
         "gp_decide": (I32, [P, I32, C.POINTER(GpRequest), C.POINTER(GpDemand), C.POINTER(GpAction)]),
         "gp_grow_page": (I32, [P, C.POINTER(GpRequest)]),
         "gp_compress_hold": (I32, [P, I32, C.POINTER(GpRequest)]),
+        "gp_shrink": (I32, [P, I32, C.POINTER(GpRequest)]),
+        "gp_compress_fill": (I32, [P, I32, C.POINTER(GpRequest)]),
         "gp_compact_kv": (I32, [P, I32, C.POINTER(GpRequest), P]),
         "gp_debug_demand_k": (I32, [P, I32, P]),
         "gp_debug_scores": (I32, [P, I32, P]),
@@ -289,6 +295,20 @@ def gp_grow_page(ctx, req: Request):
 def gp_compress_hold(ctx, reqs):
     arr = _marshal(reqs)
     st = load().gp_compress_hold(ctx, len(reqs), arr)
+    _unmarshal(arr, reqs)
+    _check(ctx, st)
+
+
+def gp_shrink(ctx, reqs):
+    arr = _marshal(reqs)
+    st = load().gp_shrink(ctx, len(reqs), arr)
+    _unmarshal(arr, reqs)
+    _check(ctx, st)
+
+
+def gp_compress_fill(ctx, reqs):
+    arr = _marshal(reqs)
+    st = load().gp_compress_fill(ctx, len(reqs), arr)
     _unmarshal(arr, reqs)
     _check(ctx, st)
 

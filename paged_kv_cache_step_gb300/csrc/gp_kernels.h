@@ -161,6 +161,8 @@ struct CompressArgs {
   int num_pages_total;
   int L, Hkv, D, elt;      // elt = bytes per element
   int b, R, k_loc;
+  int drop;                // pages' worth of history dropped: 1 Compress & Hold, 2 Shrink
+  int fill;                // 1: hole-fill compaction (order-destroying), 0: stable
   const DevReq* reqs;
   const int32_t* old_bt;
   const int32_t* new_bt;

@@ -87,6 +87,7 @@ struct gp_ctx {
   std::vector<CompressRec> last_compress;
 
   gp_stats_t stats{};
+  int64_t decisions = 0;           // decisions taken so far (index of the RANDOM policy's draws)
   bool timing = false;
   std::vector<TimedEvent> timed;
   std::vector<cudaEvent_t> event_pool;
@@ -275,6 +276,10 @@ gp_status gp_config_default(gp_config* cfg) {
   cfg->p = 0.99;
   cfg->tau = 0.0;
   cfg->rope_theta = 10000.0;
+  cfg->random_compress = 0.7;
+  cfg->shrink_threshold = -0.005;
+  cfg->shrink_floor_pages = 4;  // 1024 tokens
+  cfg->random_seed = 0u;
   return GP_OK;
 }
 
@@ -295,7 +300,10 @@ gp_status gp_create(const gp_config* cfg, void* k_cache, void* v_cache, void* st
   if (g.max_pages_per_req > kMaxPagesPerReq) return GP_ERR_UNSUPPORTED;
   if (g.recent_window < 0 || g.recent_window >= kPage || g.k_loc < 0 || g.reserve_pages < 0)
     return GP_ERR_INVALID;
-  if (g.policy != GP_POLICY_GROWPAGE && g.policy != GP_POLICY_FIXED) return GP_ERR_INVALID;
+  if (g.policy < GP_POLICY_GROWPAGE || g.policy > GP_POLICY_SHRINK) return GP_ERR_INVALID;
+  if (!(g.random_compress >= 0.0 && g.random_compress <= 1.0) || !std::isfinite(g.shrink_threshold) ||
+      g.shrink_floor_pages < 2)
+    return GP_ERR_INVALID;
   if (!(g.p > 0.0 && g.p < 1.0) || !(g.beta_s >= 0.0 && g.beta_s < 1.0) ||
       !(g.beta_l >= 0.0 && g.beta_l < 1.0) || !(g.rope_theta > 0.0) || !std::isfinite(g.tau))
     return GP_ERR_INVALID;
@@ -685,28 +693,59 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   return GP_OK;
 }
 
+namespace {
+
+// SplitMix64 output function (Steele, Lea and Flood, OOPSLA 2014): the
+// state x advanced by the golden-ratio increment, then mixed.
+uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Uniform draw in [0, 1) of the k-th decision of a context.
+double policy_draw(uint32_t seed, int64_t k) {
+  const uint64_t v = splitmix64(((uint64_t)seed << 32) + (uint64_t)k);
+  return (double)(v >> 11) * (1.0 / 9007199254740992.0);  // 2^-53
+}
+
+}  // namespace
+
 gp_status gp_decide(gp_ctx* c, int32_t n, const gp_request* reqs, const gp_demand* demand, gp_action* out) {
   if (!c) return GP_ERR_INVALID;
   if (n < 0) return fail(c, GP_ERR_INVALID, "negative n");
   if (n > 0 && (!reqs || !demand || !out)) return fail(c, GP_ERR_INVALID, "null argument");
   const gp_config& g = c->cfg;
+  for (int r = 0; r < n; ++r)
+    if (reqs[r].num_pages < 1) return fail(c, GP_ERR_INVALID, "request %d: num_pages %d", r, reqs[r].num_pages);
   int64_t free_now = (int64_t)c->free_pages.size();
   int64_t granted = 0;
   for (int r = 0; r < n; ++r) {
     const int P = reqs[r].num_pages;
-    if (P < 1) return fail(c, GP_ERR_INVALID, "request %d: num_pages %d", r, P);
     gp_action a{GP_ACT_COMPRESS, 0, 0};
+    const int64_t k = c->decisions++;
     if (P == 1) {
       a.kind = GP_ACT_GROW;
       a.forced = 1;
     } else {
-      // Delta > tau, evaluated exactly from the integer sums for tau = 0
       const double units = (double)demand[r].num_units;
       const double cand = (double)demand[r].num_candidates;
       const int64_t diff = demand[r].sum_k_short - demand[r].sum_k_long;
-      bool want = false;
-      if (g.policy == GP_POLICY_GROWPAGE) {
-        want = (g.tau == 0.0) ? diff > 0 : ((double)diff / (cand * units)) > g.tau;
+      const double delta = (double)diff / (cand * units);
+      // Delta > tau; for tau = 0 the exact integer test
+      const bool above_tau = (g.tau == 0.0) ? diff > 0 : delta > g.tau;
+      bool want = false, shrink = false;
+      switch (g.policy) {
+        case GP_POLICY_GROWPAGE: want = above_tau; break;
+        case GP_POLICY_FIXED: want = false; break;
+        case GP_POLICY_RANDOM: want = !(policy_draw(g.random_seed, k) < g.random_compress); break;
+        case GP_POLICY_INVERSE: want = !above_tau; break;
+        case GP_POLICY_SHRINK:
+          want = above_tau;
+          shrink = !want && delta < g.shrink_threshold && P > g.shrink_floor_pages;
+          break;
+        default: break;
       }
       if (want) {
         if (free_now - granted > (int64_t)g.reserve_pages) {
@@ -716,12 +755,16 @@ gp_status gp_decide(gp_ctx* c, int32_t n, const gp_request* reqs, const gp_deman
           a.kind = GP_ACT_COMPRESS;
           a.fallback = 1;
         }
+      } else if (shrink) {
+        a.kind = GP_ACT_SHRINK;
       }
     }
     out[r] = a;
     if (a.kind == GP_ACT_GROW) {
       c->stats.grow += 1;
       if (a.forced) c->stats.forced_grow += 1;
+    } else if (a.kind == GP_ACT_SHRINK) {
+      c->stats.shrink += 1;
     } else {
       c->stats.compress += 1;
       if (a.fallback) c->stats.fallback += 1;
@@ -747,7 +790,10 @@ gp_status gp_grow_page(gp_ctx* c, gp_request* req) {
 namespace {
 
 // Shared path of gp_compress_hold (keep_in == null) and gp_compact_kv.
-gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t* keep_in) {
+// drop: pages' worth of history dropped per (layer, KV head): 1 for Compress &
+// Hold, 2 for Shrink (which then returns the emptied last page).
+// fill: hole-fill compaction (order-destroying) instead of the stable one.
+gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t* keep_in, int drop, int fill = 0) {
   gp_status st = need_device(c);
   if (st != GP_OK) return st;
   if (n < 0 || n > c->cfg.max_slots) return fail(c, GP_ERR_INVALID, "n = %d outside [0, max_slots]", n);
@@ -761,8 +807,9 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
   for (int r = 0; r < n; ++r) {
     st = validate_request(c, reqs[r], r, keep_in == nullptr);
     if (st != GP_OK) return st;
-    if (reqs[r].num_pages < 2)
-      return fail(c, GP_ERR_INVALID, "request %d: Compress & Hold needs at least 2 pages", r);
+    if (reqs[r].num_pages < drop + 1)
+      return fail(c, GP_ERR_INVALID, "request %d: %s needs at least %d pages", r,
+                  drop == 1 ? "Compress & Hold" : "Shrink", drop + 1);
     if (keep_in == nullptr) {
       if (!slots.insert(reqs[r].slot).second)
         return fail(c, GP_ERR_INVALID, "slot %d appears twice in one call", reqs[r].slot);
@@ -833,6 +880,8 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
   ca.b = kPage;
   ca.R = g.recent_window;
   ca.k_loc = g.k_loc;
+  ca.drop = drop;
+  ca.fill = fill;
   ca.reqs = dev_at<gp::DevReq>(c, 0);
   ca.old_bt = dev_at<int32_t>(c, s.off_bt);
   ca.new_bt = dev_at<int32_t>(c, s.off_bt_new);
@@ -860,6 +909,11 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
     for (int j = 0; j < P; ++j) reqs[r].block_table[j] = s.bt_new[(size_t)r * maxp + j];
     for (int32_t pg : replaced[r]) gp_page_unref(c, pg);
     c->stats.cow_pages += (int64_t)replaced[r].size();
+    if (drop == 2) {
+      // Shrink: the emptied last page goes back to the pool
+      gp_page_unref(c, reqs[r].block_table[P - 1]);
+      reqs[r].num_pages = P - 1;
+    }
     if (reqs[r].slot >= 0 && reqs[r].slot < g.max_slots) ++c->slot_gen[reqs[r].slot];
     c->last_compress[r].num_pages = P;
     c->last_compress[r].mask_off = mask_off[r];
@@ -869,12 +923,18 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
 
 }  // namespace
 
-gp_status gp_compress_hold(gp_ctx* c, int32_t n, gp_request* reqs) { return compress_common(c, n, reqs, nullptr); }
+gp_status gp_compress_hold(gp_ctx* c, int32_t n, gp_request* reqs) { return compress_common(c, n, reqs, nullptr, 1); }
+
+gp_status gp_shrink(gp_ctx* c, int32_t n, gp_request* reqs) { return compress_common(c, n, reqs, nullptr, 2); }
+
+gp_status gp_compress_fill(gp_ctx* c, int32_t n, gp_request* reqs) {
+  return compress_common(c, n, reqs, nullptr, 1, 1);
+}
 
 gp_status gp_compact_kv(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t* keep_masks_dev) {
   if (!c) return GP_ERR_INVALID;
   if (n > 0 && !keep_masks_dev) return fail(c, GP_ERR_INVALID, "null keep masks");
-  return compress_common(c, n, reqs, keep_masks_dev);
+  return compress_common(c, n, reqs, keep_masks_dev, 1);
 }
 
 // ---- inspection --------------------------------------------------------------

@@ -25,6 +25,10 @@
 //                in-place pass race-free with several chunks in flight.
 //                Rows whose physical location does not change are neither
 //                read nor written.
+//  hole-fill  -- an order-destroying variant (not the paper's compaction):
+//                kept rows of the first P-1 pages stay where they are and
+//                the last page's kept rows fill the holes, the k-th of them
+//                the k-th hole; at most a page of rows moves per unit.
 #include <cstdint>
 
 #include "gp_kernels.h"
@@ -151,6 +155,8 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
   __shared__ unsigned whist[NWARP][256];
   __shared__ unsigned red[NWARP];
   __shared__ int s_old[PAGE], s_new[PAGE];
+  __shared__ int s_hole[PAGE];            // hole-fill mode: the holes in order
+  __shared__ int s_nholes;
   __shared__ unsigned s_sel[4];           // prefix, mask, above, flags
   __shared__ int s_abort;
 
@@ -165,8 +171,8 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
   const int N = P * PAGE;
   const int words = N / 32;
   const int ncmp = N - a.R;
-  const int kt = (P - 1) * PAGE - a.R;
-  const unsigned target_kept = (unsigned)((P - 1) * PAGE);
+  const int kt = (P - a.drop) * PAGE - a.R;          // K_t (Eq. 10); Shrink drops two pages' worth
+  const unsigned target_kept = (unsigned)((P - a.drop) * PAGE);
 
   if (tid == 0) {
     s_abort = 0;
@@ -401,6 +407,26 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
 
   // ---- compaction ---------------------------------------------------------
   word_prefix(keep, pre, words, red);
+  // hole-fill mode: the holes (slots of [0, (P-1) b) not kept), in order;
+  // the k-th kept slot of the last page fills the k-th hole
+  const int lastp = (P - 1) * PAGE;
+  if (a.fill) {
+    if (warp == 0) {
+      int nh = 0;
+      for (int w = 0; w < lastp / 32; ++w) {
+        const bool hole = !((keep[w] >> lane) & 1u);
+        const unsigned b = __ballot_sync(0xffffffffu, hole);
+        if (hole && nh + __popc(b & ((1u << lane) - 1u)) < PAGE) s_hole[nh + __popc(b & ((1u << lane) - 1u))] = w * 32 + lane;
+        nh += __popc(b);
+      }
+      if (lane == 0) {
+        if (nh > PAGE) atomicOr(a.err, ERR_BAD_COUNT);
+        s_nholes = min(nh, PAGE);
+      }
+    }
+    __syncthreads();
+  }
+  const int kept_first = lastp - (a.fill ? s_nholes : 0);  // kept slots of the first P-1 pages
   constexpr int CR = (16384 / RB) < 64 ? (16384 / RB) : 64;  // rows per chunk: K and V of it fill a stage
   constexpr int PIECES = RB / 16;                            // 16-byte pieces per row
   static_assert(2 * CR * RB <= STAGE_BYTES && PAGE % CR == 0 && CR % 32 == 0, "chunk shape");
@@ -414,7 +440,14 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
     const int w = i >> 5, bit = i & 31;
     const unsigned word = keep[w];
     if (!((word >> bit) & 1u)) return -1;
-    const int dst = (int)(pre[w] + __popc(word & ((1u << bit) - 1u)));
+    int dst;
+    if (a.fill) {
+      // kept rows of the first P-1 pages stay; the last page's kept rows fill the holes
+      const int rank = (int)(pre[w] + __popc(word & ((1u << bit) - 1u))) - kept_first;
+      dst = i < lastp ? i : s_hole[min(PAGE - 1, max(0, rank))];
+    } else {
+      dst = (int)(pre[w] + __popc(word & ((1u << bit) - 1u)));
+    }
     return (s_old[i >> 8] == s_new[dst >> 8] && (i & 255) == (dst & 255)) ? -1 : dst;
   };
   // chunks that move any row, in order (loc is free once the keep words exist)

@@ -156,7 +156,7 @@ def dp_ok(gpu_k: int, a_oracle: np.ndarray, p: float):
     return False, f"gpu {gpu_k} oracle {k} (C_(D-1)={before!r}, C_D={at!r})"
 
 
-def topk_ok(gpu_keep: np.ndarray, s: np.ndarray, P: int, recent=16, k_loc=64):
+def topk_ok(gpu_keep: np.ndarray, s: np.ndarray, P: int, recent=16, k_loc=64, drop=1):
     """Compare a GPU keep mask with the oracle's Eq. 10 selection.
 
     Returns (ok, n_diff, message).  Differences are allowed only for slots
@@ -166,12 +166,12 @@ def topk_ok(gpu_keep: np.ndarray, s: np.ndarray, P: int, recent=16, k_loc=64):
     b = PAGE
     n = P * b
     ncmp = n - recent
-    kt = (P - 1) * b - recent
-    ref = og.select_retained(s, P, b, recent, k_loc)
+    kt = (P - drop) * b - recent
+    ref = og.select_retained(s, P, b, recent, k_loc, drop)
     gk = np.asarray(gpu_keep[:n], dtype=bool)
     # validity of the GPU set on its own
-    if gk.sum() != (P - 1) * b:
-        return False, -1, f"kept {gk.sum()} != {(P - 1) * b}"
+    if gk.sum() != (P - drop) * b:
+        return False, -1, f"kept {gk.sum()} != {(P - drop) * b}"
     if not gk[ncmp:].all():
         return False, -1, "recent window not kept"
     quota = min(k_loc, kt // P)

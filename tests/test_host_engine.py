@@ -47,9 +47,10 @@ def test_struct_layout_matches_header():
 #include <stddef.h>
 #include "growpage.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(gp_config), offsetof(gp_config, beta_s),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(gp_config), offsetof(gp_config, beta_s),
          offsetof(gp_config, rope_theta), sizeof(gp_request), offsetof(gp_request, pos),
-         sizeof(gp_demand), sizeof(gp_action), sizeof(gp_stats_t));
+         sizeof(gp_demand), sizeof(gp_action), sizeof(gp_stats_t), offsetof(gp_config, shrink_threshold),
+         offsetof(gp_config, random_seed), offsetof(gp_stats_t, shrink));
   return 0;
 }
 """
@@ -63,7 +64,8 @@ int main(void) {
     import ctypes as C
     ref = [C.sizeof(gp.GpConfig), gp.GpConfig.beta_s.offset, gp.GpConfig.rope_theta.offset,
            C.sizeof(gp.GpRequest), gp.GpRequest.pos.offset, C.sizeof(gp.GpDemand),
-           C.sizeof(gp.GpAction), C.sizeof(gp.GpStats)]
+           C.sizeof(gp.GpAction), C.sizeof(gp.GpStats), gp.GpConfig.shrink_threshold.offset,
+           gp.GpConfig.random_seed.offset, gp.GpStats.shrink.offset]
     assert vals == ref
 
 
@@ -228,3 +230,60 @@ def test_mask_pack_roundtrip():
     rng = np.random.default_rng(2)
     keep = rng.random((3, 512)) < 0.5
     assert np.array_equal(gp.unpack_mask(gp.pack_mask(keep), 512), keep)
+
+
+POLICIES = {"growpage": gp.GP_POLICY_GROWPAGE, "fixed": gp.GP_POLICY_FIXED, "random": gp.GP_POLICY_RANDOM,
+            "inverse": gp.GP_POLICY_INVERSE, "shrink": gp.GP_POLICY_SHRINK}
+
+
+@pytest.mark.parametrize("policy", sorted(POLICIES))
+def test_decide_policies_match_oracle(policy):
+    """Every policy of App. H.1 against the oracle's rules, over random sums,
+    sizes and pool states; the random policy's draws follow the decision
+    counter, so the oracle replays them from its own generator."""
+    rng = np.random.default_rng(11)
+    ctx = _host_ctx(num_pages=64, policy=POLICIES[policy], random_seed=5)
+    try:
+        units, k = 8, 0
+        for trial in range(60):
+            n = int(rng.integers(1, 9))
+            reqs, dem = [], []
+            for i in range(n):
+                P = int(rng.integers(1, 9))
+                reqs.append(gp.Request(i, list(range(P)), P * 256, 8))
+                cand = (P - 1) * 256
+                d = gp.GpDemand()
+                d.num_candidates, d.num_units = cand, units
+                # Delta spread over the zones of Eq. 13 (and exactly 0)
+                delta = float(rng.choice([0.0, -0.005, 0.02, -0.02, rng.normal(0, 0.01)]))
+                base = int(rng.integers(0, cand * units + 1)) if cand else 0
+                d.sum_k_long = base
+                d.sum_k_short = base + int(round(delta * cand * units))
+                d.delta = 0.0
+                dem.append(d)
+            free = gp.gp_free_page_count(ctx)
+            acts = gp.gp_decide(ctx, reqs, dem)
+            granted = 0
+            for r, (q, d, a) in enumerate(zip(reqs, dem, acts)):
+                P = q.num_pages
+                delta = (d.sum_k_short - d.sum_k_long) / (d.num_candidates * d.num_units) if P > 1 else 0.0
+                ref = og.decide(delta, P, free - granted, 0, 0.0, policy=policy, draw=og.policy_draw(5, k))
+                k += 1
+                assert (a.kind, bool(a.fallback), bool(a.forced)) == (ref.kind, ref.fallback, ref.forced), \
+                    (policy, trial, r, P, delta)
+                granted += int(a.kind == gp.GP_ACT_GROW and not a.forced)
+        st = gp.gp_stats(ctx)
+        assert st["grow"] + st["compress"] + st["shrink"] == k
+        if policy == "shrink":
+            assert st["shrink"] > 0
+        if policy == "random":
+            assert 0.55 < st["compress"] / max(1, k - st["forced_grow"]) < 0.85
+    finally:
+        gp.gp_destroy(ctx)
+
+
+def test_policy_config_validation():
+    for bad in (dict(policy=9), dict(random_compress=1.5), dict(shrink_floor_pages=1),
+                dict(shrink_threshold=float("nan"))):
+        with pytest.raises(gp.GrowPageError):
+            _host_ctx(**bad)

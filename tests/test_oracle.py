@@ -498,3 +498,87 @@ def test_oracle_exports():
                  "coverage_demand", "select_retained", "cow_plan", "compress_cache",
                  "worst_case_capacity"):
         assert hasattr(oracle, name)
+
+
+# ---------------------------------------------------------------------------
+# policy variants (App. H.1) and their counter-based draws
+# ---------------------------------------------------------------------------
+
+def test_splitmix64_published_sequence():
+    # the reference generator's first outputs for seed 1234567 (state
+    # advanced by the golden-ratio increment before each output)
+    x, out = 1234567, []
+    for _ in range(5):
+        out.append(og.splitmix64(x))
+        x = (x + 0x9E3779B97F4A7C15) % (1 << 64)
+    assert out == [6457827717110365317, 3203168211198807973, 9817491932198370423,
+                   4593380528125082431, 16408922859458223821]
+
+
+def test_policy_draws_are_uniform_and_keyed():
+    u = [og.policy_draw(7, k) for k in range(20000)]
+    assert all(0.0 <= x < 1.0 for x in u)
+    assert abs(np.mean(u) - 0.5) < 0.01 and abs(np.mean(np.array(u) < 0.7) - 0.7) < 0.01
+    assert og.policy_draw(7, 3) != og.policy_draw(8, 3)
+
+
+def test_eq13_shrink_zones():
+    d = lambda delta, P=16, free=10: og.decide(delta, P, free, 0, 0.0, policy="shrink")
+    assert d(0.001).kind == og.GROW
+    assert d(0.0).kind == og.COMPRESS                     # -0.005 <= Delta <= 0
+    assert d(-0.005).kind == og.COMPRESS
+    assert d(-0.0051).kind == og.SHRINK
+    assert d(-0.2, P=4).kind == og.COMPRESS                # 1024-token floor: 4 pages
+    assert d(-0.2, P=5).kind == og.SHRINK
+    assert d(0.3, free=0).kind == og.COMPRESS and d(0.3, free=0).fallback
+
+
+def test_inverse_fixed_random_rules():
+    assert og.decide(0.1, 8, 5, 0, 0.0, policy="inverse").kind == og.COMPRESS
+    assert og.decide(0.0, 8, 5, 0, 0.0, policy="inverse").kind == og.GROW
+    assert og.decide(-0.1, 8, 5, 0, 0.0, policy="inverse").kind == og.GROW
+    assert og.decide(0.5, 8, 5, 0, 0.0, policy="fixed").kind == og.COMPRESS
+    assert og.decide(0.5, 1, 5, 0, 0.0, policy="fixed").forced
+    assert og.decide(-0.5, 8, 5, 0, 0.0, policy="random", draw=0.69).kind == og.COMPRESS
+    assert og.decide(-0.5, 8, 5, 0, 0.0, policy="random", draw=0.7).kind == og.GROW
+
+
+def test_shrink_selection_keeps_two_pages_less():
+    rng = np.random.default_rng(3)
+    for P in (3, 5, 9):
+        s = rng.random(P * 256 - 16)
+        keep = og.select_retained(s, P, 256, 16, 64, drop=2)
+        assert keep.sum() == (P - 2) * 256
+        assert keep[P * 256 - 16:].all()
+        quota = min(64, ((P - 2) * 256 - 16) // P)
+        for j in range(P):
+            lo, hi = j * 256, min((j + 1) * 256, P * 256 - 16)
+            top = np.argsort(-s[lo:hi], kind="stable")[:quota] + lo
+            assert keep[top].all()
+        # everything kept outranks everything dropped outside the block quotas
+        loc = np.zeros(P * 256, bool)
+        for j in range(P):
+            lo, hi = j * 256, min((j + 1) * 256, P * 256 - 16)
+            loc[np.argsort(-s[lo:hi], kind="stable")[:quota] + lo] = True
+        cand = ~loc
+        cand[P * 256 - 16:] = False
+        kept, dropped = s[keep[:P * 256 - 16] & cand[:P * 256 - 16]], s[~keep[:P * 256 - 16]]
+        assert kept.min() >= dropped.max()
+
+
+def test_shrink_release_returns_the_last_page():
+    pool = og.PagePool(10)
+    table = [pool.alloc() for _ in range(4)]
+    new = og.shrink_release(table, pool)
+    assert new == table[:3] and pool.refcount[table[3]] == 0 and pool.free_count() == 7
+
+
+def test_hole_fill_by_hand():
+    # P = 2 pages of 4 slots: one hole in the first page, filled by the last
+    # page's only kept row
+    rows = np.arange(8.0)[:, None]
+    keep = np.array([1, 0, 1, 1, 0, 1, 0, 0], bool)
+    assert og.hole_fill_unit(rows, keep, 2, 4)[:, 0].tolist() == [0.0, 5.0, 2.0, 3.0]
+    # no hole: nothing moves
+    keep = np.array([1, 1, 1, 1, 0, 0, 0, 0], bool)
+    assert og.hole_fill_unit(rows, keep, 2, 4)[:, 0].tolist() == [0.0, 1.0, 2.0, 3.0]
