@@ -168,7 +168,7 @@ class Clocks:
 class Stream:
     """Config-2 decode stream driven through the C ABI."""
 
-    def __init__(self, device, num_pages=64, P=32):
+    def __init__(self, device, num_pages=64, P=32, fill=False):
         import paged_kv_cache_step_gb300 as gp
         self.gp = gp
         gp.load(build_if_missing=False)
@@ -199,6 +199,7 @@ class Stream:
         self.row_bytes = sh.head_dim * 2
         self.q_bytes = sh.num_layers * sh.num_q_heads * sh.head_dim * 2
         self.actions = {"grow": 0, "compress": 0, "fallback": 0}
+        self.fill = fill   # hole-fill compaction (order-destroying variant) instead of the stable one
 
     def _query(self):
         kind = (self.t // PHASE) % 2 == 0      # concentrated phases first
@@ -232,7 +233,10 @@ class Stream:
             gp.gp_grow_page(self.ctx, self.req)
             self.actions["grow"] += 1
         else:
-            gp.gp_compress_hold(self.ctx, [self.req])
+            if self.fill:
+                gp.gp_compress_fill(self.ctx, [self.req])
+            else:
+                gp.gp_compress_hold(self.ctx, [self.req])
             self.actions["compress"] += 1
             self.actions["fallback"] += int(act.fallback)
         return scan, act.kind
@@ -247,7 +251,7 @@ def run_gpu(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     peak, peak_src = _peaks()
-    s = Stream(device)
+    s = Stream(device, fill=args.compaction == "fill")
     # warm the summaries over the first boundary interval
     s.advance(EVENT_STRIDE - 1)
 
@@ -325,7 +329,7 @@ def run_gpu(args, world, rank, local):
     # back every step, inside the timed region
     e2e = None
     if not args.no_e2e:
-        s = Stream(device)
+        s = Stream(device, fill=args.compaction == "fill")
         s.advance(EVENT_STRIDE - 1)
         for _ in range(args.warmup):
             q = s._query()
@@ -366,7 +370,9 @@ def run_gpu(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": "llama8b_single: 1 request, 32L 32q/8kv d128 bf16, 32 pages x 256 "
                                "at the first boundary, 64-page pool, 512-step concentrated/diffuse "
-                               "query phases, boundary every 256 decode steps",
+                               "query phases, boundary every 256 decode steps"
+                               + ("; hole-fill compaction (order-destroying variant)" if args.compaction == "fill"
+                                  else ""),
                    "l2": "inputs larger than L2 (0.54+ GB of K scanned per event, 1.07 GB K/V)",
                    "parallelism": f"replicas x{world}"},
         "step_ms": [round(x, 4) for x in times],
@@ -662,6 +668,8 @@ def main():
     ap.add_argument("--workload", default="llama8b_single",
                     choices=["llama8b_single", "batch64", "qwen3_8b", "stream256"])
     ap.add_argument("--policy", default="growpage", choices=["growpage", "fixed"])
+    ap.add_argument("--compaction", default="stable", choices=["stable", "fill"],
+                    help="fill: the order-destroying hole-fill variant (reported separately)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = _dist()
