@@ -308,6 +308,25 @@ gp_status gp_compress_fill(gp_ctx* ctx, int32_t n, gp_request* reqs);
 gp_status gp_compact_kv(gp_ctx* ctx, int32_t n, gp_request* reqs,
                         const uint32_t* keep_masks_dev);
 
+/* ---- asynchronous compaction (App. E.3: compaction overlapped with decoding)
+ * gp_set_compaction_stream: from now on the compaction of gp_compress_hold,
+ * gp_shrink, gp_compress_fill and gp_compact_kv runs on `stream` (a caller
+ * CUDA stream; NULL: the engine stream again).  Each such call makes the
+ * side stream wait for the work the engine stream holds at that point, then
+ * returns without waiting for the compaction; the block tables and the page
+ * pool are updated on the host as before.  While it runs, gp_update_summaries
+ * (which touches no K/V) and the caller's work on other streams may
+ * overlap it; every later engine call that reads K/V or the engine's
+ * scratch (demand, compaction, inspection, gp_stats, gp_destroy) first
+ * waits for it on the host.  Before reading the compacted requests' K/V,
+ * the caller makes its own stream wait with gp_wait_compaction.  Waits for a
+ * pending compaction first. */
+gp_status gp_set_compaction_stream(gp_ctx* ctx, void* stream);
+/* gp_wait_compaction: `stream` (NULL: the engine stream) waits for the last
+ * compaction launched on the side stream (no-op if none ever was).  It
+ * enqueues the wait and returns at once. */
+gp_status gp_wait_compaction(gp_ctx* ctx, void* stream);
+
 /* ---- inspection (tests, benchmarks) ---------------------------------------
  * All of these synchronise the stream.  req_idx indexes the request list of
  * the last gp_boundary_demand (k, probabilities, scores) or of the last

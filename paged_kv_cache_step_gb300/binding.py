@@ -38,6 +38,7 @@ EXPORTS = [
     "gp_debug_demand_k",
     "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
     "gp_set_scan_kernel", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
+    "gp_set_compaction_stream", "gp_wait_compaction",
 ]
 
 
@@ -133,6 +134,8 @@ def load(build_if_missing: bool = True):
         "gp_kernel_time": (I32, [P, I32, C.POINTER(C.c_double), C.POINTER(I64)]),
         "gp_reset_timing": (I32, [P]),
         "gp_stats": (I32, [P, C.POINTER(GpStats)]),
+        "gp_set_compaction_stream": (I32, [P, P]),
+        "gp_wait_compaction": (I32, [P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -311,6 +314,20 @@ def gp_compress_fill(ctx, reqs):
     st = load().gp_compress_fill(ctx, len(reqs), arr)
     _unmarshal(arr, reqs)
     _check(ctx, st)
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        return None
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def gp_set_compaction_stream(ctx, stream):
+    _check(ctx, load().gp_set_compaction_stream(ctx, _stream_ptr(stream)))
+
+
+def gp_wait_compaction(ctx, stream=None):
+    _check(ctx, load().gp_wait_compaction(ctx, _stream_ptr(stream)))
 
 
 def gp_compact_kv(ctx, reqs, keep_masks_dev):

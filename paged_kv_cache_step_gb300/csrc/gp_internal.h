@@ -27,6 +27,9 @@ struct CtxView {
 bool ctx_view(const gp_ctx* c, CtxView* out);
 // True if `slot` is bound to a request.
 bool ctx_slot_bound(const gp_ctx* c, int slot);
+// Waits for a compaction still running on the side stream (see
+// gp_set_compaction_stream) before the caller reads K/V or engine scratch.
+gp_status ctx_join_compaction(gp_ctx* c);
 // Records the text returned by gp_last_error and returns `st`.
 gp_status ctx_fail(gp_ctx* c, gp_status st, const char* msg);
 

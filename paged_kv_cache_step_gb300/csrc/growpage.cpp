@@ -82,6 +82,11 @@ struct gp_ctx {
   void* pinned = nullptr;
   size_t pinned_cap = 0;
   cudaEvent_t pinned_free = nullptr;  // recorded after the last async use of `pinned`
+  // asynchronous compaction: a side stream, the event the side stream waits
+  // for (engine stream state), and the event of the last compaction there
+  cudaStream_t cstream = nullptr;
+  cudaEvent_t ev_ready = nullptr, ev_done = nullptr;
+  bool compaction_pending = false;
 
   std::vector<DemandRec> last_demand;
   std::vector<CompressRec> last_compress;
@@ -156,18 +161,35 @@ cudaEvent_t take_event(gp_ctx* c) {
 
 // Launch wrapper: brackets the launch with events when timing is on.
 template <typename F>
-gp_status timed_launch(gp_ctx* c, int kernel, const char* name, F&& launch) {
+gp_status timed_launch_on(gp_ctx* c, cudaStream_t s, int kernel, const char* name, F&& launch) {
   cudaEvent_t a = nullptr, b = nullptr;
   if (c->timing) {
     a = take_event(c);
     b = take_event(c);
-    cudaEventRecord(a, c->stream);
+    cudaEventRecord(a, s);
   }
   cudaError_t e = launch();
   if (e != cudaSuccess) return fail(c, GP_ERR_CUDA, "%s launch failed: %s", name, cudaGetErrorString(e));
   if (c->timing) {
-    cudaEventRecord(b, c->stream);
+    cudaEventRecord(b, s);
     c->timed.push_back({kernel, a, b});
+  }
+  return GP_OK;
+}
+
+template <typename F>
+gp_status timed_launch(gp_ctx* c, int kernel, const char* name, F&& launch) {
+  return timed_launch_on(c, c->stream, kernel, name, std::forward<F>(launch));
+}
+
+// Waits (host) for a compaction still running on the side stream: its K/V
+// writes, its reads of the engine's scratch (tables, importance, masks) and
+// its statistics must be done before the engine reuses, regrows or reads
+// any of them.
+gp_status join_compaction(gp_ctx* c) {
+  if (c->compaction_pending) {
+    GP_CUDA(c, cudaEventSynchronize(c->ev_done));
+    c->compaction_pending = false;
   }
   return GP_OK;
 }
@@ -349,7 +371,10 @@ gp_status gp_create(const gp_config* cfg, void* k_cache, void* v_cache, void* st
 gp_status gp_destroy(gp_ctx* c) {
   if (!c) return GP_ERR_INVALID;
   if (!c->host_only) {
+    join_compaction(c);
     cudaStreamSynchronize(c->stream);
+    if (c->ev_ready) cudaEventDestroy(c->ev_ready);
+    if (c->ev_done) cudaEventDestroy(c->ev_done);
     for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->bq, &c->scores, &c->aval, &c->tickets, &c->kout, &c->ksum,
                       &c->masks, &c->xstat})
       if (b->p) cudaFree(b->p);
@@ -514,6 +539,7 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
                              gp_demand* out) {
   gp_status st = need_device(c);
   if (st != GP_OK) return st;
+  if ((st = join_compaction(c)) != GP_OK) return st;
   if (n < 0 || n > c->cfg.max_slots) return fail(c, GP_ERR_INVALID, "n = %d outside [0, max_slots]", n);
   if (n == 0) return GP_OK;
   if (!reqs || !out || !q_cur_dev) return fail(c, GP_ERR_INVALID, "null argument");
@@ -796,6 +822,7 @@ namespace {
 gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t* keep_in, int drop, int fill = 0) {
   gp_status st = need_device(c);
   if (st != GP_OK) return st;
+  if ((st = join_compaction(c)) != GP_OK) return st;
   if (n < 0 || n > c->cfg.max_slots) return fail(c, GP_ERR_INVALID, "n = %d outside [0, max_slots]", n);
   if (n == 0) return GP_OK;
   if (!reqs) return fail(c, GP_ERR_INVALID, "null requests");
@@ -892,7 +919,18 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
   ca.n_work = n;
   ca.moved = c->moved_dev;
   ca.err = c->err_dev;
-  st = timed_launch(c, GP_KERNEL_COMPRESS, "compress_hold", [&] { return gp::launch_compress(ca, c->stream); });
+  // on the side stream (if any), after everything the engine stream holds
+  cudaStream_t ks = c->stream;
+  if (c->cstream) {
+    GP_CUDA(c, cudaEventRecord(c->ev_ready, c->stream));
+    GP_CUDA(c, cudaStreamWaitEvent(c->cstream, c->ev_ready, 0));
+    ks = c->cstream;
+  }
+  st = timed_launch_on(c, ks, GP_KERNEL_COMPRESS, "compress_hold", [&] { return gp::launch_compress(ca, ks); });
+  if (st == GP_OK && c->cstream) {
+    GP_CUDA(c, cudaEventRecord(c->ev_done, c->cstream));
+    c->compaction_pending = true;
+  }
   if (st != GP_OK) {
     // roll back the page allocations
     for (int r = 0; r < n; ++r)
@@ -942,6 +980,7 @@ gp_status gp_compact_kv(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t* 
 gp_status gp_debug_demand_k(gp_ctx* c, int32_t req_idx, int32_t* k_out) {
   gp_status st = need_device(c);
   if (st != GP_OK) return st;
+  if ((st = join_compaction(c)) != GP_OK) return st;
   if (!k_out || req_idx < 0 || req_idx >= (int)c->last_demand.size())
     return fail(c, GP_ERR_INVALID, "no demand result %d", req_idx);
   const int units = units_of(c);
@@ -954,6 +993,7 @@ gp_status gp_debug_demand_k(gp_ctx* c, int32_t req_idx, int32_t* k_out) {
 gp_status gp_debug_scores(gp_ctx* c, int32_t req_idx, float* out) {
   gp_status st = need_device(c);
   if (st != GP_OK) return st;
+  if ((st = join_compaction(c)) != GP_OK) return st;
   if (!out || req_idx < 0 || req_idx >= (int)c->last_demand.size())
     return fail(c, GP_ERR_INVALID, "no demand result %d", req_idx);
   const DemandRec& rec = c->last_demand[req_idx];
@@ -967,6 +1007,7 @@ gp_status gp_debug_scores(gp_ctx* c, int32_t req_idx, float* out) {
 gp_status gp_debug_probs(gp_ctx* c, int32_t req_idx, float* out) {
   gp_status st = need_device(c);
   if (st != GP_OK) return st;
+  if ((st = join_compaction(c)) != GP_OK) return st;
   if (!out || req_idx < 0 || req_idx >= (int)c->last_demand.size())
     return fail(c, GP_ERR_INVALID, "no demand result %d", req_idx);
   const DemandRec& rec = c->last_demand[req_idx];
@@ -981,6 +1022,7 @@ gp_status gp_debug_probs(gp_ctx* c, int32_t req_idx, float* out) {
 gp_status gp_debug_keep_mask(gp_ctx* c, int32_t req_idx, uint32_t* out) {
   gp_status st = need_device(c);
   if (st != GP_OK) return st;
+  if ((st = join_compaction(c)) != GP_OK) return st;
   if (!out || req_idx < 0 || req_idx >= (int)c->last_compress.size())
     return fail(c, GP_ERR_INVALID, "no compress result %d", req_idx);
   const CompressRec& rec = c->last_compress[req_idx];
@@ -1056,6 +1098,7 @@ gp_status gp_stats(const gp_ctx* c, gp_stats_t* out) {
   if (!c || !out) return GP_ERR_INVALID;
   *out = c->stats;
   if (!c->host_only) {
+    if (c->compaction_pending && cudaEventSynchronize(c->ev_done) != cudaSuccess) return GP_ERR_CUDA;
     unsigned long long moved = 0;
     if (cudaMemcpyAsync(&moved, c->moved_dev, sizeof(moved), cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
         cudaStreamSynchronize(c->stream) != cudaSuccess)
@@ -1066,11 +1109,34 @@ gp_status gp_stats(const gp_ctx* c, gp_stats_t* out) {
 }
 
 
+// ---- asynchronous compaction (side stream) ------------------------------------
+
+gp_status gp_set_compaction_stream(gp_ctx* c, void* stream) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if ((st = join_compaction(c)) != GP_OK) return st;
+  if (stream && (!c->ev_ready || !c->ev_done)) {
+    GP_CUDA(c, cudaEventCreateWithFlags(&c->ev_ready, cudaEventDisableTiming));
+    GP_CUDA(c, cudaEventCreateWithFlags(&c->ev_done, cudaEventDisableTiming));
+  }
+  c->cstream = static_cast<cudaStream_t>(stream);
+  return GP_OK;
+}
+
+gp_status gp_wait_compaction(gp_ctx* c, void* stream) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if (c->ev_done) GP_CUDA(c, cudaStreamWaitEvent(stream ? static_cast<cudaStream_t>(stream) : c->stream, c->ev_done, 0));
+  return GP_OK;
+}
+
 // ---- read-only view for other translation units (gp_internal.h) ------------
 
 #include "gp_internal.h"
 
 namespace gp {
+
+gp_status ctx_join_compaction(gp_ctx* c) { return c ? join_compaction(c) : GP_ERR_INVALID; }
 
 bool ctx_view(const gp_ctx* c, CtxView* out) {
   if (!c || !out) return false;

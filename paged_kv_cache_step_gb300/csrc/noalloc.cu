@@ -111,6 +111,12 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
     if (bad != GP_OK) return bad;
   }
 
+  {
+    // a compaction still running on a side stream writes K/V this call reads
+    const gp_status js = gp::ctx_join_compaction(c);
+    if (js != GP_OK) return js;
+  }
+
   // ---- scratch layout and its limit ------------------------------------------
   const int units = g.num_layers * g.num_kv_heads;
   const int G = g.num_q_heads / g.num_kv_heads;
