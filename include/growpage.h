@@ -308,6 +308,24 @@ gp_status gp_compress_fill(gp_ctx* ctx, int32_t n, gp_request* reqs);
 gp_status gp_compact_kv(gp_ctx* ctx, int32_t n, gp_request* reqs,
                         const uint32_t* keep_masks_dev);
 
+/* gp_decode_attention: one layer of a decode step -- attention over each
+ * request's paged cache with the summary update fused in, where the paper
+ * integrates it (Sec. 4.1: the decode attention kernel updates the query
+ * summaries in passing).  For request r and query head g (KV head g / G):
+ *   the summaries of (layer, slot, g) are updated from the PRE-RoPE query q
+ *   exactly as gp_update_summaries does (first_dev[r]: both set to q);
+ *   z_i = RoPE_pos(q) . k_i / sqrt(d) over the first num_tokens[r] logical
+ *   slots (keys are stored rotated, rotate-half at rope_theta), a =
+ *   softmax(z), out[r][g] = sum_i a_i v_i.
+ * q_dev: device [n][Hq][d] in q_dtype; first_dev: device uint8 [n];
+ * num_tokens: HOST int32 [n], 0 <= num_tokens[r] <= num_pages * 256 (0 gives
+ * a zero output); out_dev: device fp32 [n][Hq][d].  Requests need not be at
+ * a boundary.  Waits for a pending side-stream compaction.  Asynchronous on
+ * the engine stream. */
+gp_status gp_decode_attention(gp_ctx* ctx, int32_t layer, int32_t n, const gp_request* reqs,
+                              const int32_t* num_tokens, const void* q_dev, const uint8_t* first_dev,
+                              float* out_dev);
+
 /* ---- asynchronous compaction (App. E.3: compaction overlapped with decoding)
  * gp_set_compaction_stream: from now on the compaction of gp_compress_hold,
  * gp_shrink, gp_compress_fill and gp_compact_kv runs on `stream` (a caller
@@ -363,7 +381,8 @@ gp_status gp_set_scan_kernel(gp_ctx* ctx, int32_t kind);
 #define GP_KERNEL_PREP 1
 #define GP_KERNEL_DEMAND 2
 #define GP_KERNEL_COMPRESS 3
-#define GP_KERNEL_COUNT 4
+#define GP_KERNEL_ATTENTION 4
+#define GP_KERNEL_COUNT 5
 gp_status gp_set_timing(gp_ctx* ctx, int32_t enabled);
 gp_status gp_kernel_time(gp_ctx* ctx, int32_t kernel, double* ms, int64_t* launches);
 gp_status gp_reset_timing(gp_ctx* ctx);

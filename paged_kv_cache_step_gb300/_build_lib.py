@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgrowpage.so")
 
-SOURCES = ["growpage.cpp", "k_summaries.cu", "k_demand.cu", "k_demand_tc.cu", "k_compress.cu", "noalloc.cu"]
+SOURCES = ["growpage.cpp", "k_summaries.cu", "k_demand.cu", "k_demand_tc.cu", "k_compress.cu", "k_attention.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

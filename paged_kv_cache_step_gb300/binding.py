@@ -26,8 +26,9 @@ GP_DTYPE_BF16, GP_DTYPE_F32 = 0, 1
 GP_POLICY_GROWPAGE, GP_POLICY_FIXED, GP_POLICY_RANDOM, GP_POLICY_INVERSE, GP_POLICY_SHRINK = 0, 1, 2, 3, 4
 GP_ACT_GROW, GP_ACT_COMPRESS, GP_ACT_SHRINK = 0, 1, 2
 GP_SCAN_AUTO, GP_SCAN_CUDA_CORE, GP_SCAN_TENSOR_CORE = 0, 1, 2
-GP_KERNEL_EMA, GP_KERNEL_PREP, GP_KERNEL_DEMAND, GP_KERNEL_COMPRESS = 0, 1, 2, 3
-KERNEL_NAMES = {0: "ema_update", 1: "prep_queries", 2: "boundary_demand", 3: "compress_hold"}
+GP_KERNEL_EMA, GP_KERNEL_PREP, GP_KERNEL_DEMAND, GP_KERNEL_COMPRESS, GP_KERNEL_ATTENTION = 0, 1, 2, 3, 4
+KERNEL_NAMES = {0: "ema_update", 1: "prep_queries", 2: "boundary_demand", 3: "compress_hold",
+                4: "decode_attention"}
 
 EXPORTS = [
     "gp_config_default", "gp_create", "gp_destroy", "gp_last_error", "gp_status_string",
@@ -38,7 +39,7 @@ EXPORTS = [
     "gp_debug_demand_k",
     "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
     "gp_set_scan_kernel", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
-    "gp_set_compaction_stream", "gp_wait_compaction",
+    "gp_set_compaction_stream", "gp_wait_compaction", "gp_decode_attention",
 ]
 
 
@@ -136,6 +137,7 @@ def load(build_if_missing: bool = True):
         "gp_stats": (I32, [P, C.POINTER(GpStats)]),
         "gp_set_compaction_stream": (I32, [P, P]),
         "gp_wait_compaction": (I32, [P, P]),
+        "gp_decode_attention": (I32, [P, I32, I32, C.POINTER(GpRequest), P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -328,6 +330,15 @@ def gp_set_compaction_stream(ctx, stream):
 
 def gp_wait_compaction(ctx, stream=None):
     _check(ctx, load().gp_wait_compaction(ctx, _stream_ptr(stream)))
+
+
+def gp_decode_attention(ctx, layer: int, reqs, num_tokens, q_dev, first_dev, out_dev):
+    """One layer of decode attention with the summary update fused in.
+    num_tokens: host int32 per request; q_dev [n][Hq][d]; out_dev fp32 [n][Hq][d]."""
+    arr = _marshal(reqs)
+    nt = np.ascontiguousarray(np.asarray(num_tokens, dtype=np.int32))
+    _check(ctx, load().gp_decode_attention(ctx, layer, len(reqs), arr, nt.ctypes.data, _ptr(q_dev),
+                                           _ptr(first_dev), _ptr(out_dev)))
 
 
 def gp_compact_kv(ctx, reqs, keep_masks_dev):

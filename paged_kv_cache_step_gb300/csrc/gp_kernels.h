@@ -154,6 +154,30 @@ inline DemandPlan demand_plan(int P, bool tc_ok) {
   return pl;
 }
 
+// ---- decode attention with the summary update fused in (one layer) -------
+struct AttnArgs {
+  const void* k_cache;     // [L][num_pages][Hkv][b][D], keys stored rotated
+  const void* v_cache;
+  int kv_f32;
+  int num_pages_total;
+  int layer, Hq, Hkv, D, G, M;
+  const DevReq* reqs;      // [n] (num_pages, slot, pos, bt_off)
+  const int32_t* bt;       // packed block tables
+  const int32_t* ntok;     // [n] cached tokens attended to
+  const void* q;           // [n][Hq][D] pre-RoPE query of this layer
+  int q_f32;
+  const uint8_t* first;    // [n] 1: the slot's first step (summaries initialised)
+  double* pool;            // summary pool [L][M][2][Hq][D]
+  double beta_s, beta_l;
+  const double* inv_freq;  // [D/2]
+  float* out;              // [n][Hq][D]
+  float* part;             // split partials [n][Hkv][nsplit][G][D + 2]
+  unsigned* tickets;       // [n][Hkv], zero before the launch
+  int n, nsplit;
+  int* err;
+};
+cudaError_t launch_decode_attention(const AttnArgs& a, cudaStream_t s);
+
 // ---- A8-A10: window mask, Eq. 10 top-k, copy-on-write compaction -----------
 struct CompressArgs {
   void* k_cache;

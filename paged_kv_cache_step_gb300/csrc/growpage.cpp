@@ -74,7 +74,7 @@ struct gp_ctx {
   double* pool = nullptr;          // [L][M][2][Hq][D]
   int* err_dev = nullptr;          // kernel error bits
   unsigned long long* moved_dev = nullptr;
-  DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks, xstat;
+  DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks, xstat, attn;
   double* inv_freq = nullptr;      // [D/2] theta^(-2i/D) for RoPE
   CUtensorMap kmap;                // K cache as a 2-D bf16 tensor (tensor-core scan)
   bool tc_ok = false;              // kmap is valid
@@ -376,7 +376,7 @@ gp_status gp_destroy(gp_ctx* c) {
     if (c->ev_ready) cudaEventDestroy(c->ev_ready);
     if (c->ev_done) cudaEventDestroy(c->ev_done);
     for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->bq, &c->scores, &c->aval, &c->tickets, &c->kout, &c->ksum,
-                      &c->masks, &c->xstat})
+                      &c->masks, &c->xstat, &c->attn})
       if (b->p) cudaFree(b->p);
     if (c->inv_freq) cudaFree(c->inv_freq);
     if (c->pool) cudaFree(c->pool);
@@ -1108,6 +1108,84 @@ gp_status gp_stats(const gp_ctx* c, gp_stats_t* out) {
   return GP_OK;
 }
 
+
+// ---- decode attention with the summary update fused in --------------------------
+
+gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_request* reqs,
+                              const int32_t* num_tokens, const void* q_dev, const uint8_t* first_dev,
+                              float* out_dev) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  const gp_config& g = c->cfg;
+  if (layer < 0 || layer >= g.num_layers) return fail(c, GP_ERR_INVALID, "layer %d", layer);
+  if (n < 0 || n > g.max_slots) return fail(c, GP_ERR_INVALID, "n = %d outside [0, max_slots]", n);
+  if (n == 0) return GP_OK;
+  if (!reqs || !num_tokens || !q_dev || !first_dev || !out_dev) return fail(c, GP_ERR_INVALID, "null argument");
+  std::unordered_set<int32_t> slots;
+  for (int r = 0; r < n; ++r) {
+    if ((st = validate_request(c, reqs[r], r, true)) != GP_OK) return st;
+    if (!slots.insert(reqs[r].slot).second) return fail(c, GP_ERR_INVALID, "slot %d appears twice", reqs[r].slot);
+    if (num_tokens[r] < 0 || num_tokens[r] > reqs[r].num_pages * kPage)
+      return fail(c, GP_ERR_INVALID, "request %d: num_tokens %d outside [0, %d]", r, num_tokens[r],
+                  reqs[r].num_pages * kPage);
+  }
+  if ((st = join_compaction(c)) != GP_OK) return st;
+  const int G = g.num_q_heads / g.num_kv_heads;
+  const int maxp = g.max_pages_per_req;
+  // splits over pages: about four CTAs per SM over the whole call
+  int nsplit = (4 * 152 + n * g.num_kv_heads - 1) / (n * g.num_kv_heads);
+  nsplit = std::max(1, std::min(nsplit, 64));
+  const size_t part_floats = (size_t)n * g.num_kv_heads * nsplit * G * (g.head_dim + 2);
+  const size_t tick_off = (part_floats * sizeof(float) + 255) & ~size_t(255);
+  if ((st = ensure(c, c->attn, tick_off + sizeof(unsigned) * (size_t)n * g.num_kv_heads)) != GP_OK) return st;
+  Staged s{};
+  if ((st = stage(c, n, false, &s)) != GP_OK) return st;
+  for (int r = 0; r < n; ++r) {
+    gp::DevReq& d = s.reqs[r];
+    d.num_pages = reqs[r].num_pages;
+    d.slot = reqs[r].slot;
+    d.pos = reqs[r].pos;
+    d.score_off = 0;
+    d.aval_off = 0;
+    d.mask_off = 0;
+    d.bt_off = r * maxp;
+    d.pad = 0;
+    std::memcpy(s.bt + (size_t)r * maxp, reqs[r].block_table, sizeof(int32_t) * reqs[r].num_pages);
+    s.work[r] = num_tokens[r];  // the staged work array carries the token counts here
+  }
+  if ((st = upload(c, s)) != GP_OK) return st;
+  char* base = static_cast<char*>(c->attn.p);
+  GP_CUDA(c, cudaMemsetAsync(base + tick_off, 0, sizeof(unsigned) * (size_t)n * g.num_kv_heads, c->stream));
+  gp::AttnArgs a{};
+  a.k_cache = c->k_cache;
+  a.v_cache = c->v_cache;
+  a.kv_f32 = g.kv_dtype == GP_DTYPE_F32;
+  a.num_pages_total = g.num_pages;
+  a.layer = layer;
+  a.Hq = g.num_q_heads;
+  a.Hkv = g.num_kv_heads;
+  a.D = g.head_dim;
+  a.G = G;
+  a.M = g.max_slots;
+  a.reqs = dev_at<gp::DevReq>(c, 0);
+  a.bt = dev_at<int32_t>(c, s.off_bt);
+  a.ntok = dev_at<int32_t>(c, s.off_work);
+  a.q = q_dev;
+  a.q_f32 = g.q_dtype == GP_DTYPE_F32;
+  a.first = first_dev;
+  a.pool = c->pool;
+  a.beta_s = g.beta_s;
+  a.beta_l = g.beta_l;
+  a.inv_freq = c->inv_freq;
+  a.out = out_dev;
+  a.part = reinterpret_cast<float*>(base);
+  a.tickets = reinterpret_cast<unsigned*>(base + tick_off);
+  a.n = n;
+  a.nsplit = nsplit;
+  a.err = c->err_dev;
+  return timed_launch(c, GP_KERNEL_ATTENTION, "decode_attention",
+                      [&] { return gp::launch_decode_attention(a, c->stream); });
+}
 
 // ---- asynchronous compaction (side stream) ------------------------------------
 
