@@ -544,6 +544,7 @@ def run_batch(args, device):
     gp.gp_set_timing(ctx, 0)
     comp_bytes = (gp.gp_stats(ctx)["moved_rows"] - moved0) * row * 4
     kern, rl, dom = _kernel_report(gp, ctx, peak, scan_bytes, comp_bytes)
+    attn = measure_attention(gp, ctx, w, reqs, ts, peak, args) if args.decode_attention else None
     gp.gp_destroy(ctx)
     total = sum(times)
     launches = sum(k["launches"] for k in kern.values())
@@ -557,7 +558,41 @@ def run_batch(args, device):
         "kv_gbs": (scan_bytes + comp_bytes) / (total / 1e3) / 1e9,
         "scan_bytes": scan_bytes, "compaction_bytes": comp_bytes, "compress_events": ncomp,
         "roofline": dict(rl[dom], kernel=dom, peak_source=peak_src, traffic=None) if dom else None,
-        "kernels": kern, "gpu_launches": launches, "clocks": clk}
+        "kernels": kern, "gpu_launches": launches, "clocks": clk,
+        **({"decode_attention": attn} if attn else {})}
+
+
+def measure_attention(gp, ctx, w, reqs, ts, peak, args):
+    """One decode step of attention over every request's whole cache: the
+    L layer calls of gp_decode_attention (summary update fused in).
+    Algorithmic bytes per layer: K and V of every attended token."""
+    sh = w.shape
+    n = len(reqs)
+    ntok = [r.num_pages * PAGE for r in reqs]
+    device = w.device
+    q = torch.randn(sh.num_layers, n, sh.num_q_heads, sh.head_dim, device=device).to(torch.bfloat16)
+    first = torch.zeros(n, dtype=torch.uint8, device=device)
+    out = torch.empty(n, sh.num_q_heads, sh.head_dim, device=device)
+    torch.cuda.synchronize()
+    row = sh.head_dim * 2
+    step_bytes = sum(ntok) * sh.num_kv_heads * row * 2 * sh.num_layers
+    for _ in range(2):
+        for layer in range(sh.num_layers):
+            gp.gp_decode_attention(ctx, layer, reqs, ntok, q[layer], first, out)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(max(3, args.steps)):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(ts)   # the engine's stream, which the launches go to
+        for layer in range(sh.num_layers):
+            gp.gp_decode_attention(ctx, layer, reqs, ntok, q[layer], first, out)
+        ev1.record(ts)
+        torch.cuda.synchronize()
+        times.append(ev0.elapsed_time(ev1))
+    ms = sum(times) / len(times)
+    a = step_bytes / (ms / 1e3) / 1e9
+    return {"ms_per_decode_step": ms, "bytes_per_step": step_bytes, "achieved_gbs": a, "peak": peak,
+            "frac": a / peak, "layers": sh.num_layers, "requests": n}
 
 
 def run_stream(args, device):
@@ -720,6 +755,8 @@ def main():
     ap.add_argument("--workload", default="llama8b_single",
                     choices=["llama8b_single", "batch64", "qwen3_8b", "stream256"])
     ap.add_argument("--policy", default="growpage", choices=["growpage", "fixed"])
+    ap.add_argument("--decode-attention", action="store_true",
+                    help="batch workloads: also time a decode step of attention over every cache")
     ap.add_argument("--async-overlap", action="store_true",
                     help="also time compaction on a side stream overlapped with decode steps")
     ap.add_argument("--overlap-intervals", type=int, default=8)

@@ -382,7 +382,8 @@ gp_status gp_set_scan_kernel(gp_ctx* ctx, int32_t kind);
 #define GP_KERNEL_DEMAND 2
 #define GP_KERNEL_COMPRESS 3
 #define GP_KERNEL_ATTENTION 4
-#define GP_KERNEL_COUNT 5
+#define GP_KERNEL_SELECT 5
+#define GP_KERNEL_COUNT 6
 gp_status gp_set_timing(gp_ctx* ctx, int32_t enabled);
 gp_status gp_kernel_time(gp_ctx* ctx, int32_t kernel, double* ms, int64_t* launches);
 gp_status gp_reset_timing(gp_ctx* ctx);

@@ -27,8 +27,9 @@ GP_POLICY_GROWPAGE, GP_POLICY_FIXED, GP_POLICY_RANDOM, GP_POLICY_INVERSE, GP_POL
 GP_ACT_GROW, GP_ACT_COMPRESS, GP_ACT_SHRINK = 0, 1, 2
 GP_SCAN_AUTO, GP_SCAN_CUDA_CORE, GP_SCAN_TENSOR_CORE = 0, 1, 2
 GP_KERNEL_EMA, GP_KERNEL_PREP, GP_KERNEL_DEMAND, GP_KERNEL_COMPRESS, GP_KERNEL_ATTENTION = 0, 1, 2, 3, 4
+GP_KERNEL_SELECT = 5
 KERNEL_NAMES = {0: "ema_update", 1: "prep_queries", 2: "boundary_demand", 3: "compress_hold",
-                4: "decode_attention"}
+                4: "decode_attention", 5: "select"}
 
 EXPORTS = [
     "gp_config_default", "gp_create", "gp_destroy", "gp_last_error", "gp_status_string",

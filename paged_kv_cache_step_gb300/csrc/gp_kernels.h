@@ -187,6 +187,7 @@ struct CompressArgs {
   int b, R, k_loc;
   int drop;                // pages' worth of history dropped: 1 Compress & Hold, 2 Shrink
   int fill;                // 1: hole-fill compaction (order-destroying), 0: stable
+  int select_only;         // 1: write the keep masks (keep_out) and stop before the compaction
   const DevReq* reqs;
   const int32_t* old_bt;
   const int32_t* new_bt;

@@ -40,9 +40,11 @@ struct DemandRec {
   uint64_t gen = 0;
   int64_t score_off = 0;
   int64_t aval_off = 0;
+  int64_t spec_off = -1;  // word offset of its speculative keep masks, -1 if none
 };
 
 struct CompressRec {
+  bool spec = false;      // masks in the speculative buffer (at mask_off), else in `masks`
   int32_t num_pages = 0;
   int64_t mask_off = 0;
 };
@@ -74,7 +76,12 @@ struct gp_ctx {
   double* pool = nullptr;          // [L][M][2][Hq][D]
   int* err_dev = nullptr;          // kernel error bits
   unsigned long long* moved_dev = nullptr;
-  DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks, xstat, attn;
+  DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks, xstat, attn, spec_masks;
+  // speculative selection: the Eq. 10 keep masks of every request of the last
+  // demand call, computed on an engine-owned stream while the host decides
+  cudaStream_t sel_stream = nullptr;
+  cudaEvent_t ev_dem = nullptr, ev_sel = nullptr;
+  bool sel_pending = false;
   double* inv_freq = nullptr;      // [D/2] theta^(-2i/D) for RoPE
   CUtensorMap kmap;                // K cache as a 2-D bf16 tensor (tensor-core scan)
   bool tc_ok = false;              // kmap is valid
@@ -180,6 +187,17 @@ gp_status timed_launch_on(gp_ctx* c, cudaStream_t s, int kernel, const char* nam
 template <typename F>
 gp_status timed_launch(gp_ctx* c, int kernel, const char* name, F&& launch) {
   return timed_launch_on(c, c->stream, kernel, name, std::forward<F>(launch));
+}
+
+// Waits (host) for a speculative selection still running: it reads the
+// importance cache and writes the speculative masks, which the next demand
+// call rewrites.
+gp_status join_select(gp_ctx* c) {
+  if (c->sel_pending) {
+    GP_CUDA(c, cudaEventSynchronize(c->ev_sel));
+    c->sel_pending = false;
+  }
+  return GP_OK;
 }
 
 // Waits (host) for a compaction still running on the side stream: its K/V
@@ -350,6 +368,9 @@ gp_status gp_create(const gp_config* cfg, void* k_cache, void* v_cache, void* st
     if (e == cudaSuccess) e = cudaMalloc((void**)&c->err_dev, 64);
     if (e == cudaSuccess) e = cudaMemsetAsync(c->err_dev, 0, 64, c->stream);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pinned_free, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->sel_stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_dem, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_sel, cudaEventDisableTiming);
     // RoPE inverse frequencies theta^(-2i/d), computed once in fp64
     std::vector<double> inv(g.head_dim / 2);
     for (int i = 0; i < g.head_dim / 2; ++i) inv[i] = std::pow(g.rope_theta, -2.0 * i / g.head_dim);
@@ -373,10 +394,16 @@ gp_status gp_destroy(gp_ctx* c) {
   if (!c->host_only) {
     join_compaction(c);
     cudaStreamSynchronize(c->stream);
+    if (c->sel_stream) {
+      cudaStreamSynchronize(c->sel_stream);
+      cudaStreamDestroy(c->sel_stream);
+    }
+    if (c->ev_dem) cudaEventDestroy(c->ev_dem);
+    if (c->ev_sel) cudaEventDestroy(c->ev_sel);
     if (c->ev_ready) cudaEventDestroy(c->ev_ready);
     if (c->ev_done) cudaEventDestroy(c->ev_done);
     for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->bq, &c->scores, &c->aval, &c->tickets, &c->kout, &c->ksum,
-                      &c->masks, &c->xstat, &c->attn})
+                      &c->masks, &c->xstat, &c->attn, &c->spec_masks})
       if (b->p) cudaFree(b->p);
     if (c->inv_freq) cudaFree(c->inv_freq);
     if (c->pool) cudaFree(c->pool);
@@ -493,8 +520,9 @@ struct Staged {
   int32_t* bt_new;
   int32_t* work;
   int32_t* part_base;
+  int32_t* sel;  // requests of a demand call that get a speculative selection
   size_t bytes;
-  size_t off_bt, off_bt_new, off_work, off_pb;
+  size_t off_bt, off_bt_new, off_work, off_pb, off_sel;
 };
 
 // Pinned layout [DevReq n][bt n*maxP][bt_new n*maxP][work n][part_base n+1],
@@ -508,6 +536,7 @@ gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s) {
   s->off_bt_new = with_new ? take(sizeof(int32_t) * (size_t)n * maxp) : s->off_bt;
   s->off_work = take(sizeof(int32_t) * n);
   s->off_pb = take(sizeof(int32_t) * (n + 1));
+  s->off_sel = take(sizeof(int32_t) * n);
   s->bytes = o;
   gp_status st = ensure_pinned(c, o);
   if (st != GP_OK) return st;
@@ -519,6 +548,7 @@ gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s) {
   s->bt_new = reinterpret_cast<int32_t*>(p + s->off_bt_new);
   s->work = reinterpret_cast<int32_t*>(p + s->off_work);
   s->part_base = reinterpret_cast<int32_t*>(p + s->off_pb);
+  s->sel = reinterpret_cast<int32_t*>(p + s->off_sel);
   return GP_OK;
 }
 
@@ -540,6 +570,7 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   gp_status st = need_device(c);
   if (st != GP_OK) return st;
   if ((st = join_compaction(c)) != GP_OK) return st;
+  if ((st = join_select(c)) != GP_OK) return st;
   if (n < 0 || n > c->cfg.max_slots) return fail(c, GP_ERR_INVALID, "n = %d outside [0, max_slots]", n);
   if (n == 0) return GP_OK;
   if (!reqs || !out || !q_cur_dev) return fail(c, GP_ERR_INVALID, "null argument");
@@ -566,6 +597,16 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     aval_off[r] = aval_total;
     aval_total += (int64_t)units * 2 * (P - 1) * kPage;
   }
+  // speculative keep masks: every request that Compress & Hold could take
+  std::vector<int64_t> spec_off(n, -1);
+  int64_t spec_total = 0;
+  for (int r = 0; r < n; ++r) {
+    if (reqs[r].num_pages < 2) continue;
+    spec_off[r] = spec_total;
+    spec_total += (int64_t)units * (reqs[r].num_pages * kPage / 32);
+  }
+  if ((st = ensure(c, c->spec_masks, sizeof(uint32_t) * (size_t)std::max<int64_t>(spec_total, 1))) != GP_OK)
+    return st;
   Staged s{};
   st = stage(c, n, false, &s);
   if (st != GP_OK) return st;
@@ -606,7 +647,7 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     d.pos = reqs[r].pos;
     d.score_off = score_off[r];
     d.aval_off = aval_off[r];
-    d.mask_off = 0;
+    d.mask_off = std::max<int64_t>(spec_off[r], 0);
     d.bt_off = r * maxp;
     d.pad = 0;
     std::memcpy(s.bt + (size_t)r * maxp, reqs[r].block_table, sizeof(int32_t) * reqs[r].num_pages);
@@ -630,6 +671,9 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     launches.push_back({gp::DEMAND_FFMA, it->first, bucket_ppc[it->first], wpos, (int)it->second.size()});
     for (int32_t r : it->second) s.work[wpos++] = r;
   }
+  int n_sel = 0;
+  for (int r = 0; r < n; ++r)
+    if (spec_off[r] >= 0) s.sel[n_sel++] = r;
   if ((st = upload(c, s)) != GP_OK) return st;
 
   gp::PrepArgs pa{};
@@ -689,6 +733,43 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     st = timed_launch(c, GP_KERNEL_DEMAND, "boundary_demand", [&] { return gp::launch_demand(da, c->stream); });
     if (st != GP_OK) return st;
   }
+  // Speculative selection: the Eq. 10 keep masks of every request that could
+  // be compressed, on the engine's selection stream, while the host reads
+  // the sums and decides.  A Compress & Hold of these requests then only
+  // moves rows.
+  if (n_sel > 0) {
+    GP_CUDA(c, cudaEventRecord(c->ev_dem, c->stream));
+    GP_CUDA(c, cudaStreamWaitEvent(c->sel_stream, c->ev_dem, 0));
+    gp::CompressArgs ca{};
+    ca.k_cache = c->k_cache;
+    ca.v_cache = c->v_cache;
+    ca.num_pages_total = g.num_pages;
+    ca.L = g.num_layers;
+    ca.Hkv = g.num_kv_heads;
+    ca.D = g.head_dim;
+    ca.elt = elt_bytes(g.kv_dtype);
+    ca.b = kPage;
+    ca.R = g.recent_window;
+    ca.k_loc = g.k_loc;
+    ca.drop = 1;
+    ca.fill = 0;
+    ca.select_only = 1;
+    ca.reqs = pa.reqs;
+    ca.old_bt = dev_at<int32_t>(c, s.off_bt);
+    ca.new_bt = ca.old_bt;
+    ca.scores = static_cast<const float*>(c->scores.p);
+    ca.keep_in = nullptr;
+    ca.keep_out = static_cast<uint32_t*>(c->spec_masks.p);
+    ca.work = dev_at<int32_t>(c, s.off_sel);
+    ca.n_work = n_sel;
+    ca.moved = c->moved_dev;
+    ca.err = c->err_dev;
+    st = timed_launch_on(c, c->sel_stream, GP_KERNEL_SELECT, "select",
+                         [&] { return gp::launch_compress(ca, c->sel_stream); });
+    if (st != GP_OK) return st;
+    GP_CUDA(c, cudaEventRecord(c->ev_sel, c->sel_stream));
+    c->sel_pending = true;
+  }
   std::vector<unsigned long long> sums((size_t)n * 2);
   GP_CUDA(c, cudaMemcpyAsync(sums.data(), c->ksum.p, sizeof(unsigned long long) * sums.size(),
                              cudaMemcpyDeviceToHost, c->stream));
@@ -713,6 +794,7 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     rec.gen = c->slot_gen[reqs[r].slot];
     rec.score_off = score_off[r];
     rec.aval_off = aval_off[r];
+    rec.spec_off = spec_off[r];
   }
   c->stats.demand_calls += 1;
   c->stats.demand_requests += n;
@@ -823,13 +905,15 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
   gp_status st = need_device(c);
   if (st != GP_OK) return st;
   if ((st = join_compaction(c)) != GP_OK) return st;
+  // the speculative selection reads the upload buffer this call rewrites
+  if ((st = join_select(c)) != GP_OK) return st;
   if (n < 0 || n > c->cfg.max_slots) return fail(c, GP_ERR_INVALID, "n = %d outside [0, max_slots]", n);
   if (n == 0) return GP_OK;
   if (!reqs) return fail(c, GP_ERR_INVALID, "null requests");
   const gp_config& g = c->cfg;
   const int units = units_of(c);
   const int maxp = g.max_pages_per_req;
-  std::vector<int64_t> score_off(n, 0);
+  std::vector<int64_t> score_off(n, 0), spec_off(n, -1);
   std::unordered_set<int32_t> slots;
   for (int r = 0; r < n; ++r) {
     st = validate_request(c, reqs[r], r, keep_in == nullptr);
@@ -848,8 +932,13 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
         return fail(c, GP_ERR_STATE,
                     "request %d: no gp_boundary_demand result for its current pages (call it first)", r);
       score_off[r] = rec->score_off;
+      spec_off[r] = rec->spec_off;
     }
   }
+  // the speculative keep masks of the last demand call serve Compress & Hold
+  // (stable or hole fill) when every request has them; Shrink selects anew
+  bool spec = keep_in == nullptr && drop == 1;
+  for (int r = 0; r < n && spec; ++r) spec = spec_off[r] >= 0;
   // copy-on-write plan (App. E.2): every shared page gets a fresh target page
   size_t need = 0;
   for (int r = 0; r < n; ++r)
@@ -879,7 +968,7 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
     d.pos = reqs[r].pos;
     d.score_off = score_off[r];
     d.aval_off = 0;
-    d.mask_off = mask_off[r];
+    d.mask_off = spec ? spec_off[r] : mask_off[r];
     d.bt_off = r * maxp;
     d.pad = 0;
     for (int j = 0; j < P; ++j) {
@@ -913,8 +1002,8 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
   ca.old_bt = dev_at<int32_t>(c, s.off_bt);
   ca.new_bt = dev_at<int32_t>(c, s.off_bt_new);
   ca.scores = static_cast<const float*>(c->scores.p);
-  ca.keep_in = keep_in;
-  ca.keep_out = static_cast<uint32_t*>(c->masks.p);
+  ca.keep_in = spec ? static_cast<const uint32_t*>(c->spec_masks.p) : keep_in;
+  ca.keep_out = spec ? nullptr : static_cast<uint32_t*>(c->masks.p);
   ca.work = dev_at<int32_t>(c, s.off_work);
   ca.n_work = n;
   ca.moved = c->moved_dev;
@@ -926,6 +1015,7 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
     GP_CUDA(c, cudaStreamWaitEvent(c->cstream, c->ev_ready, 0));
     ks = c->cstream;
   }
+  if (spec) GP_CUDA(c, cudaStreamWaitEvent(ks, c->ev_sel, 0));  // the speculative masks are written (joined above)
   st = timed_launch_on(c, ks, GP_KERNEL_COMPRESS, "compress_hold", [&] { return gp::launch_compress(ca, ks); });
   if (st == GP_OK && c->cstream) {
     GP_CUDA(c, cudaEventRecord(c->ev_done, c->cstream));
@@ -954,7 +1044,8 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
     }
     if (reqs[r].slot >= 0 && reqs[r].slot < g.max_slots) ++c->slot_gen[reqs[r].slot];
     c->last_compress[r].num_pages = P;
-    c->last_compress[r].mask_off = mask_off[r];
+    c->last_compress[r].mask_off = spec ? spec_off[r] : mask_off[r];
+    c->last_compress[r].spec = spec;
   }
   return GP_OK;
 }
@@ -1027,8 +1118,8 @@ gp_status gp_debug_keep_mask(gp_ctx* c, int32_t req_idx, uint32_t* out) {
     return fail(c, GP_ERR_INVALID, "no compress result %d", req_idx);
   const CompressRec& rec = c->last_compress[req_idx];
   const size_t count = (size_t)units_of(c) * (rec.num_pages * kPage / 32);
-  GP_CUDA(c, cudaMemcpyAsync(out, static_cast<uint32_t*>(c->masks.p) + rec.mask_off, sizeof(uint32_t) * count,
-                             cudaMemcpyDeviceToHost, c->stream));
+  const uint32_t* src = static_cast<const uint32_t*>(rec.spec ? c->spec_masks.p : c->masks.p);
+  GP_CUDA(c, cudaMemcpyAsync(out, src + rec.mask_off, sizeof(uint32_t) * count, cudaMemcpyDeviceToHost, c->stream));
   return check_kernel_errors(c);
 }
 
@@ -1130,6 +1221,7 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
                   reqs[r].num_pages * kPage);
   }
   if ((st = join_compaction(c)) != GP_OK) return st;
+  if ((st = join_select(c)) != GP_OK) return st;  // it reads the upload buffer this call rewrites
   const int G = g.num_q_heads / g.num_kv_heads;
   const int maxp = g.max_pages_per_req;
   // splits over pages: about four CTAs per SM over the whole call

@@ -404,6 +404,7 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
     __syncthreads();
     return;
   }
+  if (a.select_only) return;  // the keep masks were all that was asked for
 
   // ---- compaction ---------------------------------------------------------
   word_prefix(keep, pre, words, red);
