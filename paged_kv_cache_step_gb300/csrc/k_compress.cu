@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
   __shared__ unsigned red[NWARP];
   __shared__ int s_old[PAGE], s_new[PAGE];
   __shared__ int s_hole[PAGE];            // hole-fill mode: the holes in order
+  __shared__ int s_fast;                  // the selection's fast path applied
   __shared__ int s_nholes;
   __shared__ unsigned s_sel[4];           // prefix, mask, above, flags
   __shared__ int s_abort;
@@ -214,166 +215,199 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
     }
     for (int w = tid; w < words; w += NT) loc[w] = 0u;
     __syncthreads();
-    // ---- Eq. 10, block-local part: TopK_{k_loc'}(B_j) per logical block ----
-    const int quota = min(a.k_loc, kt / P);
-    // Bit-serial radix select of each block's kj-th largest key: at each bit
-    // the keys that match the prefix and have the bit set are counted with
-    // warp ballots.  A warp takes GB blocks at once, so their
-    // independent reduction chains overlap.  Afterwards prefix = that key
-    // and above = the number of keys above it.
-    constexpr int GB = 4;
-    for (int j0 = warp; j0 < P; j0 += NWARP * GB) {
-      unsigned key[GB][8], prefix[GB], above[GB], need[GB];
-      bool val[GB][8];
-      int kjv[GB];
-#pragma unroll
-      for (int g = 0; g < GB; ++g) {
-        const int j = j0 + g * NWARP;
-        const int lo = j * PAGE;
-        const int hi = min(lo + PAGE, ncmp);
-        kjv[g] = j < P ? max(0, min(quota, hi - lo)) : 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int s = lo + 32 * e + lane;
-          val[g][e] = j < P && s < hi;
-          key[g][e] = val[g][e] ? okey(sc[s]) : 0u;
-        }
-        prefix[g] = 0u;
-        above[g] = 0u;
-        need[g] = (unsigned)kjv[g];
-      }
-      unsigned mask = 0u;
-      for (int bit = 31; bit >= 0; --bit) {
-        const unsigned m2 = mask | (1u << bit);
-        unsigned tot[GB];
-#pragma unroll
-        for (int g = 0; g < GB; ++g) {
-          const unsigned p2 = prefix[g] | (1u << bit);
-          unsigned c = 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            c += (unsigned)__popc(__ballot_sync(0xffffffffu, val[g][e] && (key[g][e] & m2) == p2));
-          tot[g] = c;
-        }
-#pragma unroll
-        for (int g = 0; g < GB; ++g) {
-          if (tot[g] >= need[g]) {
-            prefix[g] |= 1u << bit;
-          } else {
-            need[g] -= tot[g];
-            above[g] += tot[g];
+    // ---- Eq. 10, global part: TopK_{K_t - |S_loc|}(C \ S_loc), then the keep words
+    auto global_keep = [&]() {
+      unsigned nloc = 0;
+      for (int w = tid; w < words; w += NT) nloc += __popc(loc[w]);
+  #pragma unroll
+      for (int o = 16; o > 0; o >>= 1) nloc += __shfl_xor_sync(0xffffffffu, nloc, o);
+      if (lane == 0) red[warp] = nloc;
+      if (tid == 0) { s_sel[0] = 0; s_sel[1] = 0; s_sel[2] = 0; s_sel[3] = 0; }
+      __syncthreads();
+      unsigned tot_loc = 0;
+      for (int w = 0; w < NWARP; ++w) tot_loc += red[w];
+      const int need_g = kt - (int)tot_loc;
+      const int iters = (ncmp + NT - 1) / NT;
+      // radix select (8-bit digits) of the need_g-th largest key among the
+      // candidates outside S_loc
+      unsigned* hist = whist[0];
+      if (need_g > 0) {
+        for (int ro = 0; ro < 4; ++ro) {
+          const int shift = 24 - 8 * ro;
+          hist[tid] = 0u;
+          __syncthreads();
+          const unsigned prefix = s_sel[0], mask = s_sel[1];
+          for (int it0 = 0; it0 < iters; it0 += 8) {
+            // eight independent loads in flight, then their histogram updates
+            unsigned kb[8];
+            bool vb[8];
+  #pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int s = tid + (it0 + j) * NT;
+              vb[j] = it0 + j < iters && s < ncmp;
+              kb[j] = 0u;
+              if (vb[j]) {
+                vb[j] = !((loc[s >> 5] >> (s & 31)) & 1u);
+                kb[j] = okey(sc[s]);
+                vb[j] = vb[j] && ((kb[j] & mask) == prefix);
+              }
+            }
+  #pragma unroll
+            for (int j = 0; j < 8; ++j) warp_inc(hist, (kb[j] >> shift) & 255u, vb[j]);
           }
-        }
-        mask = m2;
-      }
-#pragma unroll
-      for (int g = 0; g < GB; ++g) {
-        if (kjv[g] <= 0) continue;
-        const int lo = (j0 + g * NWARP) * PAGE;
-        const unsigned need_eq = (unsigned)kjv[g] - above[g];
-        unsigned run = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const bool gt = val[g][e] && key[g][e] > prefix[g];
-          const bool eq = val[g][e] && key[g][e] == prefix[g];
-          const unsigned be = __ballot_sync(0xffffffffu, eq);
-          const unsigned rank = run + __popc(be & ((1u << lane) - 1u));
-          run += __popc(be);
-          const unsigned bw = __ballot_sync(0xffffffffu, gt || (eq && rank < need_eq));
-          if (lane == 0) loc[(lo >> 5) + e] = bw;
-        }
-      }
-    }
-    __syncthreads();
-    // ---- Eq. 10, global part: TopK_{K_t - |S_loc|}(C \ S_loc) ----------------
-    unsigned nloc = 0;
-    for (int w = tid; w < words; w += NT) nloc += __popc(loc[w]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nloc += __shfl_xor_sync(0xffffffffu, nloc, o);
-    if (lane == 0) red[warp] = nloc;
-    if (tid == 0) { s_sel[0] = 0; s_sel[1] = 0; s_sel[2] = 0; s_sel[3] = 0; }
-    __syncthreads();
-    unsigned tot_loc = 0;
-    for (int w = 0; w < NWARP; ++w) tot_loc += red[w];
-    const int need_g = kt - (int)tot_loc;
-    const int iters = (ncmp + NT - 1) / NT;
-    // radix select (8-bit digits) of the need_g-th largest key among the
-    // candidates outside S_loc
-    unsigned* hist = whist[0];
-    if (need_g > 0) {
-      for (int ro = 0; ro < 4; ++ro) {
-        const int shift = 24 - 8 * ro;
-        hist[tid] = 0u;
-        __syncthreads();
-        const unsigned prefix = s_sel[0], mask = s_sel[1];
-        for (int it0 = 0; it0 < iters; it0 += 8) {
-          // eight independent loads in flight, then their histogram updates
-          unsigned kb[8];
-          bool vb[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int s = tid + (it0 + j) * NT;
-            vb[j] = it0 + j < iters && s < ncmp;
-            kb[j] = 0u;
-            if (vb[j]) {
-              vb[j] = !((loc[s >> 5] >> (s & 31)) & 1u);
-              kb[j] = okey(sc[s]);
-              vb[j] = vb[j] && ((kb[j] & mask) == prefix);
+          __syncthreads();
+          if (warp == 0) {
+            unsigned bin, ab;
+            bool ok;
+            find_bin(hist, (unsigned)need_g - s_sel[2], bin, ab, ok);
+            if (lane == 0) {
+              if (!ok) atomicOr(a.err, ERR_BAD_COUNT);
+              s_sel[0] |= bin << shift;
+              s_sel[1] |= 255u << shift;
+              s_sel[2] += ab;
+              if (ro == 3) s_sel[3] = hist[bin];
             }
           }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) warp_inc(hist, (kb[j] >> shift) & 255u, vb[j]);
+          __syncthreads();
         }
-        __syncthreads();
-        if (warp == 0) {
-          unsigned bin, ab;
-          bool ok;
-          find_bin(hist, (unsigned)need_g - s_sel[2], bin, ab, ok);
-          if (lane == 0) {
-            if (!ok) atomicOr(a.err, ERR_BAD_COUNT);
-            s_sel[0] |= bin << shift;
-            s_sel[1] |= 255u << shift;
-            s_sel[2] += ab;
-            if (ro == 3) s_sel[3] = hist[bin];
-          }
-        }
-        __syncthreads();
       }
-    }
-    const unsigned T = s_sel[0];
-    const unsigned need_eq = need_g > 0 ? (unsigned)need_g - s_sel[2] : 0u;
-    const bool all_ties = need_g > 0 && s_sel[3] == need_eq;
-    const bool rank_ties = need_g > 0 && !all_ties;
-    // ties at T beyond need_eq are ranked in slot order (lower slot first):
-    // tie bits per word, then their exclusive prefix counts
-    if (rank_ties) {
+      const unsigned T = s_sel[0];
+      const unsigned need_eq = need_g > 0 ? (unsigned)need_g - s_sel[2] : 0u;
+      const bool all_ties = need_g > 0 && s_sel[3] == need_eq;
+      const bool rank_ties = need_g > 0 && !all_ties;
+      // ties at T beyond need_eq are ranked in slot order (lower slot first):
+      // tie bits per word, then their exclusive prefix counts
+      if (rank_ties) {
+        for (int w = warp; w < words; w += NWARP) {
+          const int s = w * 32 + lane;
+          bool eq = false;
+          if (s < ncmp && !((loc[w] >> lane) & 1u)) eq = okey(sc[s]) == T;
+          const unsigned b = __ballot_sync(0xffffffffu, eq);
+          if (lane == 0) tmp[w] = b;
+        }
+        __syncthreads();
+        word_prefix(tmp, pre, words, red);
+      }
+      // final keep words: local picks | global picks | recent window
       for (int w = warp; w < words; w += NWARP) {
         const int s = w * 32 + lane;
-        bool eq = false;
-        if (s < ncmp && !((loc[w] >> lane) & 1u)) eq = okey(sc[s]) == T;
-        const unsigned b = __ballot_sync(0xffffffffu, eq);
-        if (lane == 0) tmp[w] = b;
+        bool kp = (loc[w] >> lane) & 1u;
+        if (!kp && s < ncmp && need_g > 0) {
+          const unsigned k = okey(sc[s]);
+          if (k > T) {
+            kp = true;
+          } else if (k == T) {
+            kp = all_ties || (pre[w] + __popc(tmp[w] & ((1u << lane) - 1u))) < need_eq;
+          }
+        }
+        if (s >= ncmp) kp = true;
+        const unsigned b = __ballot_sync(0xffffffffu, kp);
+        if (lane == 0) keep[w] = b;
       }
       __syncthreads();
-      word_prefix(tmp, pre, words, red);
-    }
-    // final keep words: local picks | global picks | recent window
-    for (int w = warp; w < words; w += NWARP) {
-      const int s = w * 32 + lane;
-      bool kp = (loc[w] >> lane) & 1u;
-      if (!kp && s < ncmp && need_g > 0) {
-        const unsigned k = okey(sc[s]);
-        if (k > T) {
-          kp = true;
-        } else if (k == T) {
-          kp = all_ties || (pre[w] + __popc(tmp[w] & ((1u << lane) - 1u))) < need_eq;
+    };
+    const int quota = min(a.k_loc, kt / P);
+    // Fast path, exact whenever it applies: take the global top-K_t of ALL
+    // candidates first.  Its drop set D0 is a suffix of the (score desc,
+    // slot asc) order, so each block's kept part is a prefix of the block.
+    // If every block keeps at least its quota k_loc', each block's top
+    // k_loc' (S_loc) lies outside D0, and the Eq. 10 drop set -- the bottom
+    // of C minus S_loc -- is D0 itself.  Otherwise Eq. 10 runs in full.
+    global_keep();
+    if (tid == 0) s_fast = 1;
+    __syncthreads();
+    for (int j = warp; j < P; j += NWARP) {
+      const int lo = j * PAGE, hi = min(lo + PAGE, ncmp);
+      const int kj = min(quota, hi - lo);
+      if (kj <= 0) continue;
+      unsigned c = 0;
+      if (lane < PAGE / 32) {
+        const int w = (lo >> 5) + lane, s0 = w * 32;
+        if (s0 < hi) {
+          const int nb = min(32, hi - s0);
+          c = __popc(keep[w] & (nb == 32 ? 0xffffffffu : ((1u << nb) - 1u)));
         }
       }
-      if (s >= ncmp) kp = true;
-      const unsigned b = __ballot_sync(0xffffffffu, kp);
-      if (lane == 0) keep[w] = b;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      if (lane == 0 && c < (unsigned)kj) s_fast = 0;
     }
     __syncthreads();
+    if (!s_fast) {
+      // ---- Eq. 10, block-local part: TopK_{k_loc'}(B_j) per logical block ----
+      // Bit-serial radix select of each block's kj-th largest key: at each bit
+      // the keys that match the prefix and have the bit set are counted with
+      // warp ballots.  A warp takes GB blocks at once, so their
+      // independent reduction chains overlap.  Afterwards prefix = that key
+      // and above = the number of keys above it.
+      constexpr int GB = 4;
+      for (int j0 = warp; j0 < P; j0 += NWARP * GB) {
+        unsigned key[GB][8], prefix[GB], above[GB], need[GB];
+        bool val[GB][8];
+        int kjv[GB];
+  #pragma unroll
+        for (int g = 0; g < GB; ++g) {
+          const int j = j0 + g * NWARP;
+          const int lo = j * PAGE;
+          const int hi = min(lo + PAGE, ncmp);
+          kjv[g] = j < P ? max(0, min(quota, hi - lo)) : 0;
+  #pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s = lo + 32 * e + lane;
+            val[g][e] = j < P && s < hi;
+            key[g][e] = val[g][e] ? okey(sc[s]) : 0u;
+          }
+          prefix[g] = 0u;
+          above[g] = 0u;
+          need[g] = (unsigned)kjv[g];
+        }
+        unsigned mask = 0u;
+        for (int bit = 31; bit >= 0; --bit) {
+          const unsigned m2 = mask | (1u << bit);
+          unsigned tot[GB];
+  #pragma unroll
+          for (int g = 0; g < GB; ++g) {
+            const unsigned p2 = prefix[g] | (1u << bit);
+            unsigned c = 0;
+  #pragma unroll
+            for (int e = 0; e < 8; ++e)
+              c += (unsigned)__popc(__ballot_sync(0xffffffffu, val[g][e] && (key[g][e] & m2) == p2));
+            tot[g] = c;
+          }
+  #pragma unroll
+          for (int g = 0; g < GB; ++g) {
+            if (tot[g] >= need[g]) {
+              prefix[g] |= 1u << bit;
+            } else {
+              need[g] -= tot[g];
+              above[g] += tot[g];
+            }
+          }
+          mask = m2;
+        }
+  #pragma unroll
+        for (int g = 0; g < GB; ++g) {
+          if (kjv[g] <= 0) continue;
+          const int lo = (j0 + g * NWARP) * PAGE;
+          const unsigned need_eq = (unsigned)kjv[g] - above[g];
+          unsigned run = 0;
+  #pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const bool gt = val[g][e] && key[g][e] > prefix[g];
+            const bool eq = val[g][e] && key[g][e] == prefix[g];
+            const unsigned be = __ballot_sync(0xffffffffu, eq);
+            const unsigned rank = run + __popc(be & ((1u << lane) - 1u));
+            run += __popc(be);
+            const unsigned bw = __ballot_sync(0xffffffffu, gt || (eq && rank < need_eq));
+            if (lane == 0) loc[(lo >> 5) + e] = bw;
+          }
+        }
+      }
+      __syncthreads();
+
+      __syncthreads();
+      global_keep();
+    }
   }
 
   // ---- validate: exactly (P-1) b slots kept ------------------------------
