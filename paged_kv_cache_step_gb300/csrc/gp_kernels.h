@@ -171,9 +171,13 @@ struct AttnArgs {
   double beta_s, beta_l;
   const double* inv_freq;  // [D/2]
   float* out;              // [n][Hq][D]
-  float* part;             // split partials [n][Hkv][nsplit][G][D + 2]
+  float* part;             // split partials [n_ctas][G][D + 2], those of (r, h) together
   unsigned* tickets;       // [n][Hkv], zero before the launch
-  int n, nsplit;
+  const int32_t* split_base;  // [n + 1] first CTA of each request, in `order`
+  const int32_t* order;    // [n] requests, longest first; request order[i] has
+                           // (split_base[i+1] - split_base[i]) / Hkv splits, CTA
+                           // split_base[i] + split * Hkv + h
+  int n, n_ctas;
   int* err;
 };
 cudaError_t launch_decode_attention(const AttnArgs& a, cudaStream_t s);

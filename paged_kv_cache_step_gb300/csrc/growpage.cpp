@@ -1224,14 +1224,35 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   if ((st = join_select(c)) != GP_OK) return st;  // it reads the upload buffer this call rewrites
   const int G = g.num_q_heads / g.num_kv_heads;
   const int maxp = g.max_pages_per_req;
-  // splits over pages: about four CTAs per SM over the whole call
-  int nsplit = (4 * 152 + n * g.num_kv_heads - 1) / (n * g.num_kv_heads);
-  nsplit = std::max(1, std::min(nsplit, 64));
-  const size_t part_floats = (size_t)n * g.num_kv_heads * nsplit * G * (g.head_dim + 2);
+  const int Hkv = g.num_kv_heads;
+  // Splits over the attended pages: about `chunk` pages per CTA, so that the
+  // call fills roughly three waves of two CTAs per SM; longest requests first,
+  // so that the largest CTAs start first.
+  std::vector<int> npg(n), order(n), nsp(n);
+  long long total_pages = 0;
+  for (int r = 0; r < n; ++r) {
+    npg[r] = (num_tokens[r] + kPage - 1) / kPage;
+    total_pages += npg[r];
+    order[r] = r;
+  }
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return npg[x] > npg[y]; });
+  const long long target_ctas = 3LL * 2 * 152;
+  const long long chunk = std::max(1LL, (total_pages * Hkv + target_ctas - 1) / target_ctas);
+  long long n_ctas = 0;
+  for (int r = 0; r < n; ++r) {
+    nsp[r] = (int)std::max(1LL, std::min(64LL, (npg[r] + chunk - 1) / chunk));
+    n_ctas += (long long)nsp[r] * Hkv;
+  }
+  const size_t part_floats = (size_t)n_ctas * G * (g.head_dim + 2);
   const size_t tick_off = (part_floats * sizeof(float) + 255) & ~size_t(255);
-  if ((st = ensure(c, c->attn, tick_off + sizeof(unsigned) * (size_t)n * g.num_kv_heads)) != GP_OK) return st;
+  if ((st = ensure(c, c->attn, tick_off + sizeof(unsigned) * (size_t)n * Hkv)) != GP_OK) return st;
   Staged s{};
   if ((st = stage(c, n, false, &s)) != GP_OK) return st;
+  s.part_base[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    s.sel[i] = order[i];
+    s.part_base[i + 1] = s.part_base[i] + nsp[order[i]] * Hkv;
+  }
   for (int r = 0; r < n; ++r) {
     gp::DevReq& d = s.reqs[r];
     d.num_pages = reqs[r].num_pages;
@@ -1272,8 +1293,10 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   a.out = out_dev;
   a.part = reinterpret_cast<float*>(base);
   a.tickets = reinterpret_cast<unsigned*>(base + tick_off);
+  a.split_base = dev_at<int32_t>(c, s.off_pb);
+  a.order = dev_at<int32_t>(c, s.off_sel);
   a.n = n;
-  a.nsplit = nsplit;
+  a.n_ctas = (int)n_ctas;
   a.err = c->err_dev;
   return timed_launch(c, GP_KERNEL_ATTENTION, "decode_attention",
                       [&] { return gp::launch_decode_attention(a, c->stream); });
