@@ -167,3 +167,35 @@ def test_theorem31_bound_after_compress_and_hold():
         assert checked == n * sh.num_layers * sh.num_q_heads
     finally:
         run.close()
+
+
+def test_decode_attention_multi_page_splits():
+    """Enough pages that a split spans several pages (the host gives each CTA
+    about total_pages * Hkv / 912 pages) and the 64-split cap applies to the
+    longest request; ragged token counts end inside a stage."""
+    sh = SHAPES["bf16_g4_d128"]
+    sizes = [160, 150, 130, 97, 40, 5]  # 582 pages x 2 KV heads: about 2 pages per CTA
+    w = synth.make_workload("custom", device="cuda", shape=sh, sizes=sizes, seed_xor=44)
+    run = hz.EngineRun(w)
+    try:
+        run.feed_history()
+        n, G, layer = len(sizes), sh.group, 0
+        ntok = [160 * PAGE, 150 * PAGE - 77, 130 * PAGE - 1, 97 * PAGE - 255, 40 * PAGE - 128, 5 * PAGE - 130]
+        q = torch.randn(n, sh.num_q_heads, sh.head_dim, device="cuda").to(torch.bfloat16)
+        first = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        out = torch.full((n, sh.num_q_heads, sh.head_dim), float("nan"), device="cuda")
+        gp.gp_decode_attention(run.ctx, layer, run.reqs, ntok, q, first, out)
+        torch.cuda.synchronize()
+        out = out.cpu().numpy().astype(np.float64)
+        qn = q.double().cpu().numpy()
+        for r, req in enumerate(run.reqs):
+            for h in range(sh.num_kv_heads):
+                keys = hz.unit_keys_dev(w.k_cache, req.pages, layer, h)[:ntok[r]]
+                vals = hz.unit_keys_dev(w.v_cache, req.pages, layer, h)[:ntok[r]]
+                ref, _ = _oracle_attention(qn[r, h * G:(h + 1) * G], keys, vals, req.pos, sh.rope_theta)
+                got = out[r, h * G:(h + 1) * G]
+                tol = 1e-4 * np.abs(vals).max() + 1e-5 * np.abs(ref)
+                assert np.all(np.abs(got - ref) <= tol), \
+                    f"request {r} head {h}: error {np.abs(got - ref).max()}"
+    finally:
+        run.close()
