@@ -181,6 +181,28 @@ def coverage_demand_detail(a, p: float):
 
 
 # ---------------------------------------------------------------------------
+# Sec. 5.3, Table 2: attention entropy in place of the Top-p working set
+# ---------------------------------------------------------------------------
+
+def entropy_support(a) -> float:
+    """exp(H(a)) with H(a) = -sum_i a_i ln a_i over the a_i > 0.
+
+    The dual-timescale ablation of Sec. 5.3 (Table 2) swaps the Top-p
+    working-set metric for attention entropy and gives no formula.  The
+    reading taken here is the entropy's effective support size: the number
+    of equally weighted tokens with the same entropy (1 for a point mass, N
+    for the uniform distribution over N).  It stands where K^x = D_p stands
+    in Eq. 8, so Delta = mean over (layer, KV head) of
+    (exp H(a^S) - exp H(a^L)) / |C_t| (demand_trend with these values).
+    """
+    a = np.asarray(a, np.float64)
+    nz = a[a > 0]
+    if nz.size == 0:
+        return 0.0
+    return float(np.exp(-np.sum(nz * np.log(nz))))
+
+
+# ---------------------------------------------------------------------------
 # One (request, layer, KV head) unit at a capacity boundary
 # ---------------------------------------------------------------------------
 

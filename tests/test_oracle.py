@@ -15,6 +15,7 @@ import os
 import numpy as np
 import pytest
 import scipy.special
+import scipy.stats
 
 import oracle
 from oracle import growpage as og
@@ -449,6 +450,52 @@ def test_pool_cow_and_compaction():
 
 
 # ---------------------------------------------------------------------------
+# Sec. 5.3, Table 2: the entropy metric's effective support size exp(H)
+# ---------------------------------------------------------------------------
+
+def check_entropy_support(es=og.entropy_support):
+    rng = np.random.default_rng(11)
+    # a point mass spreads over one token, a uniform distribution over all of them
+    assert es(np.eye(1, 37, 5)[0]) == 1.0
+    for n in (1, 2, 7, 256, 8176):
+        assert abs(es(np.full(n, 1.0 / n)) - n) <= 1e-9 * n
+    # uniform over m of n slots, zeros elsewhere: m (zeros carry no entropy)
+    a = np.zeros(1000)
+    a[rng.choice(1000, 40, replace=False)] = 1.0 / 40
+    assert abs(es(a) - 40) <= 1e-9
+    # scipy's Shannon entropy (natural log) on random distributions
+    for n in (3, 50, 4096):
+        a = rng.dirichlet(np.full(n, 0.3))
+        assert abs(math.log(es(a)) - scipy.stats.entropy(a)) <= 1e-10 * max(1.0, scipy.stats.entropy(a))
+    # additivity over a product distribution, and the bounds 1/max(a) <= exp(H) <= N
+    x, y = rng.dirichlet(np.ones(9)), rng.dirichlet(np.full(13, 0.5))
+    assert abs(es(np.outer(x, y).ravel()) - es(x) * es(y)) <= 1e-9 * es(x) * es(y)
+    for _ in range(20):
+        a = rng.dirichlet(np.full(64, rng.uniform(0.05, 3.0)))
+        assert 1.0 / a.max() - 1e-9 <= es(a) <= 64 + 1e-9
+    # permutation invariance
+    a = rng.dirichlet(np.ones(100))
+    assert abs(es(a) - es(rng.permutation(a))) <= 1e-12 * es(a)
+
+
+def test_entropy_support():
+    check_entropy_support()
+
+
+def test_entropy_trend_and_decision():
+    """With exp(H) in place of K^x, Eq. 8 and the decision keep their form:
+    a short summary spread wider than the long one grows, a narrower one compresses."""
+    n_cand = 7 * 256
+    wide = og.entropy_support(np.full(n_cand, 1.0 / n_cand))
+    narrow = og.entropy_support(np.full(64, 1.0 / 64))
+    assert wide == pytest.approx(n_cand) and narrow == pytest.approx(64)
+    d = og.demand_trend([wide, narrow], [narrow, narrow], n_cand)
+    assert d == pytest.approx((n_cand - 64) / (2 * n_cand))
+    assert og.decide(d, 8, 10, 0, 0.0).kind == og.GROW
+    assert og.decide(-d, 8, 10, 0, 0.0).kind == og.COMPRESS
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes (in the oracle, on the CPU) are caught by the pins
 # ---------------------------------------------------------------------------
 
@@ -491,6 +538,30 @@ def test_pins_catch_dp_mutants(mutant):
 def test_pins_catch_ema_mutant():
     with pytest.raises(AssertionError):
         check_ema_golden(_ema_swapped)
+
+
+def _entropy_sign_flipped(a):
+    nz = np.asarray(a, float)
+    nz = nz[nz > 0]
+    return float(np.exp(np.sum(nz * np.log(nz))))
+
+
+def _entropy_log2(a):
+    nz = np.asarray(a, float)
+    nz = nz[nz > 0]
+    return float(np.exp(-np.sum(nz * np.log2(nz))))
+
+
+def _entropy_unweighted(a):
+    nz = np.asarray(a, float)
+    nz = nz[nz > 0]
+    return float(np.exp(-np.mean(np.log(nz))))
+
+
+@pytest.mark.parametrize("mutant", [_entropy_sign_flipped, _entropy_log2, _entropy_unweighted])
+def test_pins_catch_entropy_mutants(mutant):
+    with pytest.raises(AssertionError):
+        check_entropy_support(mutant)
 
 
 def test_oracle_exports():
