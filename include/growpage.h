@@ -89,6 +89,15 @@ typedef enum {
   GP_POLICY_SHRINK = 4
 } gp_policy;
 typedef enum { GP_ACT_GROW = 0, GP_ACT_COMPRESS = 1, GP_ACT_SHRINK = 2 } gp_action_kind;
+/* Working-set metric of the demand estimation.
+ *   TOP_P:   K^x = D_p(a^x) over C_t (Eq. 2, Eq. 7), the method's metric.
+ *   ENTROPY: the ablation of Sec. 5.3 (Table 2) that puts attention entropy
+ *            in its place.  The pages give no formula; the engine takes the
+ *            entropy's effective support size E^x = exp(H(a^x)),
+ *            H(a) = -sum_i a_i ln a_i over C_t (1 for a point mass, |C_t| for
+ *            the uniform distribution), and uses it where K^x stands in
+ *            Eq. 8.  D_p is still computed and reported. */
+typedef enum { GP_METRIC_TOP_P = 0, GP_METRIC_ENTROPY = 1 } gp_metric;
 
 /* Engine configuration.  Defaults (gp_config_default) follow the paper:
  * page_size 256, recent_window 16, k_loc 64, beta_s 0.9, beta_l 0.999,
@@ -118,6 +127,7 @@ typedef struct gp_config {
   double shrink_threshold;   /* SHRINK: Shrink iff Delta < this */
   int32_t shrink_floor_pages;/* SHRINK: no Shrink at or below this many pages */
   uint32_t random_seed;      /* RANDOM: seed of the counter-based draws */
+  int32_t demand_metric;     /* gp_metric; default TOP_P */
 } gp_config;
 
 /* One request as the caller's scheduler sees it.  block_table is a HOST
@@ -135,13 +145,19 @@ typedef struct gp_request {
 /* Result of the demand estimation for one request (Eqs. 7-8):
  * sum_k_short = sum over (layer, KV head) of K^S, likewise sum_k_long;
  * num_candidates = |C_t| = (P - 1) * b; num_units = L * Hkv;
- * delta = (sum_k_short - sum_k_long) / (num_candidates * num_units). */
+ * delta = (sum_k_short - sum_k_long) / (num_candidates * num_units).
+ * Under GP_METRIC_ENTROPY, eff_short / eff_long = sums over the units of
+ * exp(H(a^S)) / exp(H(a^L)) (in unit order), and
+ * delta = (eff_short - eff_long) / (num_candidates * num_units); under
+ * TOP_P both are 0. */
 typedef struct gp_demand {
   int64_t sum_k_short;
   int64_t sum_k_long;
   int32_t num_candidates;
   int32_t num_units;
   double delta;
+  double eff_short;
+  double eff_long;
 } gp_demand;
 
 typedef struct gp_action {
@@ -240,6 +256,8 @@ gp_status gp_boundary_demand(gp_ctx* ctx, int32_t n, const gp_request* reqs,
  * are the caller's: out is host gp_demand[n]; k_units, if not NULL, is host
  * int32[n][L * Hkv][2] receiving K^S, K^L per (layer, KV head).  It does not
  * prepare a following gp_compress_hold (call gp_boundary_demand for that).
+ * Contexts with demand_metric GP_METRIC_ENTROPY are refused
+ * (GP_ERR_UNSUPPORTED); eff_short and eff_long are 0.
  * Synchronises the stream. */
 gp_status gp_boundary_demand_noalloc(gp_ctx* ctx, int32_t n, const gp_request* reqs,
                                      const void* q_cur_dev, gp_demand* out,
@@ -248,7 +266,9 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* ctx, int32_t n, const gp_request* r
 /* gp_decide: per the configured policy (gp_policy above; GROWPAGE: Grow iff
  * Delta > tau, else Compress & Hold, Sec. 3.2).  Delta is compared as
  * delta = (sum_k_short - sum_k_long) / (num_candidates * num_units) in
- * double (for tau == 0 the Grow test is the exact integer one).  P == 1
+ * double (for tau == 0 the Grow test is the exact integer one); under
+ * GP_METRIC_ENTROPY as (eff_short - eff_long) / (num_candidates *
+ * num_units), compared with tau in double.  P == 1
  * forces Grow; a Grow that would leave the pool at or below reserve_pages
  * (counting earlier grants of this call) becomes a fallback Compress
  * (Sec. 4.2, App. H.2).  Host only. */
@@ -359,6 +379,10 @@ gp_status gp_debug_scores(gp_ctx* ctx, int32_t req_idx, float* out);
 gp_status gp_debug_probs(gp_ctx* ctx, int32_t req_idx, float* out);
 /* Keep masks of the last gp_compress_hold: host uint32[L*Hkv][ceil(P b/32)]. */
 gp_status gp_debug_keep_mask(gp_ctx* ctx, int32_t req_idx, uint32_t* out);
+/* Effective support sizes exp(H(a^S)), exp(H(a^L)) per unit of the last
+ * demand call: host double[L * Hkv * 2] ([unit][x]).  GP_ERR_STATE unless
+ * the context's demand_metric is GP_METRIC_ENTROPY. */
+gp_status gp_debug_entropy(gp_ctx* ctx, int32_t req_idx, double* out);
 /* Summaries of one slot: host double[L][2][Hq][d]. */
 gp_status gp_read_summaries(gp_ctx* ctx, int32_t slot, double* out);
 
@@ -383,7 +407,8 @@ gp_status gp_set_scan_kernel(gp_ctx* ctx, int32_t kind);
 #define GP_KERNEL_COMPRESS 3
 #define GP_KERNEL_ATTENTION 4
 #define GP_KERNEL_SELECT 5
-#define GP_KERNEL_COUNT 6
+#define GP_KERNEL_ENTROPY 6
+#define GP_KERNEL_COUNT 7
 gp_status gp_set_timing(gp_ctx* ctx, int32_t enabled);
 gp_status gp_kernel_time(gp_ctx* ctx, int32_t kernel, double* ms, int64_t* launches);
 gp_status gp_reset_timing(gp_ctx* ctx);

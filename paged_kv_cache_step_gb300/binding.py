@@ -25,11 +25,12 @@ GP_ERR_CUDA, GP_ERR_TIMEOUT, GP_ERR_STATE, GP_ERR_UNSUPPORTED = 4, 5, 6, 7
 GP_DTYPE_BF16, GP_DTYPE_F32 = 0, 1
 GP_POLICY_GROWPAGE, GP_POLICY_FIXED, GP_POLICY_RANDOM, GP_POLICY_INVERSE, GP_POLICY_SHRINK = 0, 1, 2, 3, 4
 GP_ACT_GROW, GP_ACT_COMPRESS, GP_ACT_SHRINK = 0, 1, 2
+GP_METRIC_TOP_P, GP_METRIC_ENTROPY = 0, 1
 GP_SCAN_AUTO, GP_SCAN_CUDA_CORE, GP_SCAN_TENSOR_CORE = 0, 1, 2
 GP_KERNEL_EMA, GP_KERNEL_PREP, GP_KERNEL_DEMAND, GP_KERNEL_COMPRESS, GP_KERNEL_ATTENTION = 0, 1, 2, 3, 4
-GP_KERNEL_SELECT = 5
+GP_KERNEL_SELECT, GP_KERNEL_ENTROPY = 5, 6
 KERNEL_NAMES = {0: "ema_update", 1: "prep_queries", 2: "boundary_demand", 3: "compress_hold",
-                4: "decode_attention", 5: "select"}
+                4: "decode_attention", 5: "select", 6: "entropy"}
 
 EXPORTS = [
     "gp_config_default", "gp_create", "gp_destroy", "gp_last_error", "gp_status_string",
@@ -37,7 +38,7 @@ EXPORTS = [
     "gp_slot_acquire", "gp_slot_release", "gp_update_summaries", "gp_boundary_demand",
     "gp_boundary_demand_noalloc",
     "gp_decide", "gp_grow_page", "gp_compress_hold", "gp_shrink", "gp_compress_fill", "gp_compact_kv",
-    "gp_debug_demand_k",
+    "gp_debug_demand_k", "gp_debug_entropy",
     "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
     "gp_set_scan_kernel", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
     "gp_set_compaction_stream", "gp_wait_compaction", "gp_decode_attention",
@@ -55,6 +56,7 @@ class GpConfig(C.Structure):
         ("rope_theta", C.c_double),
         ("random_compress", C.c_double), ("shrink_threshold", C.c_double),
         ("shrink_floor_pages", C.c_int32), ("random_seed", C.c_uint32),
+        ("demand_metric", C.c_int32),
     ]
 
 
@@ -65,7 +67,8 @@ class GpRequest(C.Structure):
 
 class GpDemand(C.Structure):
     _fields_ = [("sum_k_short", C.c_int64), ("sum_k_long", C.c_int64),
-                ("num_candidates", C.c_int32), ("num_units", C.c_int32), ("delta", C.c_double)]
+                ("num_candidates", C.c_int32), ("num_units", C.c_int32), ("delta", C.c_double),
+                ("eff_short", C.c_double), ("eff_long", C.c_double)]
 
 
 class GpAction(C.Structure):
@@ -127,6 +130,7 @@ def load(build_if_missing: bool = True):
         "gp_compress_fill": (I32, [P, I32, C.POINTER(GpRequest)]),
         "gp_compact_kv": (I32, [P, I32, C.POINTER(GpRequest), P]),
         "gp_debug_demand_k": (I32, [P, I32, P]),
+        "gp_debug_entropy": (I32, [P, I32, P]),
         "gp_debug_scores": (I32, [P, I32, P]),
         "gp_debug_probs": (I32, [P, I32, P]),
         "gp_debug_keep_mask": (I32, [P, I32, P]),
@@ -352,6 +356,12 @@ def gp_compact_kv(ctx, reqs, keep_masks_dev):
 def gp_debug_demand_k(ctx, req_idx: int, units: int) -> np.ndarray:
     out = np.zeros((units, 2), dtype=np.int32)
     _check(ctx, load().gp_debug_demand_k(ctx, req_idx, out.ctypes.data))
+    return out
+
+
+def gp_debug_entropy(ctx, req_idx: int, units: int) -> np.ndarray:
+    out = np.zeros((units, 2), dtype=np.float64)
+    _check(ctx, load().gp_debug_entropy(ctx, req_idx, out.ctypes.data))
     return out
 
 

@@ -182,6 +182,15 @@ struct AttnArgs {
 };
 cudaError_t launch_decode_attention(const AttnArgs& a, cudaStream_t s);
 
+// ---- entropy metric (Sec. 5.3 ablation): exp(H(a^x)) per unit ----------------
+struct EntropyArgs {
+  const DevReq* reqs;      // [n] (num_pages, aval_off)
+  const float* aval;       // a^S, a^L over C_t of the demand call: per unit [2][(P-1) b]
+  int n, units, b;
+  double* out;             // [n][units][2]
+};
+cudaError_t launch_entropy(const EntropyArgs& a, cudaStream_t s);
+
 // ---- A8-A10: window mask, Eq. 10 top-k, copy-on-write compaction -----------
 struct CompressArgs {
   void* k_cache;

@@ -76,7 +76,7 @@ struct gp_ctx {
   double* pool = nullptr;          // [L][M][2][Hq][D]
   int* err_dev = nullptr;          // kernel error bits
   unsigned long long* moved_dev = nullptr;
-  DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks, xstat, attn, spec_masks;
+  DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks, xstat, attn, spec_masks, ent;
   // speculative selection: the Eq. 10 keep masks of every request of the last
   // demand call, computed on an engine-owned stream while the host decides
   cudaStream_t sel_stream = nullptr;
@@ -320,6 +320,7 @@ gp_status gp_config_default(gp_config* cfg) {
   cfg->shrink_threshold = -0.005;
   cfg->shrink_floor_pages = 4;  // 1024 tokens
   cfg->random_seed = 0u;
+  cfg->demand_metric = GP_METRIC_TOP_P;
   return GP_OK;
 }
 
@@ -341,6 +342,7 @@ gp_status gp_create(const gp_config* cfg, void* k_cache, void* v_cache, void* st
   if (g.recent_window < 0 || g.recent_window >= kPage || g.k_loc < 0 || g.reserve_pages < 0)
     return GP_ERR_INVALID;
   if (g.policy < GP_POLICY_GROWPAGE || g.policy > GP_POLICY_SHRINK) return GP_ERR_INVALID;
+  if (g.demand_metric != GP_METRIC_TOP_P && g.demand_metric != GP_METRIC_ENTROPY) return GP_ERR_INVALID;
   if (!(g.random_compress >= 0.0 && g.random_compress <= 1.0) || !std::isfinite(g.shrink_threshold) ||
       g.shrink_floor_pages < 2)
     return GP_ERR_INVALID;
@@ -402,7 +404,7 @@ gp_status gp_destroy(gp_ctx* c) {
     if (c->ev_sel) cudaEventDestroy(c->ev_sel);
     if (c->ev_ready) cudaEventDestroy(c->ev_ready);
     if (c->ev_done) cudaEventDestroy(c->ev_done);
-    for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->bq, &c->scores, &c->aval, &c->tickets, &c->kout, &c->ksum,
+    for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->bq, &c->scores, &c->aval, &c->tickets, &c->kout, &c->ksum, &c->ent,
                       &c->masks, &c->xstat, &c->attn, &c->spec_masks})
       if (b->p) cudaFree(b->p);
     if (c->inv_freq) cudaFree(c->inv_freq);
@@ -770,6 +772,23 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     GP_CUDA(c, cudaEventRecord(c->ev_sel, c->sel_stream));
     c->sel_pending = true;
   }
+  // the entropy metric (Sec. 5.3 ablation): exp(H(a^x)) per unit from the a-values
+  const bool entropy = g.demand_metric == GP_METRIC_ENTROPY;
+  std::vector<double> eff(entropy ? (size_t)n * units * 2 : 0);
+  if (entropy) {
+    if ((st = ensure(c, c->ent, sizeof(double) * eff.size())) != GP_OK) return st;
+    gp::EntropyArgs ea{};
+    ea.reqs = pa.reqs;
+    ea.aval = static_cast<const float*>(c->aval.p);
+    ea.n = n;
+    ea.units = units;
+    ea.b = kPage;
+    ea.out = static_cast<double*>(c->ent.p);
+    st = timed_launch(c, GP_KERNEL_ENTROPY, "entropy", [&] { return gp::launch_entropy(ea, c->stream); });
+    if (st != GP_OK) return st;
+    GP_CUDA(c, cudaMemcpyAsync(eff.data(), c->ent.p, sizeof(double) * eff.size(), cudaMemcpyDeviceToHost,
+                               c->stream));
+  }
   std::vector<unsigned long long> sums((size_t)n * 2);
   GP_CUDA(c, cudaMemcpyAsync(sums.data(), c->ksum.p, sizeof(unsigned long long) * sums.size(),
                              cudaMemcpyDeviceToHost, c->stream));
@@ -787,6 +806,15 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     o.delta = o.num_candidates > 0
                   ? (double)(o.sum_k_short - o.sum_k_long) / ((double)o.num_candidates * units)
                   : 0.0;
+    o.eff_short = 0.0;
+    o.eff_long = 0.0;
+    if (entropy) {
+      for (int u = 0; u < units; ++u) {  // unit order: the same sum on every call
+        o.eff_short += eff[((size_t)r * units + u) * 2];
+        o.eff_long += eff[((size_t)r * units + u) * 2 + 1];
+      }
+      o.delta = o.num_candidates > 0 ? (o.eff_short - o.eff_long) / ((double)o.num_candidates * units) : 0.0;
+    }
     DemandRec& rec = c->last_demand[r];
     rec.slot = reqs[r].slot;
     rec.num_pages = P;
@@ -840,9 +868,11 @@ gp_status gp_decide(gp_ctx* c, int32_t n, const gp_request* reqs, const gp_deman
       const double units = (double)demand[r].num_units;
       const double cand = (double)demand[r].num_candidates;
       const int64_t diff = demand[r].sum_k_short - demand[r].sum_k_long;
-      const double delta = (double)diff / (cand * units);
-      // Delta > tau; for tau = 0 the exact integer test
-      const bool above_tau = (g.tau == 0.0) ? diff > 0 : delta > g.tau;
+      const bool entropy = g.demand_metric == GP_METRIC_ENTROPY;
+      const double delta = entropy ? (demand[r].eff_short - demand[r].eff_long) / (cand * units)
+                                   : (double)diff / (cand * units);
+      // Delta > tau; for D_p and tau = 0 the exact integer test
+      const bool above_tau = (g.tau == 0.0 && !entropy) ? diff > 0 : delta > g.tau;
       bool want = false, shrink = false;
       switch (g.policy) {
         case GP_POLICY_GROWPAGE: want = above_tau; break;
@@ -1077,6 +1107,20 @@ gp_status gp_debug_demand_k(gp_ctx* c, int32_t req_idx, int32_t* k_out) {
   const int units = units_of(c);
   GP_CUDA(c, cudaMemcpyAsync(k_out, static_cast<int32_t*>(c->kout.p) + (size_t)req_idx * units * 2,
                              sizeof(int32_t) * units * 2, cudaMemcpyDeviceToHost, c->stream));
+  GP_CUDA(c, cudaStreamSynchronize(c->stream));
+  return GP_OK;
+}
+
+gp_status gp_debug_entropy(gp_ctx* c, int32_t req_idx, double* out) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if ((st = join_compaction(c)) != GP_OK) return st;
+  if (c->cfg.demand_metric != GP_METRIC_ENTROPY) return fail(c, GP_ERR_STATE, "the demand metric is not ENTROPY");
+  if (!out || req_idx < 0 || req_idx >= (int)c->last_demand.size())
+    return fail(c, GP_ERR_INVALID, "no demand result %d", req_idx);
+  const int units = units_of(c);
+  GP_CUDA(c, cudaMemcpyAsync(out, static_cast<double*>(c->ent.p) + (size_t)req_idx * units * 2,
+                             sizeof(double) * units * 2, cudaMemcpyDeviceToHost, c->stream));
   GP_CUDA(c, cudaStreamSynchronize(c->stream));
   return GP_OK;
 }

@@ -80,6 +80,8 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
     return fail(c, GP_ERR_INVALID, "n = %lld outside [0, %lld]", n, GP_NOALLOC_MAX_REQ);
   if (n == 0) return GP_OK;
   if (!reqs || !out || !q_cur_dev) return fail(c, GP_ERR_INVALID, "null argument");
+  if (g.demand_metric != GP_METRIC_TOP_P)
+    return fail(c, GP_ERR_UNSUPPORTED, "the entropy metric needs gp_boundary_demand");
   if (g.num_pages > (int)GP_NOALLOC_MAX_PAGES_BITS)
     return fail(c, GP_ERR_UNSUPPORTED, "more than %lld pages", GP_NOALLOC_MAX_PAGES_BITS);
 
@@ -302,6 +304,8 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
                        ? (double)(out[r].sum_k_short - out[r].sum_k_long) /
                              ((double)out[r].num_candidates * units)
                        : 0.0;
+    out[r].eff_short = 0.0;
+    out[r].eff_long = 0.0;
   }
   return GP_OK;
 }

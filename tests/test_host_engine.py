@@ -47,10 +47,11 @@ def test_struct_layout_matches_header():
 #include <stddef.h>
 #include "growpage.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(gp_config), offsetof(gp_config, beta_s),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(gp_config), offsetof(gp_config, beta_s),
          offsetof(gp_config, rope_theta), sizeof(gp_request), offsetof(gp_request, pos),
          sizeof(gp_demand), sizeof(gp_action), sizeof(gp_stats_t), offsetof(gp_config, shrink_threshold),
-         offsetof(gp_config, random_seed), offsetof(gp_stats_t, shrink));
+         offsetof(gp_config, random_seed), offsetof(gp_stats_t, shrink), offsetof(gp_config, demand_metric),
+         offsetof(gp_demand, eff_long));
   return 0;
 }
 """
@@ -65,7 +66,8 @@ int main(void) {
     ref = [C.sizeof(gp.GpConfig), gp.GpConfig.beta_s.offset, gp.GpConfig.rope_theta.offset,
            C.sizeof(gp.GpRequest), gp.GpRequest.pos.offset, C.sizeof(gp.GpDemand),
            C.sizeof(gp.GpAction), C.sizeof(gp.GpStats), gp.GpConfig.shrink_threshold.offset,
-           gp.GpConfig.random_seed.offset, gp.GpStats.shrink.offset]
+           gp.GpConfig.random_seed.offset, gp.GpStats.shrink.offset, gp.GpConfig.demand_metric.offset,
+           gp.GpDemand.eff_long.offset]
     assert vals == ref
 
 
@@ -284,6 +286,55 @@ def test_decide_policies_match_oracle(policy):
 
 def test_policy_config_validation():
     for bad in (dict(policy=9), dict(random_compress=1.5), dict(shrink_floor_pages=1),
-                dict(shrink_threshold=float("nan"))):
+                dict(shrink_threshold=float("nan")), dict(demand_metric=2), dict(demand_metric=-1)):
         with pytest.raises(gp.GrowPageError):
             _host_ctx(**bad)
+
+
+@pytest.mark.parametrize("policy", ["growpage", "inverse", "shrink"])
+def test_decide_entropy_metric_matches_oracle(policy):
+    """Under the entropy metric (Sec. 5.3 ablation) Delta comes from the
+    effective support sizes exp(H(a^x)) summed over the units, compared with
+    tau in double; the D_p sums are ignored.  Against the oracle's rules."""
+    rng = np.random.default_rng(12)
+    for tau in (0.0, 0.01):
+        ctx = _host_ctx(num_pages=64, policy=POLICIES[policy], demand_metric=gp.GP_METRIC_ENTROPY, tau=tau)
+        try:
+            units = 8
+            for trial in range(40):
+                n = int(rng.integers(1, 6))
+                reqs, dem = [], []
+                for i in range(n):
+                    P = int(rng.integers(1, 9))
+                    reqs.append(gp.Request(i, list(range(P)), P * 256, 8))
+                    cand = (P - 1) * 256
+                    d = gp.GpDemand()
+                    d.num_candidates, d.num_units = cand, units
+                    e_l = rng.uniform(1.0, max(cand, 1), units)
+                    e_s = np.clip(e_l * rng.choice([1.0, 0.5, 1.5, rng.uniform(0.9, 1.1)]), 1.0, max(cand, 1))
+                    d.eff_short, d.eff_long = float(e_s.sum()), float(e_l.sum())
+                    # D_p sums that would decide the other way: the entropy metric must ignore them
+                    d.sum_k_short, d.sum_k_long = (0, 10 ** 6) if e_s.sum() > e_l.sum() else (10 ** 6, 0)
+                    dem.append(d)
+                free = gp.gp_free_page_count(ctx)
+                acts = gp.gp_decide(ctx, reqs, dem)
+                granted = 0
+                for r, (q, d, a) in enumerate(zip(reqs, dem, acts)):
+                    P = q.num_pages
+                    delta = og.demand_trend([d.eff_short], [d.eff_long], d.num_candidates * d.num_units) \
+                        if P > 1 else 0.0
+                    ref = og.decide(delta, P, free - granted, 0, tau, policy=policy)
+                    assert (a.kind, bool(a.fallback), bool(a.forced)) == (ref.kind, ref.fallback, ref.forced), \
+                        (policy, tau, trial, r, P, delta)
+                    granted += int(a.kind == gp.GP_ACT_GROW and not a.forced)
+        finally:
+            gp.gp_destroy(ctx)
+
+
+def test_host_only_context_refuses_entropy_readback():
+    ctx = _host_ctx(demand_metric=gp.GP_METRIC_ENTROPY)
+    try:
+        with pytest.raises(gp.GrowPageError):
+            gp.gp_debug_entropy(ctx, 0, 4)
+    finally:
+        gp.gp_destroy(ctx)
