@@ -165,10 +165,14 @@ class Clocks:
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def _metric(args) -> int:
+    return 1 if getattr(args, "demand_metric", "top_p") == "entropy" else 0
+
+
 class Stream:
     """Config-2 decode stream driven through the C ABI."""
 
-    def __init__(self, device, num_pages=64, P=32, fill=False):
+    def __init__(self, device, num_pages=64, P=32, fill=False, metric=0):
         import paged_kv_cache_step_gb300 as gp
         self.gp = gp
         gp.load(build_if_missing=False)
@@ -180,6 +184,7 @@ class Stream:
             num_layers=sh.num_layers, num_q_heads=sh.num_q_heads, num_kv_heads=sh.num_kv_heads,
             head_dim=sh.head_dim, kv_dtype=gp.GP_DTYPE_BF16, q_dtype=gp.GP_DTYPE_BF16,
             max_slots=8, num_pages=w.num_pages, max_pages_per_req=128, rope_theta=sh.rope_theta)
+        cfg.demand_metric = metric
         self.cfg = cfg
         self.ctx = gp.gp_create(cfg, w.k_cache, w.v_cache, self.torch_stream)
         used = set(w.block_tables[0])
@@ -251,7 +256,7 @@ def run_gpu(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     peak, peak_src = _peaks()
-    s = Stream(device, fill=args.compaction == "fill")
+    s = Stream(device, fill=args.compaction == "fill", metric=_metric(args))
     # warm the summaries over the first boundary interval
     s.advance(EVENT_STRIDE - 1)
 
@@ -329,7 +334,7 @@ def run_gpu(args, world, rank, local):
     # back every step, inside the timed region
     e2e = None
     if not args.no_e2e:
-        s = Stream(device, fill=args.compaction == "fill")
+        s = Stream(device, fill=args.compaction == "fill", metric=_metric(args))
         s.advance(EVENT_STRIDE - 1)
         for _ in range(args.warmup):
             q = s._query()
@@ -353,7 +358,7 @@ def run_gpu(args, world, rank, local):
             s.advance(EVENT_STRIDE - 1)
         maxp = s.cfg.max_pages_per_req
         h2d = s.q_bytes + 48 + 4 * maxp * 2 + 4
-        d2h = 16 + 4
+        d2h = 16 + 4 + (s.cfg.num_layers * s.cfg.num_kv_heads * 2 * 8 if _metric(args) else 0)
         e2e = {"value": len(e2e_times) / (sum(e2e_times) / 1e3), "unit": "events/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "step_ms": [round(x, 4) for x in e2e_times],
@@ -372,7 +377,8 @@ def run_gpu(args, world, rank, local):
                                "at the first boundary, 64-page pool, 512-step concentrated/diffuse "
                                "query phases, boundary every 256 decode steps"
                                + ("; hole-fill compaction (order-destroying variant)" if args.compaction == "fill"
-                                  else ""),
+                                  else "")
+                               + ("; entropy demand metric (Sec. 5.3 ablation)" if _metric(args) else ""),
                    "l2": "inputs larger than L2 (0.54+ GB of K scanned per event, 1.07 GB K/V)",
                    "parallelism": f"replicas x{world}"},
         "step_ms": [round(x, 4) for x in times],
@@ -449,7 +455,7 @@ def measure_overlap(args, device):
 # the other configurations (one JSON line each; not the default line)
 # ---------------------------------------------------------------------------
 
-def _engine_over(gp, w, stream, max_slots, max_pages, policy):
+def _engine_over(gp, w, stream, max_slots, max_pages, policy, metric=0):
     sh = w.shape
     cfg = gp.gp_config_default(
         num_layers=sh.num_layers, num_q_heads=sh.num_q_heads, num_kv_heads=sh.num_kv_heads,
@@ -457,6 +463,7 @@ def _engine_over(gp, w, stream, max_slots, max_pages, policy):
         max_slots=max_slots, num_pages=w.num_pages, max_pages_per_req=max_pages, rope_theta=sh.rope_theta)
     if policy == "fixed":
         cfg.policy = gp.GP_POLICY_FIXED
+    cfg.demand_metric = metric
     return cfg, gp.gp_create(cfg, w.k_cache, w.v_cache, stream)
 
 
@@ -485,7 +492,7 @@ def run_batch(args, device):
     w = synth.make_workload(args.workload, device=device)
     sh = w.shape
     ts = torch.cuda.Stream(device=device)
-    cfg, ctx = _engine_over(gp, w, ts, max(4, w.n), 256, args.policy)
+    cfg, ctx = _engine_over(gp, w, ts, max(4, w.n), 256, args.policy, _metric(args))
     used = set(p for t in w.block_tables for p in t)
     for _ in range(w.num_pages):
         gp.gp_page_alloc(ctx)
@@ -553,7 +560,8 @@ def run_batch(args, device):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {synth.CONFIGS[args.workload][2]}; policy {args.policy}",
+        "config": {"workload": f"{args.workload}: {synth.CONFIGS[args.workload][2]}; policy {args.policy}"
+                               + ("; entropy demand metric (Sec. 5.3 ablation)" if _metric(args) else ""),
                    "l2": "inputs larger than L2"},
         "kv_gbs": (scan_bytes + comp_bytes) / (total / 1e3) / 1e9,
         "scan_bytes": scan_bytes, "compaction_bytes": comp_bytes, "compress_events": ncomp,
@@ -760,6 +768,8 @@ def main():
     ap.add_argument("--async-overlap", action="store_true",
                     help="also time compaction on a side stream overlapped with decode steps")
     ap.add_argument("--overlap-intervals", type=int, default=8)
+    ap.add_argument("--demand-metric", default="top_p", choices=["top_p", "entropy"],
+                    help="working-set metric of the demand estimation (entropy: the Sec. 5.3 ablation)")
     ap.add_argument("--compaction", default="stable", choices=["stable", "fill"],
                     help="fill: the order-destroying hole-fill variant (reported separately)")
     args = ap.parse_args()
