@@ -6,9 +6,11 @@
 //
 // Input: the GQA-mean distributions a^S, a^L over C_t that the demand
 // kernels keep for the D_p select (fp32, per unit [2][(P-1) b]).  One CTA
-// per (request, unit, summary) streams its row with 16-byte loads; each
-// term a ln a is formed in fp32 and the sum is kept in fp64.  The row is
-// 4 bytes per candidate, 1/64 of the K bytes the scan read at d = 128.
+// per (request, unit, summary) streams its row with 16-byte loads; the four
+// terms a ln a of a load are formed and added in fp32, and those partial
+// sums are added in fp64 (GB300's fp64 rate is low, so one fp64 add per
+// four candidates, not per candidate).  The row is 4 bytes per candidate,
+// 1/64 of the K bytes the scan read at d = 128.
 #include <cstdint>
 
 #include "gp_kernels.h"
@@ -18,7 +20,7 @@ namespace {
 
 constexpr int NT = 256;
 
-__device__ __forceinline__ double plogp(float v) { return v > 0.f ? (double)(v * logf(v)) : 0.0; }
+__device__ __forceinline__ float plogp(float v) { return v > 0.f ? v * logf(v) : 0.f; }
 
 __global__ void __launch_bounds__(NT) k_entropy(EntropyArgs a) {
   __shared__ double part[NT / 32];
@@ -32,7 +34,7 @@ __global__ void __launch_bounds__(NT) k_entropy(EntropyArgs a) {
     const float4* row = reinterpret_cast<const float4*>(a.aval + rq.aval_off + ((size_t)unit * 2 + x) * ndem);
     for (int i = threadIdx.x; i < ndem / 4; i += NT) {
       const float4 v = __ldg(row + i);
-      acc += plogp(v.x) + plogp(v.y) + plogp(v.z) + plogp(v.w);
+      acc += (double)((plogp(v.x) + plogp(v.y)) + (plogp(v.z) + plogp(v.w)));
     }
   }
 #pragma unroll
