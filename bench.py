@@ -261,8 +261,7 @@ def run_gpu(args, world, rank, local):
     s.advance(EVENT_STRIDE - 1)
 
     def one_event(q):
-        scan, kind = s.event(q)
-        return scan
+        return s.event(q)  # (K bytes scanned, action kind)
 
     # warm-up events (untimed)
     for _ in range(args.warmup):
@@ -277,7 +276,7 @@ def run_gpu(args, world, rank, local):
         torch.distributed.barrier()
     clock_file = os.path.join(tempfile.gettempdir(), f"growpage_bench_clocks_{os.getpid()}_r{rank}.csv")
     clocks = Clocks(local, clock_file)
-    times = []
+    times, kinds = [], []
     scan_bytes = 0
     for _ in range(args.steps):
         q = s._query()
@@ -285,8 +284,10 @@ def run_gpu(args, world, rank, local):
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev0.record(s.torch_stream)
-        scan_bytes += one_event(q)
+        sb, kind = one_event(q)
         ev1.record(s.torch_stream)
+        scan_bytes += sb
+        kinds.append(kind)
         torch.cuda.synchronize()
         times.append(ev0.elapsed_time(ev1))
         s.advance(EVENT_STRIDE - 1)    # not timed
@@ -320,6 +321,18 @@ def run_gpu(args, world, rank, local):
                                "frac": a / peak, "bytes_per_launch": comp_bytes / cmp_["launches"],
                                "ms_per_launch": cmp_["ms"] / cmp_["launches"]}
     dom = max(rl, key=lambda k: kern[k]["ms"]) if rl else None
+    # events by action (event time on the engine stream), and demand alone
+    # (device time of its prep and scan kernels)
+    by_action = {}
+    for kid, name in ((gp.GP_ACT_GROW, "grow"), (gp.GP_ACT_COMPRESS, "compress"), (gp.GP_ACT_SHRINK, "shrink")):
+        t = [ms for ms, k in zip(times, kinds) if k == kid]
+        if t:
+            by_action[name] = {"events": len(t), "ms_mean": sum(t) / len(t), "events_per_s": len(t) / (sum(t) / 1e3)}
+    demand_ms = dem["ms"] + kern["prep_queries"]["ms"]
+    if dem["launches"] and demand_ms > 0:
+        by_action["demand_only"] = {"events": dem["launches"], "ms_mean": demand_ms / dem["launches"],
+                                    "events_per_s": dem["launches"] / (demand_ms / 1e3),
+                                    "timing": "device time of the prep and demand kernels"}
 
     actions = dict(s.actions)
     cpu = None
@@ -385,7 +398,7 @@ def run_gpu(args, world, rank, local):
         "kv_gbs": kv_gbs,
         "kv_frac": kv_gbs / peak,
         "scan_bytes": scan_bytes, "compaction_bytes": comp_bytes,
-        "actions": actions,
+        "actions": actions, "events_by_action": by_action,
         "roofline": dict(rl[dom], kernel=dom, peak_source=peak_src,
                          traffic=_traffic(dom, rl[dom]["bytes_per_launch"])) if dom else None,
         "kernels": {k: dict(v, **({"frac": rl[k]["frac"], "achieved_gbs": rl[k]["achieved"]}
