@@ -496,6 +496,71 @@ def test_entropy_trend_and_decision():
 
 
 # ---------------------------------------------------------------------------
+# summary queries (Eq. 12 then RoPE), importance (Eq. 9), retention, gather
+# ---------------------------------------------------------------------------
+
+def check_summary_queries(sq=og.summary_queries):
+    rng = np.random.default_rng(21)
+    L, hq, d = 2, 4, 64
+    qs, ql, q = (rng.normal(size=(L, hq, d)) * sc for sc in (0.3, 2.0, 1.0))
+    out = sq(qs, ql, q, 37, 1e4)
+    assert out.shape == (L, 2, hq, d)
+    # Eq. 12 restores the current query's RMS, and RoPE keeps the norm
+    for x in range(2):
+        assert np.allclose(np.sqrt(np.mean(out[:, x] ** 2, axis=-1)), np.sqrt(np.mean(q ** 2, axis=-1)),
+                           rtol=1e-12)
+    # x = 0 is the short summary: swapping the summaries swaps the rows
+    sw = sq(ql, qs, q, 37, 1e4)
+    assert np.allclose(sw[:, 0], out[:, 1]) and np.allclose(sw[:, 1], out[:, 0])
+    # at position 0 the row is the summary itself, rescaled by a positive factor
+    z = sq(qs, ql, q, 0, 1e4)
+    for x, qb in ((0, qs), (1, ql)):
+        ratio = z[:, x] / qb
+        assert np.all(ratio > 0) and np.allclose(ratio, ratio[..., :1], rtol=1e-12)
+    # logits depend on relative position only: rows at pos m against keys rotated to n
+    k = rng.normal(size=(5, d))
+    a = og.logits(sq(qs, ql, q, 90, 1e4)[0, 0], og.rope(k, 30, 1e4))
+    b = og.logits(sq(qs, ql, q, 60, 1e4)[0, 0], k)
+    assert np.allclose(a, b, rtol=1e-10, atol=1e-12)
+
+
+def test_summary_queries():
+    check_summary_queries()
+
+
+def test_importance_is_the_larger_of_the_two_distributions():
+    rng = np.random.default_rng(22)
+    a_s, a_l = rng.dirichlet(np.ones(300)), rng.dirichlet(np.full(300, 0.2))
+    s = og.importance(a_s, a_l)
+    assert np.all(s >= a_s) and np.all(s >= a_l)
+    assert np.all((s == a_s) | (s == a_l))
+    assert np.array_equal(s, og.importance(a_l, a_s))
+    assert np.array_equal(og.importance(a_s, a_s), a_s)
+
+
+def test_retention_budget_frees_exactly_drop_pages():
+    for P in (2, 5, 33, 160):
+        for drop in (1, 2):
+            if P - drop < 1:
+                continue
+            kt = og.retention_budget(P, 256, 16, drop)
+            assert P * 256 - (kt + 16) == drop * 256     # the kept set fills (P - drop) pages exactly
+    assert og.retention_budget(32, 256, 16) == 7920      # K_t = (P - 1) b - R at 32 pages
+
+
+def test_compact_unit_keeps_order_and_rows():
+    rng = np.random.default_rng(23)
+    rows = np.arange(4 * 256 * 3, dtype=np.float64).reshape(4 * 256, 3)   # row i holds 3i, 3i+1, 3i+2
+    keep = np.zeros(4 * 256, bool)
+    keep[rng.choice(4 * 256, 3 * 256, replace=False)] = True
+    out = og.compact_unit(rows, keep)
+    assert out.shape == (3 * 256, 3)
+    src = (out[:, 0] / 3).astype(int)                  # which slot each output row came from
+    assert np.all(np.diff(src) > 0)                    # ascending slot order, no repeats
+    assert np.all(keep[src]) and src.size == keep.sum()
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes (in the oracle, on the CPU) are caught by the pins
 # ---------------------------------------------------------------------------
 
@@ -562,6 +627,20 @@ def _entropy_unweighted(a):
 def test_pins_catch_entropy_mutants(mutant):
     with pytest.raises(AssertionError):
         check_entropy_support(mutant)
+
+
+def _summary_queries_swapped(qs, ql, q, pos, theta):
+    return og.summary_queries(ql, qs, q, pos, theta)
+
+
+def _summary_queries_uncalibrated(qs, ql, q, pos, theta):
+    return np.stack([og.rope(np.asarray(x, float), pos, theta) for x in (qs, ql)], axis=1)
+
+
+@pytest.mark.parametrize("mutant", [_summary_queries_swapped, _summary_queries_uncalibrated])
+def test_pins_catch_summary_query_mutants(mutant):
+    with pytest.raises(AssertionError):
+        check_summary_queries(mutant)
 
 
 def test_oracle_exports():
