@@ -224,6 +224,24 @@ def test_host_only_context_refuses_device_calls():
         with pytest.raises(gp.GrowPageError) as ei:
             gp.gp_boundary_demand(ctx, [gp.Request(0, [0], 0, 8)], 0)
         assert ei.value.status == gp.GP_ERR_STATE
+        # every other call that touches the device is refused the same way, before any work
+        req = [gp.Request(0, [0, 1], 256, 8)]
+        calls = [
+            lambda: gp.gp_boundary_demand_noalloc(ctx, req, 0),
+            lambda: gp.gp_compress_hold(ctx, req),
+            lambda: gp.gp_shrink(ctx, req),
+            lambda: gp.gp_compress_fill(ctx, req),
+            lambda: gp.gp_decode_attention(ctx, 0, req, [256], 0, 0, 0),
+            lambda: gp.gp_set_compaction_stream(ctx, None),
+            lambda: gp.gp_wait_compaction(ctx, None),
+            lambda: gp.gp_debug_probs(ctx, 0, 4, 256),
+            lambda: gp.gp_read_summaries(ctx, 0, 2, 4, 64),
+        ]
+        for i, call in enumerate(calls):
+            with pytest.raises(gp.GrowPageError) as ei:
+                call()
+            assert ei.value.status == gp.GP_ERR_STATE, i
+        assert req[0].pages == [0, 1] and req[0].num_pages == 2   # tables untouched
     finally:
         gp.gp_destroy(ctx)
 
