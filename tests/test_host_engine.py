@@ -356,3 +356,21 @@ def test_host_only_context_refuses_entropy_readback():
             gp.gp_debug_entropy(ctx, 0, 4)
     finally:
         gp.gp_destroy(ctx)
+
+
+def test_config_defaults_are_the_papers():
+    """gp_config_default against the values the pages fix: 256-token blocks
+    and the 16-token recent window (Sec. 5.1), the per-block quota
+    k_loc = 64 (App. D.2), p = 0.99 (Sec. 3.2), beta_S = 0.9 and
+    beta_L = 0.999 (the default row of Table 2, Sec. 5.3), tau = 0 (Grow iff
+    Delta > 0, Sec. 3.2), 512 summary slots (App. E.1 Eq. 11), Random(0.7),
+    the Shrink threshold -0.005 of Eq. 13 and its 1024-token floor
+    (App. H.1), and the Top-p working-set metric."""
+    cfg = gp.gp_config_default()
+    assert (cfg.page_size, cfg.recent_window, cfg.k_loc) == (256, 16, 64)
+    assert (cfg.beta_s, cfg.beta_l, cfg.p, cfg.tau) == (0.9, 0.999, 0.99, 0.0)
+    assert cfg.max_slots == 512
+    assert cfg.policy == gp.GP_POLICY_GROWPAGE and cfg.demand_metric == gp.GP_METRIC_TOP_P
+    assert cfg.random_compress == 0.7 and cfg.shrink_threshold == -0.005
+    assert cfg.shrink_floor_pages * cfg.page_size == 1024
+    assert cfg.reserve_pages == 0
