@@ -732,3 +732,135 @@ def test_hole_fill_by_hand():
     # no hole: nothing moves
     keep = np.array([1, 1, 1, 1, 0, 0, 0, 0], bool)
     assert og.hole_fill_unit(rows, keep, 2, 4)[:, 0].tolist() == [0.0, 1.0, 2.0, 3.0]
+
+
+# ---------------------------------------------------------------------------
+# input widening, rotary frequencies and the logical gather, each pinned to
+# hand-written values (tests/golden/bf16.json, rope.json, gather.json)
+# ---------------------------------------------------------------------------
+
+def check_widen_bf16(widen=og.widen_bf16):
+    cases = _golden("bf16.json")["cases"]
+    bits = np.array([int(c["bits"], 16) for c in cases], dtype=np.uint16)
+    got = np.asarray(widen(bits), dtype=np.float64)
+    assert got.dtype == np.float64 and got.shape == bits.shape
+    for c, g in zip(cases, got):
+        want = c["value"]
+        if want == "nan":
+            assert math.isnan(g), c["note"]
+        elif want in ("inf", "-inf"):
+            assert g == float(want), c["note"]
+        else:
+            w = float.fromhex(want)
+            assert g == w and math.copysign(1.0, g) == math.copysign(1.0, w), (c["note"], g, w)
+
+
+def test_widen_bf16_golden():
+    check_widen_bf16()
+
+
+def check_rope_golden(rope=og.rope):
+    gd = _golden("rope.json")
+    d, theta = gd["d"], gd["theta"]
+    half = d // 2
+    for pos, rec in gd["positions"].items():
+        c, s = np.array(rec["cos"]), np.array(rec["sin"])
+        out = np.asarray(rope(np.ones(d), int(pos), theta))
+        assert np.allclose(out[:half], c - s, rtol=0, atol=1e-15), (pos, out)
+        assert np.allclose(out[half:], c + s, rtol=0, atol=1e-15), (pos, out)
+        for j in range(half):
+            e = np.zeros(d)
+            e[j] = 1.0
+            col = np.asarray(rope(e, int(pos), theta))
+            want = np.zeros(d)
+            want[j], want[j + half] = c[j], s[j]
+            assert np.allclose(col, want, rtol=0, atol=1e-15), (pos, j, col)
+
+
+def test_rope_golden_every_frequency():
+    check_rope_golden()
+
+
+def check_gather_golden(gather=og.gather_logical):
+    gd = _golden("gather.json")
+    L, npg, hkv, b = gd["layers"], gd["pages"], gd["kv_heads"], gd["page_size"]
+    cache = np.zeros((L, npg, hkv, b, 1))
+    for layer, p, h, s in itertools.product(range(L), range(npg), range(hkv), range(b)):
+        cache[layer, p, h, s, 0] = 1000 * layer + 100 * p + 10 * h + s
+    for c in gd["cases"]:
+        got = np.asarray(gather(cache, c["block_table"], c["layer"], c["kv_head"]))
+        assert got.shape == (len(c["rows"]), 1), got.shape
+        assert got[:, 0].tolist() == c["rows"], (c, got[:, 0].tolist())
+
+
+def test_gather_logical_golden():
+    check_gather_golden()
+
+
+def _widen_shift15(bits):
+    u = np.asarray(bits).astype(np.uint32) << np.uint32(15)
+    return u.view(np.float32).astype(np.float64)
+
+
+def _widen_as_fp16(bits):
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def _widen_unsigned(bits):
+    u = (np.asarray(bits).astype(np.uint32) & np.uint32(0x7FFF)) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("mutant", [_widen_shift15, _widen_as_fp16, _widen_unsigned])
+def test_pins_catch_widen_mutants(mutant):
+    with pytest.raises(AssertionError):
+        check_widen_bf16(mutant)
+
+
+def _rope_exponent_i_over_d(x, pos, theta):
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    ang = float(pos) * np.power(float(theta), -np.arange(half) / d)
+    c, s = np.cos(ang), np.sin(ang)
+    return np.concatenate([x[..., :half] * c - x[..., half:] * s, x[..., half:] * c + x[..., :half] * s], -1)
+
+
+def _rope_interleaved(x, pos, theta):
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    ang = float(pos) * np.power(float(theta), -2.0 * np.arange(d // 2) / d)
+    c, s = np.cos(ang), np.sin(ang)
+    ev, od = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = ev * c - od * s
+    out[..., 1::2] = od * c + ev * s
+    return out
+
+
+def _rope_clockwise(x, pos, theta):
+    return og.rope(x, -pos, theta)
+
+
+@pytest.mark.parametrize("mutant", [_rope_exponent_i_over_d, _rope_interleaved, _rope_clockwise])
+def test_pins_catch_rope_mutants(mutant):
+    with pytest.raises(AssertionError):
+        check_rope_golden(mutant)
+
+
+def _gather_sorted_pages(cache, table, layer, h):
+    return og.gather_logical(cache, sorted(table), layer, h)
+
+
+def _gather_head_layer_swapped(cache, table, layer, h):
+    return np.concatenate([np.asarray(cache[h, pg, layer]) for pg in table], axis=0)
+
+
+def _gather_first_page_only(cache, table, layer, h):
+    return np.concatenate([np.asarray(cache[layer, table[0], h]) for _ in table], axis=0)
+
+
+@pytest.mark.parametrize("mutant", [_gather_sorted_pages, _gather_head_layer_swapped, _gather_first_page_only])
+def test_pins_catch_gather_mutants(mutant):
+    with pytest.raises((AssertionError, IndexError)):
+        check_gather_golden(mutant)
