@@ -290,13 +290,18 @@ def request_boundary(qbar_s, qbar_l, q_cur, k_cache, block_table, pos: int,
 def demand_trend(k_short, k_long, n_cand: int) -> float:
     """Delta = r^S - r^L with r^x = mean over (layer, KV head) of K^x / |C_t|.
 
-    GrowPage, Sec. 3.2, Eqs. 7-8 (all layers participate).
+    GrowPage, Sec. 3.2, Eqs. 7-8 (all layers participate).  |C_t| is the
+    same for every (layer, KV head) of a request, so Delta equals
+    (sum K^S - sum K^L) / (|C_t| * units).  It is evaluated in that form: the
+    sums of integer demands are exact in float64, so the sign of Delta -- and
+    with it the decision, where Delta = 0 compresses -- is exact, which two
+    separately rounded means would not guarantee.
     """
     if n_cand <= 0:
         return 0.0
-    rs = np.mean(np.asarray(k_short, np.float64) / n_cand)
-    rl = np.mean(np.asarray(k_long, np.float64) / n_cand)
-    return float(rs - rl)
+    ks = np.asarray(k_short, np.float64)
+    kl = np.asarray(k_long, np.float64)
+    return float((np.sum(ks) - np.sum(kl)) / (float(n_cand) * ks.size))
 
 
 @dataclass

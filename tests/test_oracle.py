@@ -308,6 +308,35 @@ def test_demand_trend_forms_agree_in_sign():
         assert d == pytest.approx(raw / (n * ks.size), rel=1e-12, abs=1e-15)
 
 
+def check_trend_sign_exact(trend=og.demand_trend):
+    # Eq. 8 with equal demand sums: Delta is exactly 0 whatever the split over
+    # units, so the decision after Eq. 8 compresses (Delta = tau = 0 is not
+    # above tau).  Cases written by hand: 3/7 + 5/7 and 4/7 + 4/7 are not
+    # equal once each ratio is rounded separately.
+    for ks, kl, n in (([3, 5], [4, 4], 7), ([1, 2, 3], [3, 2, 1], 11), ([10, 1, 1, 7], [5, 5, 5, 4], 23)):
+        d = trend(np.array(ks), np.array(kl), n)
+        assert d == 0.0, (ks, kl, n, d)
+        assert og.decide(d, 4, 10, 0, 0.0).kind == og.COMPRESS
+    rng = np.random.default_rng(12)
+    for _ in range(2000):
+        n = int(rng.integers(1, 40000))
+        ks = rng.integers(1, n + 1, size=int(rng.integers(2, 300)))
+        assert trend(ks, np.roll(ks, 1), n) == 0.0
+
+
+def test_trend_sign_exact_at_equal_sums():
+    check_trend_sign_exact()
+
+
+def _trend_mean_of_rounded_ratios(k_short, k_long, n_cand):
+    return float(np.mean(np.asarray(k_short, float) / n_cand) - np.mean(np.asarray(k_long, float) / n_cand))
+
+
+def test_pins_catch_trend_rounding_mutant():
+    with pytest.raises(AssertionError):
+        check_trend_sign_exact(_trend_mean_of_rounded_ratios)
+
+
 def test_planted_tiny_workloads_take_both_actions():
     # Sec. 3.2: a more concentrated short summary (Delta < 0) compresses; a
     # more diffuse one (Delta > 0) grows.  The synthetic tiny workloads put a
