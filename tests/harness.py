@@ -3,7 +3,11 @@ bench's CPU baseline: drive a synthetic workload through the C-ABI engine and
 through the fp64 oracle, and compare them with the stated tolerances.
 
 Tolerances (GrowPage boundary engine):
-  * decision, page tables, gathered K/V bytes for a given index set: exact;
+  * decision, page tables, gathered K/V bytes for a given index set: exact.
+    The decision is checked twice: it must follow exactly from the GPU's own
+    D_p values, and it must equal the oracle's unless the units where the two
+    D_p differ by the allowed 1 (t of them) could move the demand difference
+    across zero, i.e. unless -t < (sum K^S - sum K^L)_oracle <= t;
   * D_p: may differ by 1, only where the oracle's sorted cumulative mass at
     the crossing lies within 1e-6 (relative) of p;
   * top-k sets: identical except members whose oracle score is within 1e-5
@@ -16,6 +20,8 @@ Tolerances (GrowPage boundary engine):
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -213,3 +219,78 @@ def summaries_ok(gpu: np.ndarray, ref: np.ndarray):
     scale = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True)) + 1e-30
     err = np.abs(gpu.astype(np.float64) - ref) / scale
     return float(err.max())
+
+
+def decision_ok(act, k_oracle, k_gpu, num_pages, free_pages, reserve=0, tau=0.0):
+    """The GrowPage decision (after Eq. 8, Sec. 4.2) of the GPU for one request.
+
+    k_oracle, k_gpu: [units][2] D_p values (x = 0 short, 1 long) of the
+    oracle and of the GPU, already checked unit by unit with dp_ok.  The
+    GPU's action must (1) be og.decide applied to its own D_p values, and
+    (2) equal og.decide applied to the oracle's unless the t tie units could
+    flip Delta across tau.  Returns (ok, message)."""
+    P = num_pages
+    k_oracle = np.asarray(k_oracle, np.int64)
+    k_gpu = np.asarray(k_gpu, np.int64)
+    ncand = (P - 1) * PAGE
+    d_gpu = og.demand_trend(k_gpu[:, 0], k_gpu[:, 1], ncand) if P > 1 else 0.0
+    d_ora = og.demand_trend(k_oracle[:, 0], k_oracle[:, 1], ncand) if P > 1 else 0.0
+    got = (int(act.kind), bool(act.fallback), bool(act.forced))
+    mine = og.decide(d_gpu, P, free_pages, reserve, tau)
+    if got != (mine.kind, mine.fallback, mine.forced):
+        return False, f"action {got} does not follow from the GPU's own D_p (expected {mine})"
+    ref = og.decide(d_ora, P, free_pages, reserve, tau)
+    if got == (ref.kind, ref.fallback, ref.forced):
+        return True, ""
+    t = int(np.abs(k_gpu - k_oracle).sum())
+    if P > 1 and tau == 0.0:
+        diff = int(k_oracle[:, 0].sum() - k_oracle[:, 1].sum())
+        ambiguous = -t < diff <= t
+    else:
+        ambiguous = P > 1 and abs(d_ora - tau) <= t / (ncand * len(k_oracle))
+    if ambiguous:
+        return True, "tie"
+    return False, f"action {got} vs oracle {ref} with {t} tie units"
+
+
+_POOL = None
+
+
+def oracle_pool() -> ThreadPoolExecutor:
+    """Threads for oracle work over many units (numpy and the device copies
+    release the interpreter lock)."""
+    global _POOL
+    if _POOL is None:
+        _POOL = ThreadPoolExecutor(max_workers=max(2, min(32, os.cpu_count() or 2)))
+    return _POOL
+
+
+def request_dp_check(w, req, qt, ks_gpu, keep=(), p=0.99, recent=16):
+    """D_p of every (layer, KV head) unit of one request against the oracle.
+
+    The oracle runs unit by unit on a thread pool (keys widened exactly to
+    float64).  Returns (k_oracle [units][2], failures [str], {idx: UnitResult}
+    for idx in keep)."""
+    sh = w.shape
+    units = sh.num_layers * sh.num_kv_heads
+    keep = set(keep)
+
+    def one(idx):
+        layer, h = divmod(idx, sh.num_kv_heads)
+        u = oracle_unit_dev(qt, w.k_cache, req.pages, layer, h, sh.group, p, recent)
+        bad = []
+        if req.num_pages > 1:
+            for x in range(2):
+                ok, msg = dp_ok(int(ks_gpu[idx, x]), u.a_dem[x], p)
+                if not ok:
+                    bad.append(f"unit {idx} x {x}: {msg}")
+        return idx, np.array(u.k, np.int64), bad, (u if idx in keep else None)
+
+    k_or = np.zeros((units, 2), np.int64)
+    fails, kept = [], {}
+    for idx, k, bad, u in oracle_pool().map(one, range(units)):
+        k_or[idx] = k
+        fails.extend(bad)
+        if u is not None:
+            kept[idx] = u
+    return k_or, fails, kept

@@ -188,11 +188,9 @@ def test_llama_single_boundary_event():
         scores = gp.gp_debug_scores(run.ctx, 0, run.units, P * PAGE - 16)
         ks, ties = _check_demand(run, 0, res, probs, scores)
         kk = np.array([res[i].k for i in range(run.units)])
-        delta = og.demand_trend(kk[:, 0], kk[:, 1], (P - 1) * PAGE)
         act = gp.gp_decide(run.ctx, run.reqs, dem)[0]
-        ref = og.decide(delta, P, gp.gp_free_page_count(run.ctx), 0, 0.0)
-        if ties == 0:
-            assert act.kind == ref.kind
+        ok, msg = hz.decision_ok(act, kk, ks, P, gp.gp_free_page_count(run.ctx))
+        assert ok, msg
         # Compress & Hold regardless of the decision, to check selection + bytes
         pre_k, pre_v = w.k_cache.clone(), w.v_cache.clone()
         old = req.pages

@@ -122,13 +122,11 @@ class Checker:
                         self.snap[(s, idx)] = (hz.unit_keys_dev(self.w.k_cache, req.pages, layer, h),
                                                hz.unit_keys_dev(self.w.v_cache, req.pages, layer, h))
                 self.checked += 1
-            if full and ties == 0:
-                delta = og.demand_trend(kk[:, 0], kk[:, 1], (P - 1) * PAGE)
+            if full:
                 free_before = gp.gp_free_page_count(drv.ctx)
                 grants = sum(1 for a in acts[:r] if a.kind == gp.GP_ACT_GROW and not a.forced)
-                ref = og.decide(delta, P, free_before - grants, 0, 0.0)
-                assert acts[r].kind == ref.kind and bool(acts[r].fallback) == ref.fallback, \
-                    f"step {t} seat {s}: decision {acts[r].kind}/{acts[r].fallback} vs oracle {ref}"
+                ok, msg = hz.decision_ok(acts[r], kk, ks, P, free_before - grants)
+                assert ok, f"step {t} seat {s}: {msg}"
                 self.decisions += 1
 
     def post_compress(self, drv, t, cseats):
