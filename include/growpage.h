@@ -63,7 +63,10 @@ typedef enum {
   GP_ERR_NO_PAGES = 2,    /* the free pool cannot supply the pages; nothing changed */
   GP_ERR_NO_SLOTS = 3,    /* no free summary slot; nothing changed */
   GP_ERR_CUDA = 4,        /* a CUDA runtime call failed (text in gp_last_error) */
-  GP_ERR_TIMEOUT = 5,     /* reserved: a bounded device-side wait gave up */
+  GP_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (about one second of SM
+                             clock); the kernel drained its copies and returned, so the
+                             context stays usable, but that launch's outputs are
+                             unspecified */
   GP_ERR_STATE = 6,       /* call out of order (e.g. compress without a fresh demand) */
   GP_ERR_UNSUPPORTED = 7  /* shape outside what the kernels were built for */
 } gp_status;
@@ -246,16 +249,24 @@ gp_status gp_boundary_demand(gp_ctx* ctx, int32_t n, const gp_request* reqs,
  * their tensor-core operands, importance values, a-values, arrival tickets,
  * per-unit D_p and their sums) lives in one file-scope device array of
  * 64 MiB that every GPU loading the library holds until the process exits.
- * A call needing more (roughly: the sum over requests of
- * 12 * L * Hkv * P * b bytes plus L * Hkv * 9 KiB) is rejected with
- * GP_ERR_INVALID and a message naming the size; n is at most 512.  On the first call on a device, with that device current, the
+ * A call needing more is rejected with GP_ERR_INVALID and a message naming
+ * the size; n is at most 512.  The need: per request, its importance values
+ * and a-values, L * Hkv * (4 (P b - R) + 8 (P - 1) b) bytes (about
+ * 12 L Hkv P b; each region rounded up to 256 bytes), plus per (layer, KV
+ * head) of every request 16 * 8 * 26 bytes of partial softmax statistics,
+ * 8 G d bytes of calibrated summaries, (d / 64) * 128 * ceil(6 G / 16) * 16
+ * bytes of tensor-core operand and 16 bytes of counters -- about 15.3 KiB at
+ * d = 128, G = 4 -- plus small descriptor arrays.  On the first call on a device, with that device current, the
  * array's address is looked up once (cudaGetSymbolAddress); make that first
  * call before any stream capture.  All calls share the array and its host
  * staging, which keep the last call's contents: calls that overlap on the
  * GPU, or run on several host threads at once, race.  Inputs and outputs
  * are the caller's: out is host gp_demand[n]; k_units, if not NULL, is host
  * int32[n][L * Hkv][2] receiving K^S, K^L per (layer, KV head).  It does not
- * prepare a following gp_compress_hold (call gp_boundary_demand for that).
+ * prepare a following gp_compress_hold: the demand records that an earlier
+ * gp_boundary_demand left for these slots are dropped, so a
+ * gp_compress_hold of them returns GP_ERR_STATE until the next
+ * gp_boundary_demand.  Device-side errors are reported as by gp_synchronize.
  * Contexts with demand_metric GP_METRIC_ENTROPY are refused
  * (GP_ERR_UNSUPPORTED); eff_short and eff_long are 0.
  * Synchronises the stream. */
@@ -280,7 +291,16 @@ gp_status gp_decide(gp_ctx* ctx, int32_t n, const gp_request* reqs,
  * full block table leave the request unchanged.  Host only. */
 gp_status gp_grow_page(gp_ctx* ctx, gp_request* req);
 
-/* gp_compress_hold: Compress & Hold for n requests, each of which must have
+/* Device-side errors of the asynchronous calls below (a failed check inside a
+ * kernel, or a bounded wait that gave up) are reported by the next call that
+ * synchronises with the engine -- gp_synchronize, gp_boundary_demand or an
+ * inspection call -- as GP_ERR_INVALID or GP_ERR_TIMEOUT.  The host-side state
+ * of the failed call (block tables, refcounts, the pool) was committed when it
+ * returned GP_OK; the K/V rows of the units it was compacting are then
+ * unspecified.  Errors found before the launch (arguments, GP_ERR_NO_PAGES, a
+ * launch that fails) change nothing.
+ *
+ * gp_compress_hold: Compress & Hold for n requests, each of which must have
  * been passed to the last gp_boundary_demand with the same slot, pages and
  * block table (else GP_ERR_STATE).  Per (layer, KV head): importance
  * (Eq. 9), the recent R tokens always kept, block-local top-k_loc' with
@@ -340,8 +360,11 @@ gp_status gp_compact_kv(gp_ctx* ctx, int32_t n, gp_request* reqs,
  * q_dev: device [n][Hq][d] in q_dtype; first_dev: device uint8 [n];
  * num_tokens: HOST int32 [n], 0 <= num_tokens[r] <= num_pages * 256 (0 gives
  * a zero output); out_dev: device fp32 [n][Hq][d].  Requests need not be at
- * a boundary.  Waits for a pending side-stream compaction.  Asynchronous on
- * the engine stream. */
+ * a boundary.  With a compaction pending on the side stream (see
+ * gp_set_compaction_stream), the call makes the engine stream wait for it
+ * only if one of its requests holds a page that compaction reads or writes;
+ * otherwise the attention runs concurrently with it (App. E.3).
+ * Asynchronous on the engine stream. */
 gp_status gp_decode_attention(gp_ctx* ctx, int32_t layer, int32_t n, const gp_request* reqs,
                               const int32_t* num_tokens, const void* q_dev, const uint8_t* first_dev,
                               float* out_dev);
@@ -353,12 +376,17 @@ gp_status gp_decode_attention(gp_ctx* ctx, int32_t layer, int32_t n, const gp_re
  * side stream wait for the work the engine stream holds at that point, then
  * returns without waiting for the compaction; the block tables and the page
  * pool are updated on the host as before.  While it runs, gp_update_summaries
- * (which touches no K/V) and the caller's work on other streams may
- * overlap it; every later engine call that reads K/V or the engine's
- * scratch (demand, compaction, inspection, gp_stats, gp_destroy) first
- * waits for it on the host.  Before reading the compacted requests' K/V,
- * the caller makes its own stream wait with gp_wait_compaction.  Waits for a
- * pending compaction first. */
+ * (which touches no K/V), gp_decode_attention of requests that share no page
+ * with it, and the caller's work on other streams may overlap it; every
+ * later engine call that reads K/V or the engine's scratch (demand,
+ * compaction, inspection, gp_stats, gp_synchronize, gp_destroy) first waits
+ * for it on the host.  Before reading the compacted requests' K/V, the
+ * caller makes its own stream wait with gp_wait_compaction.  The pages such
+ * a call releases (shared pages replaced by copy-on-write, the page Shrink
+ * returns) are back in the pool when it returns, while the side stream may
+ * still read them: a caller that writes into a page the pool hands out
+ * (gp_page_alloc, gp_grow_page) makes the writing stream wait with
+ * gp_wait_compaction first.  Waits for a pending compaction first. */
 gp_status gp_set_compaction_stream(gp_ctx* ctx, void* stream);
 /* gp_wait_compaction: `stream` (NULL: the engine stream) waits for the last
  * compaction launched on the side stream (no-op if none ever was).  It
@@ -386,11 +414,34 @@ gp_status gp_debug_entropy(gp_ctx* ctx, int32_t req_idx, double* out);
 /* Summaries of one slot: host double[L][2][Hq][d]. */
 gp_status gp_read_summaries(gp_ctx* ctx, int32_t slot, double* out);
 
+/* gp_synchronize: waits for every piece of engine work (the engine stream,
+ * the speculative selection, a side-stream compaction) and reports the
+ * device-side errors of earlier asynchronous calls: GP_ERR_TIMEOUT if only
+ * bounded waits gave up, GP_ERR_INVALID if a device-side check failed (the
+ * text names the error bits), GP_OK otherwise.  The error word is cleared. */
+gp_status gp_synchronize(gp_ctx* ctx);
+
+/* ---- test hooks -------------------------------------------------------------
+ * gp_debug_set_wait_limit: the limit, in SM clock cycles, of the bounded copy
+ * waits of later launches of `kernel` (GP_KERNEL_COMPRESS: the compaction;
+ * GP_KERNEL_SELECT: the speculative selection); 0 makes each such wait give
+ * up at once, a negative value restores the default of 2^31 (about one
+ * second).  A wait that gives up makes its CTA wait for the copies it already
+ * issued (always with the default limit), record a timeout and return;
+ * gp_synchronize then reports GP_ERR_TIMEOUT.  Other kernels:
+ * GP_ERR_UNSUPPORTED.  Host only; for tests of the timeout path.
+ * gp_debug_fail_next_launch: the next launch of `kernel` (GP_KERNEL_*) fails
+ * without running, as a failed launch would (GP_ERR_CUDA); -1 clears it.
+ * Host only; for tests of the rollback paths. */
+gp_status gp_debug_set_wait_limit(gp_ctx* ctx, int32_t kernel, int64_t cycles);
+gp_status gp_debug_fail_next_launch(gp_ctx* ctx, int32_t kernel);
+
 /* Which kernel scans the cache in gp_boundary_demand.  AUTO (default): the
- * tensor-core (tcgen05) scan for bf16 caches and requests of at most 160
- * pages, the CUDA-core (fp32 FMA) scan otherwise.  CUDA_CORE forces the
- * latter everywhere; TENSOR_CORE makes requests it cannot serve fail with
- * GP_ERR_UNSUPPORTED.  Both give the same results within the tolerances of
+ * tensor-core (tcgen05) scan for bf16 caches (every request length up to
+ * the 256-page block-table limit), the CUDA-core (fp32 FMA) scan for fp32
+ * caches or a K cache no tensor map can describe (base not 16-byte aligned,
+ * or 2^31 or more key rows).  CUDA_CORE forces the latter everywhere;
+ * TENSOR_CORE makes requests it cannot serve fail with GP_ERR_UNSUPPORTED.  Both give the same results within the tolerances of
  * fp32 arithmetic.  Host only. */
 #define GP_SCAN_AUTO 0
 #define GP_SCAN_CUDA_CORE 1

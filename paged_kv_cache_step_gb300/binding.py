@@ -42,6 +42,7 @@ EXPORTS = [
     "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
     "gp_set_scan_kernel", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
     "gp_set_compaction_stream", "gp_wait_compaction", "gp_decode_attention",
+    "gp_synchronize", "gp_debug_set_wait_limit", "gp_debug_fail_next_launch",
 ]
 
 
@@ -143,6 +144,9 @@ def load(build_if_missing: bool = True):
         "gp_set_compaction_stream": (I32, [P, P]),
         "gp_wait_compaction": (I32, [P, P]),
         "gp_decode_attention": (I32, [P, I32, I32, C.POINTER(GpRequest), P, P, P, P]),
+        "gp_synchronize": (I32, [P]),
+        "gp_debug_set_wait_limit": (I32, [P, I32, I64]),
+        "gp_debug_fail_next_launch": (I32, [P, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -406,6 +410,19 @@ def gp_kernel_time(ctx, kernel: int):
 
 def gp_reset_timing(ctx):
     _check(ctx, load().gp_reset_timing(ctx))
+
+
+def gp_synchronize(ctx):
+    """Wait for all engine work; raise on device-side errors of earlier calls."""
+    _check(ctx, load().gp_synchronize(ctx))
+
+
+def gp_debug_set_wait_limit(ctx, kernel: int, cycles: int):
+    _check(ctx, load().gp_debug_set_wait_limit(ctx, int(kernel), int(cycles)))
+
+
+def gp_debug_fail_next_launch(ctx, kernel: int):
+    _check(ctx, load().gp_debug_fail_next_launch(ctx, int(kernel)))
 
 
 def gp_stats(ctx) -> dict:

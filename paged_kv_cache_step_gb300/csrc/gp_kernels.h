@@ -94,7 +94,7 @@ struct DemandArgs {
   // work order; request work[i] owns parts [part_base[i], part_base[i+1])
   const int32_t* part_base;// [n_work + 1]
   int n_parts;
-  float2* xstat;           // per unit and part: softmax statistics [n][units][16][16]
+  float2* xstat;           // per unit and part: softmax statistics [n][units][TC_MAX_PARTS][16]
   unsigned* xcount;        // per unit: parts whose statistics are in, zero between calls
   float* scores;           // importance cache, log2 domain
   float* aval;             // a^S, a^L over C_t: per unit [2][(P-1) b]
@@ -116,7 +116,8 @@ int demand_tc_resident(int D, int G);
 
 // How a request of P pages is scanned.
 //
-// Tensor-core variant (bf16 caches, P <= TC_MAX_PAGES): a persistent
+// Tensor-core variant (bf16 caches, P <= TC_MAX_PAGES, which covers every
+// request the engine accepts, max_pages_per_req <= 256): a persistent
 // cooperative grid of one CTA per SM.  Each unit (request, layer, KV head)
 // is split into tc_parts(P) parts of balanced page ranges, at most
 // TC_MAX_PPC pages each (a CTA keeps two parts of logits in TMEM beside its
@@ -126,11 +127,11 @@ int demand_tc_resident(int D, int G);
 // the parts are listed from a rotating start, so the larger ranges of
 // uneven splits spread over the CTAs.
 //
-// CUDA-core variant (fp32 caches, or longer requests): a cluster of C CTAs
-// per unit keeps its logits in shared memory, 8 pages per CTA up to 128
-// pages, 16 beyond (P <= 256).
+// CUDA-core variant (fp32 caches, or when forced): a cluster of C CTAs per
+// unit keeps its logits in shared memory, 8 pages per CTA up to 128 pages,
+// 16 beyond (P <= 256).
 constexpr int TC_MAX_PPC = 10;
-constexpr int TC_MAX_PARTS = 16;
+constexpr int TC_MAX_PARTS = 26;  // ceil(256 / TC_MAX_PPC)
 constexpr int TC_MAX_PAGES = TC_MAX_PARTS * TC_MAX_PPC;
 __host__ __device__ inline int tc_parts(int P) { return P <= TC_MAX_PPC ? 1 : (P + TC_MAX_PPC - 1) / TC_MAX_PPC; }
 
@@ -211,7 +212,11 @@ struct CompressArgs {
   int n_work;
   unsigned long long* moved;
   int* err;
+  long long wait_limit;    // clock cycles a copy wait may take before the CTA gives up
+                           // (ERR_TIMEOUT; 0: at once); drains of copies already issued
+                           // always wait up to kDefaultWaitLimit
 };
+constexpr long long kDefaultWaitLimit = 1ll << 31;  // about one second of SM clock
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 
 }  // namespace gp

@@ -21,6 +21,7 @@
 #include <unordered_set>
 #include <vector>
 
+#include "gp_internal.h"
 #include "gp_kernels.h"
 
 namespace {
@@ -77,6 +78,7 @@ struct gp_ctx {
   int* err_dev = nullptr;          // kernel error bits
   unsigned long long* moved_dev = nullptr;
   DevBuf upload, bt2, qt, bq, scores, aval, tickets, kout, ksum, masks, xstat, attn, spec_masks, ent;
+  DevBuf upload_attn;              // decode attention's own descriptors (it may overlap a compaction)
   // speculative selection: the Eq. 10 keep masks of every request of the last
   // demand call, computed on an engine-owned stream while the host decides
   cudaStream_t sel_stream = nullptr;
@@ -94,6 +96,7 @@ struct gp_ctx {
   cudaStream_t cstream = nullptr;
   cudaEvent_t ev_ready = nullptr, ev_done = nullptr;
   bool compaction_pending = false;
+  std::unordered_set<int32_t> pending_pages;  // old and new pages of the pending compaction
 
   std::vector<DemandRec> last_demand;
   std::vector<CompressRec> last_compress;
@@ -105,6 +108,11 @@ struct gp_ctx {
   std::vector<cudaEvent_t> event_pool;
   double t_ms[GP_KERNEL_COUNT] = {};
   int64_t t_count[GP_KERNEL_COUNT] = {};
+  // test hooks: the copy-wait limit of the selection / compaction launches,
+  // and a launch to fail without running (-1: none)
+  long long wait_limit_select = gp::kDefaultWaitLimit;
+  long long wait_limit_compress = gp::kDefaultWaitLimit;
+  int inject_fail = -1;
 };
 
 namespace {
@@ -169,6 +177,10 @@ cudaEvent_t take_event(gp_ctx* c) {
 // Launch wrapper: brackets the launch with events when timing is on.
 template <typename F>
 gp_status timed_launch_on(gp_ctx* c, cudaStream_t s, int kernel, const char* name, F&& launch) {
+  if (c->inject_fail == kernel) {  // test hook: fail as a launch failure would, without running
+    c->inject_fail = -1;
+    return fail(c, GP_ERR_CUDA, "%s launch failed: injected failure (test hook)", name);
+  }
   cudaEvent_t a = nullptr, b = nullptr;
   if (c->timing) {
     a = take_event(c);
@@ -208,6 +220,7 @@ gp_status join_compaction(gp_ctx* c) {
   if (c->compaction_pending) {
     GP_CUDA(c, cudaEventSynchronize(c->ev_done));
     c->compaction_pending = false;
+    c->pending_pages.clear();
   }
   return GP_OK;
 }
@@ -218,15 +231,19 @@ gp_status need_device(gp_ctx* c) {
   return GP_OK;
 }
 
-// Read and clear the kernels' error word (synchronises the stream).
+// Read and clear the kernels' error word (synchronises the stream).  A word
+// holding only ERR_TIMEOUT (bounded waits gave up) is GP_ERR_TIMEOUT; any
+// failed device-side check makes it GP_ERR_INVALID.
 gp_status check_kernel_errors(gp_ctx* c) {
   int e = 0;
   GP_CUDA(c, cudaMemcpyAsync(&e, c->err_dev, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
   GP_CUDA(c, cudaStreamSynchronize(c->stream));
   if (e) {
     GP_CUDA(c, cudaMemsetAsync(c->err_dev, 0, sizeof(int), c->stream));
-    return fail(c, GP_ERR_INVALID,
-                "device-side check failed (bits 0x%x: 1 slot, 2 page, 4 keep mask count, 8 selection)", e);
+    GP_CUDA(c, cudaStreamSynchronize(c->stream));
+    return fail(c, gp::status_of_kernel_error(e),
+                "device-side error (bits 0x%x: 1 slot, 2 page, 4 keep mask count, 8 selection, 16 wait timed out)",
+                e);
   }
   return GP_OK;
 }
@@ -405,7 +422,7 @@ gp_status gp_destroy(gp_ctx* c) {
     if (c->ev_ready) cudaEventDestroy(c->ev_ready);
     if (c->ev_done) cudaEventDestroy(c->ev_done);
     for (DevBuf* b : {&c->upload, &c->bt2, &c->qt, &c->bq, &c->scores, &c->aval, &c->tickets, &c->kout, &c->ksum, &c->ent,
-                      &c->masks, &c->xstat, &c->attn, &c->spec_masks})
+                      &c->masks, &c->xstat, &c->attn, &c->spec_masks, &c->upload_attn})
       if (b->p) cudaFree(b->p);
     if (c->inv_freq) cudaFree(c->inv_freq);
     if (c->pool) cudaFree(c->pool);
@@ -517,6 +534,7 @@ gp_status gp_update_summaries(gp_ctx* c, int32_t n, const int32_t* slots_dev, co
 namespace {
 
 struct Staged {
+  DevBuf* dev;   // the device mirror the descriptors are uploaded to
   gp::DevReq* reqs;
   int32_t* bt;
   int32_t* bt_new;
@@ -528,8 +546,9 @@ struct Staged {
 };
 
 // Pinned layout [DevReq n][bt n*maxP][bt_new n*maxP][work n][part_base n+1],
-// mirrored in `upload`.
-gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s) {
+// mirrored in `dev` (the engine's upload buffer unless another is given).
+gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s, DevBuf* dev = nullptr) {
+  s->dev = dev ? dev : &c->upload;
   const int maxp = c->cfg.max_pages_per_req;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o += (bytes + 255) & ~size_t(255); return r; };
@@ -542,7 +561,7 @@ gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s) {
   s->bytes = o;
   gp_status st = ensure_pinned(c, o);
   if (st != GP_OK) return st;
-  st = ensure(c, c->upload, o);
+  st = ensure(c, *s->dev, o);
   if (st != GP_OK) return st;
   char* p = static_cast<char*>(c->pinned);
   s->reqs = reinterpret_cast<gp::DevReq*>(p + off_req);
@@ -555,14 +574,14 @@ gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s) {
 }
 
 gp_status upload(gp_ctx* c, const Staged& s) {
-  GP_CUDA(c, cudaMemcpyAsync(c->upload.p, c->pinned, s.bytes, cudaMemcpyHostToDevice, c->stream));
+  GP_CUDA(c, cudaMemcpyAsync(s.dev->p, c->pinned, s.bytes, cudaMemcpyHostToDevice, c->stream));
   GP_CUDA(c, cudaEventRecord(c->pinned_free, c->stream));
   return GP_OK;
 }
 
 template <typename T>
-T* dev_at(const gp_ctx* c, size_t off) {
-  return reinterpret_cast<T*>(static_cast<char*>(c->upload.p) + off);
+T* dev_at(const Staged& s, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(s.dev->p) + off);
 }
 
 }  // namespace
@@ -632,8 +651,8 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   for (int r = 0; r < n; ++r) {
     const gp::DemandPlan pl = gp::demand_plan(reqs[r].num_pages, tc);
     if (c->scan_kernel == GP_SCAN_TENSOR_CORE && pl.variant != gp::DEMAND_TC)
-      return fail(c, GP_ERR_UNSUPPORTED, "request %d: the tensor-core scan needs a bf16 cache and at most 160 pages",
-                  r);
+      return fail(c, GP_ERR_UNSUPPORTED, "request %d: the tensor-core scan needs a bf16 cache and at most %d pages",
+                  r, gp::TC_MAX_PAGES);
     if (pl.variant == gp::DEMAND_TC) {
       tc_work.push_back(r);
     } else {
@@ -682,7 +701,7 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
   pa.pool = c->pool;
   pa.q = q_cur_dev;
   pa.q_f32 = g.q_dtype == GP_DTYPE_F32;
-  pa.reqs = dev_at<gp::DevReq>(c, 0);
+  pa.reqs = dev_at<gp::DevReq>(s, 0);
   pa.n = n;
   pa.L = g.num_layers;
   pa.Hq = g.num_q_heads;
@@ -717,12 +736,12 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     da.qt = pa.qt;
     da.bq = pa.bq;
     da.reqs = pa.reqs;
-    da.bt = dev_at<int32_t>(c, s.off_bt);
-    da.work = dev_at<int32_t>(c, s.off_work) + l.first;
+    da.bt = dev_at<int32_t>(s, s.off_bt);
+    da.work = dev_at<int32_t>(s, s.off_work) + l.first;
     da.n_work = l.count;
     da.C = l.C;
     da.ppc = l.ppc;
-    da.part_base = dev_at<int32_t>(c, s.off_pb);
+    da.part_base = dev_at<int32_t>(s, s.off_pb);
     da.n_parts = n_parts;
     da.xstat = static_cast<float2*>(c->xstat.p);
     da.xcount = static_cast<unsigned*>(c->tickets.p) + (size_t)n * units;
@@ -757,15 +776,16 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     ca.fill = 0;
     ca.select_only = 1;
     ca.reqs = pa.reqs;
-    ca.old_bt = dev_at<int32_t>(c, s.off_bt);
+    ca.old_bt = dev_at<int32_t>(s, s.off_bt);
     ca.new_bt = ca.old_bt;
     ca.scores = static_cast<const float*>(c->scores.p);
     ca.keep_in = nullptr;
     ca.keep_out = static_cast<uint32_t*>(c->spec_masks.p);
-    ca.work = dev_at<int32_t>(c, s.off_sel);
+    ca.work = dev_at<int32_t>(s, s.off_sel);
     ca.n_work = n_sel;
     ca.moved = c->moved_dev;
     ca.err = c->err_dev;
+    ca.wait_limit = c->wait_limit_select;
     st = timed_launch_on(c, c->sel_stream, GP_KERNEL_SELECT, "select",
                          [&] { return gp::launch_compress(ca, c->sel_stream); });
     if (st != GP_OK) return st;
@@ -1028,16 +1048,17 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
   ca.k_loc = g.k_loc;
   ca.drop = drop;
   ca.fill = fill;
-  ca.reqs = dev_at<gp::DevReq>(c, 0);
-  ca.old_bt = dev_at<int32_t>(c, s.off_bt);
-  ca.new_bt = dev_at<int32_t>(c, s.off_bt_new);
+  ca.reqs = dev_at<gp::DevReq>(s, 0);
+  ca.old_bt = dev_at<int32_t>(s, s.off_bt);
+  ca.new_bt = dev_at<int32_t>(s, s.off_bt_new);
   ca.scores = static_cast<const float*>(c->scores.p);
   ca.keep_in = spec ? static_cast<const uint32_t*>(c->spec_masks.p) : keep_in;
   ca.keep_out = spec ? nullptr : static_cast<uint32_t*>(c->masks.p);
-  ca.work = dev_at<int32_t>(c, s.off_work);
+  ca.work = dev_at<int32_t>(s, s.off_work);
   ca.n_work = n;
   ca.moved = c->moved_dev;
   ca.err = c->err_dev;
+  ca.wait_limit = c->wait_limit_compress;
   // on the side stream (if any), after everything the engine stream holds
   cudaStream_t ks = c->stream;
   if (c->cstream) {
@@ -1050,6 +1071,12 @@ gp_status compress_common(gp_ctx* c, int32_t n, gp_request* reqs, const uint32_t
   if (st == GP_OK && c->cstream) {
     GP_CUDA(c, cudaEventRecord(c->ev_done, c->cstream));
     c->compaction_pending = true;
+    c->pending_pages.clear();
+    for (int r = 0; r < n; ++r)
+      for (int j = 0; j < reqs[r].num_pages; ++j) {
+        c->pending_pages.insert(s.bt[(size_t)r * maxp + j]);
+        c->pending_pages.insert(s.bt_new[(size_t)r * maxp + j]);
+      }
   }
   if (st != GP_OK) {
     // roll back the page allocations
@@ -1229,6 +1256,34 @@ gp_status gp_reset_timing(gp_ctx* c) {
   return GP_OK;
 }
 
+gp_status gp_synchronize(gp_ctx* c) {
+  gp_status st = need_device(c);
+  if (st != GP_OK) return st;
+  if ((st = join_compaction(c)) != GP_OK) return st;
+  if ((st = join_select(c)) != GP_OK) return st;
+  return check_kernel_errors(c);  // synchronises the engine stream
+}
+
+gp_status gp_debug_set_wait_limit(gp_ctx* c, int32_t kernel, int64_t cycles) {
+  if (!c) return GP_ERR_INVALID;
+  const long long v = cycles >= 0 ? (long long)cycles : gp::kDefaultWaitLimit;
+  if (kernel == GP_KERNEL_COMPRESS) {
+    c->wait_limit_compress = v;
+  } else if (kernel == GP_KERNEL_SELECT) {
+    c->wait_limit_select = v;
+  } else {
+    return fail(c, GP_ERR_UNSUPPORTED, "kernel %d has no settable wait limit", kernel);
+  }
+  return GP_OK;
+}
+
+gp_status gp_debug_fail_next_launch(gp_ctx* c, int32_t kernel) {
+  if (!c) return GP_ERR_INVALID;
+  if (kernel < -1 || kernel >= GP_KERNEL_COUNT) return fail(c, GP_ERR_INVALID, "unknown kernel %d", kernel);
+  c->inject_fail = kernel;
+  return GP_OK;
+}
+
 gp_status gp_stats(const gp_ctx* c, gp_stats_t* out) {
   if (!c || !out) return GP_ERR_INVALID;
   *out = c->stats;
@@ -1264,8 +1319,17 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
       return fail(c, GP_ERR_INVALID, "request %d: num_tokens %d outside [0, %d]", r, num_tokens[r],
                   reqs[r].num_pages * kPage);
   }
-  if ((st = join_compaction(c)) != GP_OK) return st;
-  if ((st = join_select(c)) != GP_OK) return st;  // it reads the upload buffer this call rewrites
+  // A compaction pending on the side stream (App. E.3) runs on: this call
+  // waits for it on the device only if one of its requests holds a page the
+  // compaction reads or writes.  The call uploads its descriptors to its own
+  // buffer, so neither the compaction nor the speculative selection, which
+  // read the engine's upload buffer, is disturbed.
+  bool overlap = false;
+  if (c->compaction_pending)
+    for (int r = 0; r < n && !overlap; ++r)
+      for (int j = 0; j < reqs[r].num_pages && !overlap; ++j)
+        overlap = c->pending_pages.count(reqs[r].block_table[j]) != 0;
+  if (overlap) GP_CUDA(c, cudaStreamWaitEvent(c->stream, c->ev_done, 0));
   const int G = g.num_q_heads / g.num_kv_heads;
   const int maxp = g.max_pages_per_req;
   const int Hkv = g.num_kv_heads;
@@ -1291,7 +1355,7 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   const size_t tick_off = (part_floats * sizeof(float) + 255) & ~size_t(255);
   if ((st = ensure(c, c->attn, tick_off + sizeof(unsigned) * (size_t)n * Hkv)) != GP_OK) return st;
   Staged s{};
-  if ((st = stage(c, n, false, &s)) != GP_OK) return st;
+  if ((st = stage(c, n, false, &s, &c->upload_attn)) != GP_OK) return st;
   s.part_base[0] = 0;
   for (int i = 0; i < n; ++i) {
     s.sel[i] = order[i];
@@ -1324,9 +1388,9 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   a.D = g.head_dim;
   a.G = G;
   a.M = g.max_slots;
-  a.reqs = dev_at<gp::DevReq>(c, 0);
-  a.bt = dev_at<int32_t>(c, s.off_bt);
-  a.ntok = dev_at<int32_t>(c, s.off_work);
+  a.reqs = dev_at<gp::DevReq>(s, 0);
+  a.bt = dev_at<int32_t>(s, s.off_bt);
+  a.ntok = dev_at<int32_t>(s, s.off_work);
   a.q = q_dev;
   a.q_f32 = g.q_dtype == GP_DTYPE_F32;
   a.first = first_dev;
@@ -1337,8 +1401,8 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   a.out = out_dev;
   a.part = reinterpret_cast<float*>(base);
   a.tickets = reinterpret_cast<unsigned*>(base + tick_off);
-  a.split_base = dev_at<int32_t>(c, s.off_pb);
-  a.order = dev_at<int32_t>(c, s.off_sel);
+  a.split_base = dev_at<int32_t>(s, s.off_pb);
+  a.order = dev_at<int32_t>(s, s.off_sel);
   a.n = n;
   a.n_ctas = (int)n_ctas;
   a.err = c->err_dev;
@@ -1369,11 +1433,22 @@ gp_status gp_wait_compaction(gp_ctx* c, void* stream) {
 
 // ---- read-only view for other translation units (gp_internal.h) ------------
 
-#include "gp_internal.h"
-
 namespace gp {
 
 gp_status ctx_join_compaction(gp_ctx* c) { return c ? join_compaction(c) : GP_ERR_INVALID; }
+
+gp_status ctx_join_select(gp_ctx* c) { return c ? join_select(c) : GP_ERR_INVALID; }
+
+gp_status status_of_kernel_error(int bits) {
+  if (bits == 0) return GP_OK;
+  return (bits & ~ERR_TIMEOUT) == 0 ? GP_ERR_TIMEOUT : GP_ERR_INVALID;
+}
+
+void ctx_forget_demand(gp_ctx* c, int slot) {
+  if (!c) return;
+  for (auto& d : c->last_demand)
+    if (d.slot == slot) d.slot = -1;
+}
 
 bool ctx_view(const gp_ctx* c, CtxView* out) {
   if (!c || !out) return false;

@@ -45,7 +45,9 @@ constexpr int MAX_WORDS = 256 * PAGE / 32;  // 256 pages
 #endif
 constexpr int CSTAGES = GP_CMP_STAGES;
 constexpr int STAGE_BYTES = 32 * 1024;      // K and V rows of one chunk
-constexpr long long kWaitLimit = 1ll << 31;  // clock cycles (about one second)
+// Drains (waits for copies already issued, before the CTA's shared memory
+// goes away) always use the full limit, whatever a.wait_limit says.
+constexpr long long kDrainLimit = kDefaultWaitLimit;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -59,12 +61,32 @@ __device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for a phase of an mbarrier; false when the limit passed.
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool bar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for a phase of an mbarrier; false when `limit` clock cycles
+// passed first.  try_wait may suspend the thread for a while by itself, so a
+// limit far below the default polls with the non-blocking test_wait instead,
+// checking the clock first: then the limit alone decides when the wait gives
+// up, and a limit of 0 gives up at once.
+constexpr long long kPollBelow = 1ll << 20;
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, long long limit) {
+  if (limit < kPollBelow) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < limit)
+      if (bar_test(bar, parity)) return true;
+    return false;
+  }
   if (bar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (!bar_try(bar, parity))
-    if (clock64() - t0 > kWaitLimit) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
 }
 
@@ -159,7 +181,7 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
   __shared__ int s_fast;                  // the selection's fast path applied
   __shared__ int s_nholes;
   __shared__ unsigned s_sel[4];           // prefix, mask, above, flags
-  __shared__ int s_abort;
+  __shared__ int s_abort;                 // 1: a wait gave up; 2: the keep count is wrong
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int units = a.L * a.Hkv;
@@ -208,7 +230,7 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
                      "l"(sc), "r"((uint32_t)(ncmp * 4)), "r"(bar)
                      : "memory");
       }
-      if (!bar_wait(bar, 0u)) atomicOr(&s_abort, 1);
+      if (!bar_wait(bar, 0u, a.wait_limit)) atomicOr(&s_abort, 1);
       sc = reinterpret_cast<const float*>(stage_mem);
       // phase 0 of stage 0's barrier is used: the compaction starts at phase 1
       if (tid == 0) s_stage0 = 1;
@@ -421,8 +443,10 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
     if (tid == 0) {
       unsigned tot = 0;
       for (int w = 0; w < NWARP; ++w) tot += red[w];
-      if (tot != target_kept) {
-        s_abort = 1;
+      if (s_abort) {
+        atomicOr(a.err, ERR_TIMEOUT);  // the selection ran on scores still being staged
+      } else if (tot != target_kept) {
+        s_abort = 2;
         atomicOr(a.err, a.keep_in ? ERR_BAD_MASK : ERR_BAD_COUNT);
       }
     }
@@ -434,7 +458,7 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
   }
   if (s_abort) {
     // a staging copy of the scores may still be in flight (bounded wait)
-    if (tid == 0 && s_stage0) bar_wait(smem_addr(&full_bar[0]), 0u);
+    if (tid == 0 && s_stage0) bar_wait(smem_addr(&full_bar[0]), 0u, kDrainLimit);
     __syncthreads();
     return;
   }
@@ -547,7 +571,7 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
   int done = 0;  // chunks consumed
   for (int k = 0; k < nlist; ++k) {
     const int st = k % CSTAGES;
-    if (!bar_wait(smem_addr(&full_bar[st]), phase(k))) atomicOr(&s_abort, 1);
+    if (!bar_wait(smem_addr(&full_bar[st]), phase(k), a.wait_limit)) atomicOr(&s_abort, 1);
     __syncthreads();
     if (s_abort) break;  // every thread reads it after the barrier: all leave together
     const int c = (int)list[k];
@@ -580,7 +604,7 @@ __global__ void __launch_bounds__(NT, 1) k_compress(CompressArgs a) {
     if (tid == 0) {
       atomicOr(a.err, ERR_TIMEOUT);
       for (int k = done; k < nlist && k < done + CSTAGES; ++k)
-        bar_wait(smem_addr(&full_bar[k % CSTAGES]), phase(k));
+        bar_wait(smem_addr(&full_bar[k % CSTAGES]), phase(k), kDrainLimit);
     }
     __syncthreads();
   }
@@ -606,7 +630,7 @@ cudaError_t launch_rb(const CompressArgs& a, cudaStream_t s) {
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
   if (a.n_work == 0) return cudaSuccess;
-  if (a.b != PAGE) return cudaErrorInvalidValue;
+  if (a.b != PAGE || a.wait_limit < 0) return cudaErrorInvalidValue;
   switch (a.D * a.elt) {
     case 128: return launch_rb<128>(a, s);
     case 256: return launch_rb<256>(a, s);

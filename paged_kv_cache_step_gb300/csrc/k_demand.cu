@@ -1,7 +1,8 @@
 // Boundary demand kernel, CUDA-core variant (fp32 FMA): GrowPage Sec. 3.2
 // Eqs. 2, 7 and App. E.1, plus the Eq. 9 importance cached for Compress &
-// Hold.  It serves fp32 caches and requests longer than 160 pages; bf16
-// caches up to 160 pages take the tcgen05 variant (k_demand_tc.cu).
+// Hold.  It serves fp32 caches (and bf16 ones when forced, or when the K
+// cache cannot be described by a tensor map); bf16 caches otherwise take the
+// tcgen05 variant (k_demand_tc.cu).
 //
 // Work unit: one (request, layer, KV head), owned by a cluster of C CTAs;
 // CTA c scores the balanced page range [c P / C, (c+1) P / C) (at most ppc

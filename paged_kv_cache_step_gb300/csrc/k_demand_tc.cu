@@ -1,6 +1,6 @@
 // Boundary demand kernel, tensor-core variant (tcgen05, sm_103a): GrowPage
 // Sec. 3.2 Eqs. 2, 7 and App. E.1, plus the Eq. 9 importance cached for
-// Compress & Hold, for bf16 caches and requests of at most 160 pages.
+// Compress & Hold, for bf16 caches and requests of up to 256 pages.
 //
 // Why the tensor core on an HBM-bound scan: each key meets 2G = 8 summary
 // rows, 2 * 8 * d flops per 2 d bytes of K.  On CUDA cores that is 8 FMAs
@@ -283,8 +283,9 @@ struct TcSmem {
   using T = TcCfg<D, ROWS>;
   static constexpr size_t STAGE = 0;
   static constexpr size_t BQ = STAGE + (size_t)T::NSTAGE * T::TILE_BYTES;  // 2 buffers
-  static constexpr size_t XG = BQ + 2 * (size_t)T::BQ_BYTES;               // XStat [2][16][16]
-  static constexpr size_t BARS = XG + sizeof(XStat) * 2 * 16 * 16;
+  static constexpr size_t XG = BQ + 2 * (size_t)T::BQ_BYTES;               // XStat [32 parts][16]
+  static_assert(TC_MAX_PARTS <= 32, "merge buffer");
+  static constexpr size_t BARS = XG + sizeof(XStat) * 32 * 16;
   // full[NSTAGE], empty[NSTAGE], bqfull[2], bqempty[2], mmadone, sel, ready[W], wfree[W]
   static constexpr int NBARS = 2 * T::NSTAGE + 6 + 2 * T::WSLOTS;
   static constexpr size_t PART = BARS + 8 * (size_t)NBARS;                 // [EPI_NW][16] XStat

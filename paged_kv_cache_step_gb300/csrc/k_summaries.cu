@@ -2,9 +2,11 @@
 //
 //  k_ema_update  -- GrowPage Sec. 3.2 Eq. 6 with the App. E.1 first-step
 //                   initialisation, in place on the fp64 summary pool
-//                   [L][M][2][Hq][D] (App. E.1 Eq. 11).  Pure streaming: one
-//                   thread per 4 elements, 16-byte loads/stores; 34 bytes of
-//                   HBM traffic per element for bf16 queries.
+//                   [L][M][2][Hq][D] (App. E.1 Eq. 11).  Pure streaming: a
+//                   block per (1024-element chunk, request, layer), whose
+//                   queries and two summary rows are contiguous; one thread
+//                   per 4 elements, 16-byte loads/stores; 34 bytes of HBM
+//                   traffic per element for bf16 queries.
 //  k_prep_queries -- App. E.1 Eq. 12 calibration gamma = RMS(q_t)/RMS(qbar)
 //                   and rotate-half RoPE at the current position, for the
 //                   requests at a capacity boundary, pre-scaled by
@@ -13,66 +15,123 @@
 //                   the tensor-core operand layout.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "gp_kernels.h"
 
 namespace gp {
 namespace {
 
-__device__ __forceinline__ void load4(const void* q, int q_f32, size_t idx, double v[4]) {
-  if (q_f32) {
-    const float4 t = *reinterpret_cast<const float4*>(static_cast<const float*>(q) + idx);
-    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-  } else {
-    const uint2 t = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(q) + idx);
-    v[0] = __uint_as_float(t.x << 16);
-    v[1] = __uint_as_float(t.x & 0xffff0000u);
-    v[2] = __uint_as_float(t.y << 16);
-    v[3] = __uint_as_float(t.y & 0xffff0000u);
-  }
+// Exact float -> double by integer operations (a normal or zero float: the
+// exponent is rebased and the fraction moved up); other inputs take the
+// ordinary conversion.  Keeps the widening of the queries off GB300's narrow
+// fp64 pipe, which the two fused multiply-adds per summary element already use.
+__device__ __forceinline__ double widen_exact(float f) {
+  const unsigned u = __float_as_uint(f);
+  const unsigned e = (u >> 23) & 0xffu;
+  if ((u & 0x7fffffffu) == 0u) return __hiloint2double((int)(u & 0x80000000u), 0);
+  if (e == 0u || e == 0xffu) return (double)f;
+  const unsigned hi = (u & 0x80000000u) | ((e + 896u) << 20) | ((u & 0x7fffffu) >> 3);
+  return __hiloint2double((int)hi, (int)((u & 7u) << 29));
 }
 
-__global__ void __launch_bounds__(256) k_ema_update(EmaArgs a) {
-  const int dq = a.D / 4;
-  const size_t total = (size_t)a.L * a.n * a.Hq * dq;
-  const size_t hd = (size_t)a.Hq * a.D;
-  const double ws = 1.0 - a.beta_s, wl = 1.0 - a.beta_l;
-  for (size_t it = (size_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += (size_t)gridDim.x * blockDim.x) {
-    const int d4 = (int)(it % dq);
-    size_t rest = it / dq;
-    const int g = (int)(rest % a.Hq);
-    rest /= a.Hq;
-    const int r = (int)(rest % a.n);
-    const int l = (int)(rest / a.n);
-    const int slot = a.slots[r];
-    if (slot < 0 || slot >= a.M) {
-      if (d4 == 0 && g == 0 && l == 0) atomicOr(a.err, ERR_BAD_SLOT);
-      continue;
-    }
-    double q[4];
-    load4(a.q, a.q_f32, (((size_t)l * a.n + r) * a.Hq + g) * a.D + d4 * 4, q);
-    double2* row_s = reinterpret_cast<double2*>(
-        a.pool + (((size_t)l * a.M + slot) * 2 + 0) * hd + (size_t)g * a.D + d4 * 4);
-    double2* row_l = reinterpret_cast<double2*>(reinterpret_cast<double*>(row_s) + hd);
-    double2 s0, s1, l0, l1;
-    if (a.first[r]) {
-      s0 = make_double2(q[0], q[1]);
-      s1 = make_double2(q[2], q[3]);
-      l0 = s0;
-      l1 = s1;
-    } else {
-      const double2 os0 = row_s[0], os1 = row_s[1];
-      const double2 ol0 = row_l[0], ol1 = row_l[1];
-      s0 = make_double2(fma(a.beta_s, os0.x, ws * q[0]), fma(a.beta_s, os0.y, ws * q[1]));
-      s1 = make_double2(fma(a.beta_s, os1.x, ws * q[2]), fma(a.beta_s, os1.y, ws * q[3]));
-      l0 = make_double2(fma(a.beta_l, ol0.x, wl * q[0]), fma(a.beta_l, ol0.y, wl * q[1]));
-      l1 = make_double2(fma(a.beta_l, ol1.x, wl * q[2]), fma(a.beta_l, ol1.y, wl * q[3]));
-    }
-    row_s[0] = s0;
-    row_s[1] = s1;
-    row_l[0] = l0;
-    row_l[1] = l1;
+// The fp64 product w q of a weight w = mw 2^(ew - 1075) (mw its 53-bit
+// integer significand, 0 < w) and a bf16 query with bit pattern qb, by
+// integer operations: the significands' product has 60 or 61 bits and is
+// rounded to 53 (to nearest, ties to even), which is exactly what the fp64
+// multiply returns.  GB300 issues fp64 arithmetic at a small fraction of its
+// integer rate, and the EMA would otherwise spend four fp64 operations per
+// element; this leaves the two fused multiply-adds.  False (and the caller
+// multiplies in fp64) for a subnormal, infinite or NaN q, or a product
+// outside the normal range.
+__device__ __forceinline__ bool mul_w_bf16(unsigned long long mw, int ew, unsigned qb, double& out) {
+  const unsigned eq = (qb >> 7) & 0xffu, sq = (qb >> 15) & 1u;
+  if (eq == 0u) {
+    if ((qb & 0x7fu) != 0u) return false;
+    out = __hiloint2double((int)(sq << 31), 0);  // +-0 (w > 0)
+    return true;
   }
+  if (eq == 0xffu) return false;
+  const unsigned long long p = mw * (unsigned long long)(0x80u | (qb & 0x7fu));  // [2^59, 2^61)
+  int sh = (p >> 60) != 0ull ? 8 : 7;
+  unsigned long long m = p >> sh;
+  const unsigned long long rem = p & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
+  if (rem > half || (rem == half && (m & 1ull))) {
+    ++m;
+    if (m == (1ull << 53)) {
+      m >>= 1;
+      ++sh;
+    }
+  }
+  // value = m 2^(ew - 1075 + eq - 134 + sh); biased exponent of m 2^k with m in [2^52, 2^53)
+  const int be = ew + (int)eq - 134 + sh;
+  if (be < 1 || be > 2046) return false;
+  const unsigned long long bits = ((unsigned long long)sq << 63) | ((unsigned long long)be << 52) |
+                                  (m & ((1ull << 52) - 1ull));
+  out = __longlong_as_double((long long)bits);
+  return true;
+}
+
+// grid (ceil(Hq D / 1024), n, L), 256 threads: thread t of block (c, r, l)
+// owns elements [4 (256 c + t), +4) of the (layer l, request r) row.
+// (mws, ews), (mwl, ewl): 1 - beta_s and 1 - beta_l as significand and
+// biased exponent, for mul_w_bf16.
+__global__ void __launch_bounds__(256) k_ema_update(EmaArgs a, unsigned long long mws, int ews,
+                                                    unsigned long long mwl, int ewl) {
+  const int r = blockIdx.y, l = blockIdx.z;
+  const int row = a.Hq * a.D;
+  const int e0 = (blockIdx.x * 256 + threadIdx.x) * 4;
+  const int slot = a.slots[r];
+  if (slot < 0 || slot >= a.M) {
+    if (blockIdx.x == 0 && l == 0 && threadIdx.x == 0) atomicOr(a.err, ERR_BAD_SLOT);
+    return;
+  }
+  if (e0 >= row) return;
+  const size_t qi = ((size_t)l * a.n + r) * row + e0;
+  float qf[4];
+  unsigned qb[4] = {0u, 0u, 0u, 0u};  // bf16 bit patterns
+  if (a.q_f32) {
+    const float4 t = *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + qi);
+    qf[0] = t.x; qf[1] = t.y; qf[2] = t.z; qf[3] = t.w;
+  } else {
+    const uint2 t = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.q) + qi);
+    qb[0] = t.x & 0xffffu;
+    qb[1] = t.x >> 16;
+    qb[2] = t.y & 0xffffu;
+    qb[3] = t.y >> 16;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) qf[i] = __uint_as_float(qb[i] << 16);
+  }
+  double q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = widen_exact(qf[i]);
+  double2* row_s = reinterpret_cast<double2*>(a.pool + ((size_t)l * a.M + slot) * 2 * row + e0);
+  double2* row_l = reinterpret_cast<double2*>(reinterpret_cast<double*>(row_s) + row);
+  double2 s0, s1, l0, l1;
+  if (a.first[r]) {
+    s0 = make_double2(q[0], q[1]);
+    s1 = make_double2(q[2], q[3]);
+    l0 = s0;
+    l1 = s1;
+  } else {
+    const double ws = 1.0 - a.beta_s, wl = 1.0 - a.beta_l;
+    const double2 os0 = __ldcs(row_s), os1 = __ldcs(row_s + 1);
+    const double2 ol0 = __ldcs(row_l), ol1 = __ldcs(row_l + 1);
+    double cs[4], cl[4];  // (1 - beta) q, rounded once as an fp64 multiply would
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (a.q_f32 || !mul_w_bf16(mws, ews, qb[i], cs[i])) cs[i] = ws * q[i];
+      if (a.q_f32 || !mul_w_bf16(mwl, ewl, qb[i], cl[i])) cl[i] = wl * q[i];
+    }
+    s0 = make_double2(fma(a.beta_s, os0.x, cs[0]), fma(a.beta_s, os0.y, cs[1]));
+    s1 = make_double2(fma(a.beta_s, os1.x, cs[2]), fma(a.beta_s, os1.y, cs[3]));
+    l0 = make_double2(fma(a.beta_l, ol0.x, cl[0]), fma(a.beta_l, ol0.y, cl[1]));
+    l1 = make_double2(fma(a.beta_l, ol1.x, cl[2]), fma(a.beta_l, ol1.y, cl[3]));
+  }
+  __stcs(row_s, s0);
+  __stcs(row_s + 1, s1);
+  __stcs(row_l, l0);
+  __stcs(row_l + 1, l1);
 }
 
 // Block per (request, layer, 8 query heads); warp per query head.  The
@@ -190,11 +249,22 @@ __global__ void __launch_bounds__(256) k_prep_queries(PrepArgs a) {
 }  // namespace
 
 cudaError_t launch_ema(const EmaArgs& a, cudaStream_t s) {
-  const size_t total = (size_t)a.L * a.n * a.Hq * (a.D / 4);
-  if (total == 0) return cudaSuccess;
-  int blocks = (int)((total + 255) / 256);
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  k_ema_update<<<blocks, 256, 0, s>>>(a);
+  if (a.n == 0 || a.L == 0) return cudaSuccess;
+  if (a.D % 4 != 0 || a.n > 65535 || a.L > 65535) return cudaErrorInvalidValue;
+  const int row = a.Hq * a.D;
+  // 1 - beta as significand and biased exponent (0 < 1 - beta <= 1: normal)
+  auto split = [](double w, unsigned long long& m, int& e) {
+    unsigned long long b;
+    std::memcpy(&b, &w, sizeof(b));
+    e = (int)((b >> 52) & 0x7ffull);
+    m = (b & ((1ull << 52) - 1ull)) | (1ull << 52);
+  };
+  unsigned long long mws, mwl;
+  int ews, ewl;
+  split(1.0 - a.beta_s, mws, ews);
+  split(1.0 - a.beta_l, mwl, ewl);
+  if (ews == 0 || ewl == 0) return cudaErrorInvalidValue;
+  k_ema_update<<<dim3((row + 1023) / 1024, a.n, a.L), 256, 0, s>>>(a, mws, ews, mwl, ewl);
   return cudaGetLastError();
 }
 

@@ -77,7 +77,8 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   if (v.host_only) return fail(c, GP_ERR_STATE, "host-only context has no device caches");
   const gp_config& g = *v.cfg;
   if (n < 0 || n > g.max_slots || n > GP_NOALLOC_MAX_REQ)
-    return fail(c, GP_ERR_INVALID, "n = %lld outside [0, %lld]", n, GP_NOALLOC_MAX_REQ);
+    return fail(c, GP_ERR_INVALID, "n = %lld outside [0, %lld]", n,
+                g.max_slots < GP_NOALLOC_MAX_REQ ? g.max_slots : GP_NOALLOC_MAX_REQ);
   if (n == 0) return GP_OK;
   if (!reqs || !out || !q_cur_dev) return fail(c, GP_ERR_INVALID, "null argument");
   if (g.demand_metric != GP_METRIC_TOP_P)
@@ -114,8 +115,11 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   }
 
   {
-    // a compaction still running on a side stream writes K/V this call reads
-    const gp_status js = gp::ctx_join_compaction(c);
+    // a compaction still running on a side stream writes K/V this call reads;
+    // a speculative selection of an earlier gp_boundary_demand may still write
+    // the kernel error word this call reads and clears
+    gp_status js = gp::ctx_join_compaction(c);
+    if (js == GP_OK) js = gp::ctx_join_select(c);
     if (js != GP_OK) return js;
   }
 
@@ -134,16 +138,22 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   const size_t off_kout = o;  o = align256(o + sizeof(int32_t) * (size_t)n * units * 2);
   const size_t off_ksum = o;  o = align256(o + sizeof(unsigned long long) * (size_t)n * 2);
   const size_t off_tk = o;    o = align256(o + sizeof(unsigned) * 2 * (size_t)n * units);  // tickets, counts
-  // one float region: per request its importance values, then its a-values
+  // one float region: per request its importance values, then its a-values,
+  // each starting on a 256-byte boundary (the D_p select reads a unit's
+  // a-values with 16-byte loads and bulk copies; every unit's a-values span a
+  // multiple of 256 floats, so aligning the request's start aligns them all)
   const size_t off_sc = o;
   for (int r = 0; r < n; ++r) {
     g_reqs[r].num_pages = reqs[r].num_pages;
     g_reqs[r].slot = reqs[r].slot;
     g_reqs[r].pos = reqs[r].pos;
     g_reqs[r].score_off = (int64_t)((o - off_sc) / sizeof(float));
-    o += sizeof(float) * (size_t)units * (reqs[r].num_pages * kPage - g.recent_window);
+    o = align256(o + sizeof(float) * (size_t)units * (reqs[r].num_pages * kPage - g.recent_window));
     g_reqs[r].aval_off = (int64_t)((o - off_sc) / sizeof(float));
-    o += sizeof(float) * (size_t)units * 2 * (reqs[r].num_pages - 1) * kPage;
+    if ((g_reqs[r].aval_off * sizeof(float)) % 16 != 0)
+      return fail(c, GP_ERR_INVALID, "request %lld: a-value offset %lld is not 16-byte aligned", r,
+                  g_reqs[r].aval_off);
+    o = align256(o + sizeof(float) * (size_t)units * 2 * (reqs[r].num_pages - 1) * kPage);
     g_reqs[r].mask_off = 0;
     g_reqs[r].bt_off = r * maxp;
     g_reqs[r].pad = 0;
@@ -291,9 +301,16 @@ gp_status gp_boundary_demand_noalloc(gp_ctx* c, int32_t n, const gp_request* req
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(c, "result copy", e);
   if (kerr) {
-    cudaMemsetAsync(v.err_dev, 0, sizeof(int), s);
-    return fail(c, GP_ERR_INVALID, "device-side check failed (bits 0x%llx)", kerr);
+    e = cudaMemsetAsync(v.err_dev, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(c, "error word reset", e);
+    return fail(c, gp::status_of_kernel_error(kerr),
+                "device-side error (bits 0x%llx: 1 slot, 2 page, 16 wait timed out)", kerr);
   }
+  // the allocating entry point's importance cache for these slots now
+  // predates their current queries: a Compress & Hold needs a new
+  // gp_boundary_demand (GP_ERR_STATE until then)
+  for (int r = 0; r < n; ++r) gp::ctx_forget_demand(c, reqs[r].slot);
   for (int r = 0; r < n; ++r) {
     const int P = reqs[r].num_pages;
     out[r].sum_k_short = (int64_t)g_sums[2 * r];

@@ -4,7 +4,9 @@ Two engines over identical synthetic caches run the same boundary event:
 one compacts on its own stream, the other on a side stream while summary
 updates of the next decode steps are issued on the engine stream.  After
 gp_wait_compaction the K/V caches, the block tables, the page pool, the
-keep masks and a following demand call must be identical.
+keep masks and a following demand call must be identical.  A side-stream
+compaction of two requests sharing a prefix is also checked against the
+oracle (copy-on-write plans, keep masks, gathered bytes).
 """
 
 import numpy as np
@@ -71,3 +73,80 @@ def test_side_stream_compaction_matches_engine_stream(call):
     finally:
         ra.close()
         rb.close()
+
+
+def test_side_stream_compaction_with_a_shared_prefix_matches_oracle():
+    """Both holders of a shared two-page prefix compressed in one side-stream
+    call, against the oracle: copy-on-write plans taken with the refcounts at
+    the start of the call (App. E.2; every co-sharer of the call copies, and
+    the originals are freed once both dropped them), the Eq. 10 keep masks,
+    and the K/V bytes of the oracle's gather under the new tables."""
+    import oracle.growpage as og
+    w = synth.make_workload("custom", device="cuda", shape=SHAPE, sizes=[4, 3], seed_xor=41)
+    t0, t1 = w.block_tables
+    w.block_tables[1] = [t0[0], t0[1]] + t1
+    w.positions[1] = len(w.block_tables[1]) * 256
+    cfg = hz.engine_config(w)
+    ctx = gp.gp_create(cfg, w.k_cache, w.v_cache, None)
+    side = torch.cuda.Stream()
+    try:
+        for _ in range(w.num_pages):
+            gp.gp_page_alloc(ctx)
+        used = set(t0) | set(w.block_tables[1])
+        for pg in range(w.num_pages):
+            if pg not in used:
+                gp.gp_page_unref(ctx, pg)
+        gp.gp_page_ref(ctx, t0[0])
+        gp.gp_page_ref(ctx, t0[1])
+        reqs = [gp.Request(gp.gp_slot_acquire(ctx), w.block_tables[r], w.positions[r], cfg.max_pages_per_req)
+                for r in range(2)]
+        slots = torch.tensor([q.slot for q in reqs], dtype=torch.int32, device="cuda")
+        first, nfirst = torch.ones(2, dtype=torch.uint8, device="cuda"), torch.zeros(2, dtype=torch.uint8, device="cuda")
+        for t, q in enumerate(w.history):
+            gp.gp_update_summaries(ctx, 2, slots, q.contiguous(), first if t == 0 else nfirst)
+        gp.gp_set_compaction_stream(ctx, side)
+        q = w.history[-1]
+        sh = w.shape
+        units = sh.num_layers * sh.num_kv_heads
+        # the oracle's selection inputs, from the keys before the compaction
+        oracle_units = []
+        for r, req in enumerate(reqs):
+            s, l = hz.oracle_summaries(w.history, r)
+            qt = og.summary_queries(s, l, q[:, r].double().cpu().numpy(), req.pos, sh.rope_theta)
+            oracle_units.append([hz.oracle_unit_dev(qt, w.k_cache, req.pages, u // sh.num_kv_heads,
+                                                    u % sh.num_kv_heads, sh.group) for u in range(units)])
+        pool = og.PagePool(w.num_pages, [gp.gp_page_refcount(ctx, pg) for pg in range(w.num_pages)])
+        old = [list(r.pages) for r in reqs]
+        plans = [og.cow_plan(t, pool) for t in old]          # refcounts as at the start of the call
+        for _, replaced in plans:
+            og.release_replaced(replaced, pool)
+        pre_k, pre_v = w.k_cache.double().cpu().numpy(), w.v_cache.double().cpu().numpy()
+        gp.gp_boundary_demand(ctx, reqs, q)
+        gp.gp_compress_hold(ctx, reqs)
+        for t in range(3):                                   # decode steps while the side stream compacts
+            gp.gp_update_summaries(ctx, 2, slots, synth.query_step(w, [True, False]), nfirst)
+        gp.gp_wait_compaction(ctx, torch.cuda.current_stream())
+        gp.gp_synchronize(ctx)
+        torch.cuda.synchronize()
+        assert [r.pages for r in reqs] == [p for p, _ in plans]
+        assert [gp.gp_page_refcount(ctx, pg) for pg in range(w.num_pages)] == pool.refcount
+        assert gp.gp_page_refcount(ctx, t0[0]) == 0 and gp.gp_page_refcount(ctx, t0[1]) == 0
+        ek, ev = pre_k, pre_v
+        for r, req in enumerate(reqs):
+            P = req.num_pages
+            keep = gp.unpack_mask(gp.gp_debug_keep_mask(ctx, r, units, P), P * 256)
+            for u in range(units):
+                ok, _, msg = hz.topk_ok(keep[u], oracle_units[r][u].s, P)
+                assert ok, f"request {r} unit {u}: {msg}"
+            ek, ev = og.compress_cache(ek, ev, old[r], req.pages,
+                                       keep.reshape(sh.num_layers, sh.num_kv_heads, -1), 256)
+        got_k, got_v = w.k_cache.double().cpu().numpy(), w.v_cache.double().cpu().numpy()
+        for req in reqs:
+            n_live = (req.num_pages - 1) * 256
+            for layer in range(sh.num_layers):
+                for h in range(sh.num_kv_heads):
+                    for exp, got in ((ek, got_k), (ev, got_v)):
+                        assert np.array_equal(og.gather_logical(exp, req.pages, layer, h)[:n_live],
+                                              og.gather_logical(got, req.pages, layer, h)[:n_live])
+    finally:
+        gp.gp_destroy(ctx)

@@ -3,8 +3,8 @@
 Small model shapes (2 layers, 2 KV heads) that reach every kernel variant:
 bf16 caches with head_dim 64 / 128 and GQA group 2 / 4 (the tensor-core scan
 and, when forced, the CUDA-core scan), an fp32 cache (CUDA-core only), and
-requests of 1, 2, 5, 33, 64, 65, 128, 129, 160 pages (tensor-core range,
-every cluster shape) and 161, 256 pages (beyond it: the CUDA-core scan, the
+requests of 1, 2, 5, 33, 64, 65, 128, 129, 160, 161 and 256 pages (one to
+26 tensor-core parts per unit, every cluster shape of the CUDA-core scan, the
 largest block table).  Against the fp64 oracle: D_p within the tie
 tolerance, the demand distributions within 1e-4, the importance, the
 decision (forced Grow at P = 1), the Eq. 10 keep masks and the compacted
@@ -104,6 +104,15 @@ def test_demand_decide_compress_all_sizes(shape_name):
                 assert dem[r].sum_k_long == int(ks[:, 1].sum())
                 out.append((res, ties, ks))
             per_kind[kind] = out
+        # bf16: the tensor-core scan serves every size up to the 256-page
+        # block-table limit (161 and 256 pages included) -- forcing it must not
+        # be refused, and it is the scan AUTO ran
+        if shape.kv_dtype == "bf16":
+            gp.gp_set_scan_kernel(run.ctx, gp.GP_SCAN_TENSOR_CORE)
+            gp.gp_boundary_demand(run.ctx, run.reqs, q)
+            for r in range(w.n):
+                assert np.array_equal(gp.gp_debug_demand_k(run.ctx, r, run.units), per_kind[gp.GP_SCAN_AUTO][r][2]), \
+                    f"request {r} (P={run.reqs[r].num_pages}): forced tensor-core scan differs from AUTO"
         # the two scans agree exactly where no oracle tie decides
         if len(per_kind) == 2:
             for r in range(w.n):
@@ -116,16 +125,20 @@ def test_demand_decide_compress_all_sizes(shape_name):
         acts = gp.gp_decide(run.ctx, run.reqs, dem)
         free = gp.gp_free_page_count(run.ctx)
         granted = 0
+        ks_last = [gp.gp_debug_demand_k(run.ctx, r, run.units) for r in range(w.n)]
         for r in range(w.n):
-            res, ties, _ = per_kind[gp.GP_SCAN_AUTO][r]
+            res, _, _ = per_kind[gp.GP_SCAN_AUTO][r]
             P = run.reqs[r].num_pages
             kk = np.array([res[i].k for i in range(run.units)])
-            delta = og.demand_trend(kk[:, 0], kk[:, 1], (P - 1) * PAGE) if P > 1 else 0.0
-            ref = og.decide(delta, P, free - granted, 0, 0.0)
-            if ref.kind == og.GROW and not ref.forced:
+            for idx in range(run.units):
+                for x in range(2):
+                    if P > 1:
+                        ok, msg = hz.dp_ok(int(ks_last[r][idx, x]), res[idx].a_dem[x], 0.99)
+                        assert ok, f"P={P} unit {idx} x {x}: {msg}"
+            ok, msg = hz.decision_ok(acts[r], kk, ks_last[r], P, free - granted)
+            assert ok, f"request {r} (P={P}): {msg}"
+            if acts[r].kind == gp.GP_ACT_GROW and not acts[r].forced:
                 granted += 1
-            if ties == 0:
-                assert acts[r].kind == ref.kind, f"request {r} (P={P})"
             if P == 1:
                 assert acts[r].kind == gp.GP_ACT_GROW and acts[r].forced
         # Compress & Hold on every request with two or more pages
