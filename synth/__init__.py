@@ -15,4 +15,6 @@ from .workloads import (  # noqa: F401
     make_workload,
     query_step,
     fill_page,
+    fill_pages,
+    batch_kinds,
 )

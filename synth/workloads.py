@@ -148,10 +148,15 @@ def _unit_rms(x: torch.Tensor) -> torch.Tensor:
 
 
 def _random_cache(shape: ModelShape, num_pages: int, page_size: int, gen,
-                  device) -> torch.Tensor:
+                  device, extra_pages: int = 0) -> torch.Tensor:
+    """[L][num_pages + extra_pages][Hkv][b][d]: the first num_pages pages
+    drawn N(0, 1) (the same draws whatever extra_pages is), the extra pages
+    zero (a free reserve that the caller fills before reading)."""
     dt = TORCH_DTYPE[shape.kv_dtype]
-    out = torch.empty(shape.num_layers, num_pages, shape.num_kv_heads,
+    out = torch.empty(shape.num_layers, num_pages + extra_pages, shape.num_kv_heads,
                       page_size, shape.head_dim, dtype=dt, device=device)
+    if extra_pages:
+        out[:, num_pages:].zero_()
     for layer in range(shape.num_layers):
         # chunk over pages to bound temporaries
         step = max(1, (1 << 28) // (shape.num_kv_heads * page_size * shape.head_dim))
@@ -292,7 +297,7 @@ def _llama_single(device, num_pages: int = 64, P: int = 32, **_):
 
 
 def _batch(device, name="batch64", shape=LLAMA8B, n=64, p_lo=4, p_hi=128,
-           spare_per_req=2, conc_prob=None, sizes=None, seed_xor=0, **_):
+           spare_per_req=2, conc_prob=None, sizes=None, seed_xor=0, extra_pages=0, **_):
     sh = shape
     b = 256
     gen, hgen = _gens(device, config_seed(name) ^ seed_xor)
@@ -307,8 +312,9 @@ def _batch(device, name="batch64", shape=LLAMA8B, n=64, p_lo=4, p_hi=128,
     for s in sizes:
         bts.append(perm[off:off + s])
         off += s
-    k = _random_cache(sh, num_pages, b, gen, device)
-    v = _random_cache(sh, num_pages, b, gen, device)
+    k = _random_cache(sh, num_pages, b, gen, device, extra_pages)
+    v = _random_cache(sh, num_pages, b, gen, device, extra_pages)
+    num_pages += extra_pages
     u = low_freq_directions((n, sh.num_layers, sh.num_kv_heads), sh.head_dim,
                             gen, device)
     if conc_prob is None:
@@ -330,7 +336,27 @@ def _batch(device, name="batch64", shape=LLAMA8B, n=64, p_lo=4, p_hi=128,
         if conc_prob is not None:
             kinds = [True] * n
         w.history.append(query_step(w, kinds))
+    w.extra["conc_first"] = conc_first
     return w
+
+
+def batch_kinds(w: Workload, step: int, phase_len: int = 512) -> list:
+    """Per request: True if its query at decode step ``step`` is a
+    concentrated one.  Steps 0..63 are the 64-step history (the request's
+    seeded first kind, then the other one); after it the request keeps the
+    history's second kind until step 64 + phase_len - 128, then alternates in
+    phases of phase_len steps, as the single-request decode stream does.  The
+    flips fall halfway between boundaries (every 256 steps from step 64), so
+    at every boundary the requests in a diffuse phase have spent at least
+    128 steps in it."""
+    ph = (step - 64 + 128) // phase_len if step >= 64 else -1
+    out = []
+    for cf in w.extra["conc_first"]:
+        if step < 64:
+            out.append(cf if step < 32 else (not cf))
+        else:
+            out.append((not cf) if ph % 2 == 0 else cf)
+    return out
 
 
 STREAM_DEFAULTS = dict(seats=256, group=8, prefix_pages=32, spare_pages=256, median_tokens=2048,
