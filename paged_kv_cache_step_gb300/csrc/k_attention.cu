@@ -16,10 +16,7 @@
 // G heads' summaries from the query it loads anyway.
 //   copies  -- one thread streams stages of 16 KB of K rows and the same V
 //              rows into a ring of three shared-memory stages with bulk async
-//              copies (a page's rows of one head are contiguous); each warp
-//              releases a stage on an mbarrier once it has read it, and the
-//              stage is refilled when all warps have, so no block-wide
-//              barrier holds the warps in step;
+//              copies (a page's rows of one head are contiguous);
 //   compute -- a key row is read by D/8 lanes, each owning 8 dimensions, so
 //              the lanes of a quarter warp read 128 contiguous bytes.  Each
 //              group of D/8 lanes keeps its own online softmax (base 2) over
@@ -107,9 +104,7 @@ __global__ void __launch_bounds__(NT, 2) k_decode_attn(AttnArgs a) {
   static_assert(KG * G * (D + 2) * 4 <= NSTAGE * STAGE, "the group merge fits in the ring");
   __shared__ float qs[G][D];  // rotated query rows, scaled by log2(e)/sqrt(d)
   __shared__ __align__(8) uint64_t full_bar[NSTAGE];
-  __shared__ __align__(8) uint64_t empty_bar[NSTAGE];  // every warp arrives once it has read the stage
   __shared__ int s_last;
-  __shared__ volatile int s_abort;
   extern __shared__ __align__(128) unsigned char ring[];  // NSTAGE x (K rows, V rows)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -170,13 +165,9 @@ __global__ void __launch_bounds__(NT, 2) k_decode_attn(AttnArgs a) {
                  : "memory");
   };
   if (tid == 0) {
-    for (int st = 0; st < NSTAGE; ++st) {
+    for (int st = 0; st < NSTAGE; ++st)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full_bar[st])) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty_bar[st])), "r"(NWARP)
-                   : "memory");
-    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    s_abort = 0;
   }
   __syncthreads();  // the stage barriers exist before any copy or wait uses them
   if (tid == 0) {
@@ -236,25 +227,19 @@ __global__ void __launch_bounds__(NT, 2) k_decode_attn(AttnArgs a) {
   }
 
   // ---- the stages: logits, online softmax per key group, weighted values ----
-  // Warps run through the stages at their own pace.  A wait that gives up
-  // raises s_abort; every later wait then fails at once, so each warp leaves
-  // the loop within one bounded wait.
-  for (int k = 0; k < T; ++k) {
+  int k = 0;
+  bool aborted = false;
+  for (; k < T; ++k) {
     const int st = k % NSTAGE;
-    // thread 0 refills the buffer of stage k - 1 with stage k - 1 + NSTAGE once
-    // every warp has released it
-    if (tid == 0 && k >= 1 && k - 1 + NSTAGE < T && !s_abort) {
-      if (bar_wait(smem_addr(&empty_bar[(k - 1) % NSTAGE]), (uint32_t)(((k - 1) / NSTAGE) & 1))) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the warps' reads before the copy
-        issue(k - 1 + NSTAGE);
-      } else {
-        s_abort = 1;
-      }
-    }
-    const bool ok = !s_abort && bar_wait(smem_addr(&full_bar[st]), (uint32_t)((k / NSTAGE) & 1));
-    if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform exit
-      if (lane == 0) s_abort = 1;
+    const bool ok = bar_wait(smem_addr(&full_bar[st]), (uint32_t)((k / NSTAGE) & 1));
+    if (__syncthreads_or(!ok)) {  // every thread leaves together
+      aborted = true;
       break;
+    }
+    // every thread is done with stage k - 1: its buffer takes stage k - 1 + NSTAGE
+    if (tid == 0 && k >= 1 && k - 1 + NSTAGE < T) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(k - 1 + NSTAGE);
     }
     const unsigned char* sk = ring + (size_t)st * STAGE;
     const unsigned char* sv = sk + TBYTES;
@@ -310,22 +295,18 @@ __global__ void __launch_bounds__(NT, 2) k_decode_attn(AttnArgs a) {
           for (int t = 0; t < 8; ++t) acc[g][t] = fmaf(z[u][g], f[t], acc[g][t]);
       }
     }
-    __syncwarp();
-    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[st])) : "memory");
   }
-  __syncthreads();
-  if (s_abort) {
-    // the copies issued last may still be in flight: they land before the
-    // CTA's shared memory goes away (bounded; one outstanding phase per stage)
+  if (aborted) {
+    // copies still in flight land before the CTA's shared memory goes away (bounded)
     if (tid == 0) {
       atomicOr(a.err, ERR_TIMEOUT);
-      for (int q = issued > NSTAGE ? issued - NSTAGE : 0; q < issued; ++q)
-        bar_wait(smem_addr(&full_bar[q % NSTAGE]), (uint32_t)((q / NSTAGE) & 1));
+      for (int q = k; q < issued; ++q) bar_wait(smem_addr(&full_bar[q % NSTAGE]), (uint32_t)((q / NSTAGE) & 1));
     }
     return;
   }
 
   // ---- merge the key groups (the ring is free: every copy has landed) ----
+  __syncthreads();
   float* red = reinterpret_cast<float*>(ring);  // [KG][G][D] partial outputs
   float* rms = red + KG * G * D;                 // [KG][G] (max, sum)
 #pragma unroll

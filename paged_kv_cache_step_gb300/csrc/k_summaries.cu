@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(256) k_ema_update(EmaArgs a, unsigned long lon
   const int row = a.Hq * a.D;
   const int e0 = (blockIdx.x * 256 + threadIdx.x) * 4;
   const int slot = a.slots[r];
+  const bool first = a.first[r] != 0;  // loaded beside the slot, not after it
   if (slot < 0 || slot >= a.M) {
     if (blockIdx.x == 0 && l == 0 && threadIdx.x == 0) atomicOr(a.err, ERR_BAD_SLOT);
     return;
@@ -107,16 +108,18 @@ __global__ void __launch_bounds__(256) k_ema_update(EmaArgs a, unsigned long lon
   for (int i = 0; i < 4; ++i) q[i] = widen_exact(qf[i]);
   double2* row_s = reinterpret_cast<double2*>(a.pool + ((size_t)l * a.M + slot) * 2 * row + e0);
   double2* row_l = reinterpret_cast<double2*>(reinterpret_cast<double*>(row_s) + row);
+  // the old summaries are loaded whatever `first` says, so that their loads
+  // leave with the query's instead of waiting for the flag
+  const double2 os0 = __ldcs(row_s), os1 = __ldcs(row_s + 1);
+  const double2 ol0 = __ldcs(row_l), ol1 = __ldcs(row_l + 1);
   double2 s0, s1, l0, l1;
-  if (a.first[r]) {
+  if (first) {
     s0 = make_double2(q[0], q[1]);
     s1 = make_double2(q[2], q[3]);
     l0 = s0;
     l1 = s1;
   } else {
     const double ws = 1.0 - a.beta_s, wl = 1.0 - a.beta_l;
-    const double2 os0 = __ldcs(row_s), os1 = __ldcs(row_s + 1);
-    const double2 ol0 = __ldcs(row_l), ol1 = __ldcs(row_l + 1);
     double cs[4], cl[4];  // (1 - beta) q, rounded once as an fp64 multiply would
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
