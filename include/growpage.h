@@ -448,6 +448,19 @@ gp_status gp_debug_fail_next_launch(gp_ctx* ctx, int32_t kernel);
 #define GP_SCAN_TENSOR_CORE 2
 gp_status gp_set_scan_kernel(gp_ctx* ctx, int32_t kind);
 
+/* Where Compress & Hold's Eq. 10 selection runs (Sec. 3.3).  SPECULATIVE:
+ * after every gp_boundary_demand, on an engine-owned stream, while the host
+ * reads the sums and decides, so that a following Compress & Hold (or hole
+ * fill) only moves rows.  IN_COMPACTION: at the head of each (layer, KV
+ * head) unit's compaction CTA, where the copies of the other units' CTAs
+ * keep HBM busy.  AUTO (default): speculative for demand calls of at most
+ * 4 x (SM count) units that Compress & Hold could take, in the compaction
+ * above that.  The keep masks are the same either way.  Host only. */
+#define GP_SELECT_AUTO 0
+#define GP_SELECT_SPECULATIVE 1
+#define GP_SELECT_IN_COMPACTION 2
+gp_status gp_set_selection_mode(gp_ctx* ctx, int32_t mode);
+
 /* Per-kernel device time: when enabled, every kernel launch is bracketed by
  * CUDA events on the engine stream.  names: GP_KERNEL_* below.  The query
  * synchronises and returns the summed milliseconds and launch count since

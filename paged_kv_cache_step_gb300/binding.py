@@ -27,6 +27,7 @@ GP_POLICY_GROWPAGE, GP_POLICY_FIXED, GP_POLICY_RANDOM, GP_POLICY_INVERSE, GP_POL
 GP_ACT_GROW, GP_ACT_COMPRESS, GP_ACT_SHRINK = 0, 1, 2
 GP_METRIC_TOP_P, GP_METRIC_ENTROPY = 0, 1
 GP_SCAN_AUTO, GP_SCAN_CUDA_CORE, GP_SCAN_TENSOR_CORE = 0, 1, 2
+GP_SELECT_AUTO, GP_SELECT_SPECULATIVE, GP_SELECT_IN_COMPACTION = 0, 1, 2
 GP_KERNEL_EMA, GP_KERNEL_PREP, GP_KERNEL_DEMAND, GP_KERNEL_COMPRESS, GP_KERNEL_ATTENTION = 0, 1, 2, 3, 4
 GP_KERNEL_SELECT, GP_KERNEL_ENTROPY = 5, 6
 KERNEL_NAMES = {0: "ema_update", 1: "prep_queries", 2: "boundary_demand", 3: "compress_hold",
@@ -42,7 +43,7 @@ EXPORTS = [
     "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
     "gp_set_scan_kernel", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
     "gp_set_compaction_stream", "gp_wait_compaction", "gp_decode_attention",
-    "gp_synchronize", "gp_debug_set_wait_limit", "gp_debug_fail_next_launch",
+    "gp_synchronize", "gp_debug_set_wait_limit", "gp_debug_fail_next_launch", "gp_set_selection_mode",
 ]
 
 
@@ -147,6 +148,7 @@ def load(build_if_missing: bool = True):
         "gp_synchronize": (I32, [P]),
         "gp_debug_set_wait_limit": (I32, [P, I32, I64]),
         "gp_debug_fail_next_launch": (I32, [P, I32]),
+        "gp_set_selection_mode": (I32, [P, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -396,6 +398,10 @@ def gp_read_summaries(ctx, slot: int, L: int, hq: int, d: int) -> np.ndarray:
 
 def gp_set_scan_kernel(ctx, kind: int):
     _check(ctx, load().gp_set_scan_kernel(ctx, int(kind)))
+
+
+def gp_set_selection_mode(ctx, mode: int):
+    _check(ctx, load().gp_set_selection_mode(ctx, int(mode)))
 
 
 def gp_set_timing(ctx, enabled: bool):

@@ -88,6 +88,8 @@ struct gp_ctx {
   CUtensorMap kmap;                // K cache as a 2-D bf16 tensor (tensor-core scan)
   bool tc_ok = false;              // kmap is valid
   int scan_kernel = GP_SCAN_AUTO;
+  int select_mode = GP_SELECT_AUTO;
+  int64_t spec_units_max = 4 * 152;  // AUTO: speculative selection up to this many units per call
   void* pinned = nullptr;
   size_t pinned_cap = 0;
   cudaEvent_t pinned_free = nullptr;  // recorded after the last async use of `pinned`
@@ -403,6 +405,10 @@ gp_status gp_create(const gp_config* cfg, void* k_cache, void* v_cache, void* st
     }
     c->moved_dev = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(c->err_dev) + 8);
     c->tc_ok = make_kmap(c);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+      c->spec_units_max = 4 * (int64_t)sms;
   }
   *out = c;
   return GP_OK;
@@ -618,11 +624,20 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     aval_off[r] = aval_total;
     aval_total += (int64_t)units * 2 * (P - 1) * kPage;
   }
+  // Eq. 10 selection: speculatively, right after the demand kernels on the
+  // selection stream, where it hides behind the host's decision when the call
+  // is small; for calls of many units, inside the compaction launch, where
+  // the copies of other units' CTAs keep HBM busy while a CTA selects.
+  int64_t cand_units = 0;
+  for (int r = 0; r < n; ++r)
+    if (reqs[r].num_pages >= 2) cand_units += units;
+  const bool speculate = c->select_mode == GP_SELECT_SPECULATIVE ||
+                         (c->select_mode == GP_SELECT_AUTO && cand_units <= c->spec_units_max);
   // speculative keep masks: every request that Compress & Hold could take
   std::vector<int64_t> spec_off(n, -1);
   int64_t spec_total = 0;
   for (int r = 0; r < n; ++r) {
-    if (reqs[r].num_pages < 2) continue;
+    if (!speculate || reqs[r].num_pages < 2) continue;
     spec_off[r] = spec_total;
     spec_total += (int64_t)units * (reqs[r].num_pages * kPage / 32);
   }
@@ -1212,6 +1227,14 @@ gp_status gp_set_scan_kernel(gp_ctx* c, int32_t kind) {
   if (kind == GP_SCAN_TENSOR_CORE && !c->host_only && !c->tc_ok)
     return fail(c, GP_ERR_UNSUPPORTED, "the tensor-core scan needs a 16-byte aligned bf16 K cache");
   c->scan_kernel = kind;
+  return GP_OK;
+}
+
+gp_status gp_set_selection_mode(gp_ctx* c, int32_t mode) {
+  if (!c) return GP_ERR_INVALID;
+  if (mode != GP_SELECT_AUTO && mode != GP_SELECT_SPECULATIVE && mode != GP_SELECT_IN_COMPACTION)
+    return fail(c, GP_ERR_INVALID, "unknown selection mode %d", mode);
+  c->select_mode = mode;
   return GP_OK;
 }
 

@@ -111,13 +111,18 @@ def test_shrink_needs_three_pages():
 
 
 @pytest.mark.parametrize("shared", [False, True])
-def test_hole_fill_matches_oracle(shared):
+@pytest.mark.parametrize("select_mode", ["speculative", "in_compaction"])
+def test_hole_fill_matches_oracle(shared, select_mode):
     """gp_compress_fill: the Eq. 10 selection of Compress & Hold, then the
     order-destroying hole fill: bytes exactly as the oracle's hole fill of
-    the GPU's own keep masks, copy-on-write as planned by the oracle."""
+    the GPU's own keep masks, copy-on-write as planned by the oracle.  With
+    the selection speculative (its own launch after the demand call) and
+    inside the compaction launch."""
     sizes = [2, 5, 33]
     w = synth.make_workload("custom", device="cuda", shape=SHAPE, sizes=sizes, seed_xor=23)
     run = hz.EngineRun(w)
+    gp.gp_set_selection_mode(run.ctx, gp.GP_SELECT_SPECULATIVE if select_mode == "speculative"
+                             else gp.GP_SELECT_IN_COMPACTION)
     try:
         if shared:
             pre = run.reqs[0].pages[:2]
