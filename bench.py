@@ -522,7 +522,7 @@ class Batch:
     and the page a Grow added, or the page a Compress & Hold freed, is filled
     with fresh synthetic tokens, so that every request is full again."""
 
-    def __init__(self, gp, name, device, policy="growpage", metric=0, extra_pages=0, n=None):
+    def __init__(self, gp, name, device, policy="growpage", metric=0, extra_pages=0, n=None, selection=None):
         self.gp = gp
         kw = {"n": n} if n else {}
         self.w = w = synth.make_workload(name, device=device, extra_pages=extra_pages, **kw)
@@ -536,6 +536,9 @@ class Batch:
                 gp.gp_page_unref(self.ctx, pg)
         self.reqs = [gp.Request(gp.gp_slot_acquire(self.ctx), t, w.positions[r], 256)
                      for r, t in enumerate(w.block_tables)]
+        if selection:
+            gp.gp_set_selection_mode(self.ctx, {"speculative": gp.GP_SELECT_SPECULATIVE,
+                                                "in_compaction": gp.GP_SELECT_IN_COMPACTION}[selection])
         self.slots = torch.tensor([q.slot for q in self.reqs], dtype=torch.int32, device=device)
         self.first = torch.ones(w.n, dtype=torch.uint8, device=device)
         self.notfirst = torch.zeros(w.n, dtype=torch.uint8, device=device)
@@ -621,7 +624,8 @@ def measure_overlap_batch(args, device, extra):
     import paged_kv_cache_step_gb300 as gp
     res = {}
     for mode in ("sync", "async"):
-        b = Batch(gp, args.workload, device, args.policy, _metric(args), extra, args.batch_requests)
+        b = Batch(gp, args.workload, device, args.policy, _metric(args), extra, args.batch_requests,
+                  _selection(args))
         sh = b.w.shape
         if mode == "async":
             side = torch.cuda.Stream(device=device)
@@ -693,6 +697,10 @@ def measure_overlap_batch(args, device, extra):
                         "launch to the engine stream's wait for it; device time (CUDA events)"}
 
 
+def _selection(args):
+    return None if args.selection == "auto" else args.selection
+
+
 def _batch_extra_pages(w_n: int, steps: int) -> int:
     """Free pages beyond the configuration's spare ones, so that the Grows of
     every step of the run can be granted (about half the requests grow)."""
@@ -722,7 +730,8 @@ def run_batch(args, world, rank, local):
     peak, peak_src = _peaks()
     n_req = args.batch_requests or (64 if args.workload == "batch64" else 16)
     extra = _batch_extra_pages(n_req, args.warmup + args.steps)
-    b = Batch(gp, args.workload, device, args.policy, _metric(args), extra, args.batch_requests)
+    b = Batch(gp, args.workload, device, args.policy, _metric(args), extra, args.batch_requests,
+                  _selection(args))
     w = b.w
     desc = _batch_desc(args.workload, w, extra, args.policy, _metric(args))
     cpu = None
@@ -778,7 +787,8 @@ def run_batch(args, world, rank, local):
     # inside the timed region (gp_boundary_demand reads the D_p sums back)
     e2e = None
     if not args.no_e2e:
-        b = Batch(gp, args.workload, device, args.policy, _metric(args), extra, args.batch_requests)
+        b = Batch(gp, args.workload, device, args.policy, _metric(args), extra, args.batch_requests,
+                  _selection(args))
         for _ in range(args.warmup):
             _, gr, cm = b.event(b.query())
             b.between(gr, cm)
@@ -1088,6 +1098,8 @@ def main():
     ap.add_argument("--policy", default="growpage", choices=["growpage", "fixed"])
     ap.add_argument("--single-pages", type=int, default=0,
                     help="llama8b_single: pages of the request at its first boundary (default 32)")
+    ap.add_argument("--selection", default="auto", choices=["auto", "speculative", "in_compaction"],
+                    help="batch workloads: where the Eq. 10 selection runs (gp_set_selection_mode)")
     ap.add_argument("--batch-requests", type=int, default=0,
                     help="batch workloads: this many requests instead of the configuration's (a small "
                          "case of the same recipe, e.g. for profiler captures)")

@@ -1357,7 +1357,8 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   const int maxp = g.max_pages_per_req;
   const int Hkv = g.num_kv_heads;
   // Splits over the attended pages: about `chunk` pages per CTA, so that the
-  // call fills roughly three waves of two CTAs per SM; longest requests first,
+  // call fills roughly six waves of two CTAs per SM (measured on a 64-request
+  // decode step: 2, 3, 6, 12 waves gave 69.5, 71.6, 74.0, 73.3 % of HBM); longest requests first,
   // so that the largest CTAs start first.
   std::vector<int> npg(n), order(n), nsp(n);
   long long total_pages = 0;
@@ -1367,7 +1368,7 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
     order[r] = r;
   }
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return npg[x] > npg[y]; });
-  const long long target_ctas = 3LL * 2 * 152;
+  const long long target_ctas = 6LL * 2 * 152;
   const long long chunk = std::max(1LL, (total_pages * Hkv + target_ctas - 1) / target_ctas);
   long long n_ctas = 0;
   for (int r = 0; r < n; ++r) {
