@@ -858,23 +858,31 @@ def measure_attention(gp, ctx, w, reqs, ts, peak, args):
     torch.cuda.synchronize()
     row = sh.head_dim * 2
     step_bytes = sum(ntok) * sh.num_kv_heads * row * 2 * sh.num_layers
-    for _ in range(2):
-        for layer in range(sh.num_layers):
-            gp.gp_decode_attention(ctx, layer, reqs, ntok, q[layer], first, out)
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(max(3, args.steps)):
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(ts)   # the engine's stream, which the launches go to
-        for layer in range(sh.num_layers):
-            gp.gp_decode_attention(ctx, layer, reqs, ntok, q[layer], first, out)
-        ev1.record(ts)
+
+    def timed():
+        for _ in range(2):
+            for layer in range(sh.num_layers):
+                gp.gp_decode_attention(ctx, layer, reqs, ntok, q[layer], first, out)
         torch.cuda.synchronize()
-        times.append(ev0.elapsed_time(ev1))
-    ms = sum(times) / len(times)
-    a = step_bytes / (ms / 1e3) / 1e9
+        times = []
+        for _ in range(max(3, args.steps)):
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(ts)   # the engine's stream, which the launches go to
+            for layer in range(sh.num_layers):
+                gp.gp_decode_attention(ctx, layer, reqs, ntok, q[layer], first, out)
+            ev1.record(ts)
+            torch.cuda.synchronize()
+            times.append(ev0.elapsed_time(ev1))
+        ms = sum(times) / len(times)
+        return ms, step_bytes / (ms / 1e3) / 1e9
+
+    ms, a = timed()                                       # the kernel AUTO picks (tcgen05 for bf16, d 128)
+    gp.gp_set_scan_kernel(ctx, gp.GP_SCAN_CUDA_CORE)      # the CUDA-core kernel on the same step, for comparison
+    ms_cc, a_cc = timed()
+    gp.gp_set_scan_kernel(ctx, gp.GP_SCAN_AUTO)
     return {"ms_per_decode_step": ms, "bytes_per_step": step_bytes, "achieved_gbs": a, "peak": peak,
-            "frac": a / peak, "layers": sh.num_layers, "requests": n}
+            "frac": a / peak, "layers": sh.num_layers, "requests": n,
+            "cuda_core_kernel": {"ms_per_decode_step": ms_cc, "achieved_gbs": a_cc, "frac": a_cc / peak}}
 
 
 def run_stream(args, device):

@@ -436,13 +436,17 @@ gp_status gp_synchronize(gp_ctx* ctx);
 gp_status gp_debug_set_wait_limit(gp_ctx* ctx, int32_t kernel, int64_t cycles);
 gp_status gp_debug_fail_next_launch(gp_ctx* ctx, int32_t kernel);
 
-/* Which kernel scans the cache in gp_boundary_demand.  AUTO (default): the
- * tensor-core (tcgen05) scan for bf16 caches (every request length up to
- * the 256-page block-table limit), the CUDA-core (fp32 FMA) scan for fp32
- * caches or a K cache no tensor map can describe (base not 16-byte aligned,
- * or 2^31 or more key rows).  CUDA_CORE forces the latter everywhere;
- * TENSOR_CORE makes requests it cannot serve fail with GP_ERR_UNSUPPORTED.  Both give the same results within the tolerances of
- * fp32 arithmetic.  Host only. */
+/* Which kernels do the cache-wide contractions: the scan of
+ * gp_boundary_demand and the scores and weighted values of
+ * gp_decode_attention.  AUTO (default): the tensor-core (tcgen05) kernels
+ * where they apply -- the scan for bf16 caches (every request length up to
+ * the 256-page block-table limit), attention for bf16 caches with d = 128
+ * and 2 or 4 query heads per KV head -- and the CUDA-core (fp32 FMA)
+ * kernels otherwise: fp32 caches, other attention shapes, or a K or V cache
+ * no tensor map can describe (base not 16-byte aligned, or 2^31 or more key
+ * rows).  CUDA_CORE forces the latter everywhere; TENSOR_CORE makes calls the
+ * tensor-core kernels cannot serve fail with GP_ERR_UNSUPPORTED.  Both give
+ * the same results within the tolerances of fp32 arithmetic.  Host only. */
 #define GP_SCAN_AUTO 0
 #define GP_SCAN_CUDA_CORE 1
 #define GP_SCAN_TENSOR_CORE 2

@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgrowpage.so")
 
 SOURCES = ["growpage.cpp", "k_summaries.cu", "k_demand.cu", "k_demand_tc.cu", "k_compress.cu", "k_attention.cu",
-           "k_entropy.cu", "noalloc.cu"]
+           "k_attention_tc.cu", "k_entropy.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

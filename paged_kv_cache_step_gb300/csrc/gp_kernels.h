@@ -157,6 +157,8 @@ inline DemandPlan demand_plan(int P, bool tc_ok) {
 
 // ---- decode attention with the summary update fused in (one layer) -------
 struct AttnArgs {
+  CUtensorMap kmap, vmap;  // K and V caches as [rows][D] bf16, box 64 x 128, 128-byte swizzle
+  int tc;                  // 1: the tensor-core kernel (bf16 caches, D = 128, G = 2 or 4)
   const void* k_cache;     // [L][num_pages][Hkv][b][D], keys stored rotated
   const void* v_cache;
   int kv_f32;
@@ -182,6 +184,9 @@ struct AttnArgs {
   int* err;
 };
 cudaError_t launch_decode_attention(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_decode_attention_tc(const AttnArgs& a, cudaStream_t s);
+// Whether the tensor-core attention kernel takes this shape.
+inline bool attention_tc_shape(int D, int G) { return D == 128 && (G == 2 || G == 4); }
 
 // ---- entropy metric (Sec. 5.3 ablation): exp(H(a^x)) per unit ----------------
 struct EntropyArgs {

@@ -85,8 +85,11 @@ struct gp_ctx {
   cudaEvent_t ev_dem = nullptr, ev_sel = nullptr;
   bool sel_pending = false;
   double* inv_freq = nullptr;      // [D/2] theta^(-2i/D) for RoPE
-  CUtensorMap kmap;                // K cache as a 2-D bf16 tensor (tensor-core scan)
+  CUtensorMap kmap;                // K cache as a 2-D bf16 tensor (tensor-core scan and attention)
+  CUtensorMap vmap;                // V cache the same way (tensor-core attention)
   bool tc_ok = false;              // kmap is valid
+  bool attn_tc_ok = false;         // kmap and vmap are valid
+  int sms = 152;                   // SMs of the device
   int scan_kernel = GP_SCAN_AUTO;
   int select_mode = GP_SELECT_AUTO;
   int64_t spec_units_max = 4 * 152;  // AUTO: speculative selection up to this many units per call
@@ -272,15 +275,15 @@ gp_status validate_request(gp_ctx* c, const gp_request& r, int idx, bool need_sl
 
 int units_of(const gp_ctx* c) { return c->cfg.num_layers * c->cfg.num_kv_heads; }
 
-// Tensor map of the K cache for the tensor-core scan: a 2-D bf16 tensor of
+// Tensor map of the K (or V) cache for the tensor-core kernels: a 2-D bf16 tensor of
 // rows = L * num_pages * Hkv * b keys by d elements, copied in boxes of
 // 64 elements x 128 keys with the 128-byte swizzle the MMA descriptors use.
-// False (and the CUDA-core scan is used) when the cache is not bf16, its
+// False (and the CUDA-core kernels are used) when the cache is not bf16, its
 // base is not 16-byte aligned, or the row count does not fit a coordinate.
-bool make_kmap(gp_ctx* c) {
+bool make_map(gp_ctx* c, void* cache, CUtensorMap* map) {
   const gp_config& g = c->cfg;
   if (g.kv_dtype != GP_DTYPE_BF16) return false;
-  if (reinterpret_cast<uintptr_t>(c->k_cache) & 15u) return false;
+  if (reinterpret_cast<uintptr_t>(cache) & 15u) return false;
   const uint64_t rows = (uint64_t)g.num_layers * (uint64_t)g.num_pages * (uint64_t)g.num_kv_heads * kPage;
   if (rows + 128 >= (1ull << 31)) return false;
   void* fn = nullptr;
@@ -293,7 +296,7 @@ bool make_kmap(gp_ctx* c) {
   cuuint64_t strides[1] = {(cuuint64_t)g.head_dim * 2};
   cuuint32_t box[2] = {64, 128};
   cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(&c->kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->k_cache, dims, strides, box, estr,
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cache, dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -404,11 +407,14 @@ gp_status gp_create(const gp_config* cfg, void* k_cache, void* v_cache, void* st
       return GP_ERR_CUDA;
     }
     c->moved_dev = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(c->err_dev) + 8);
-    c->tc_ok = make_kmap(c);
+    c->tc_ok = make_map(c, c->k_cache, &c->kmap);
+    c->attn_tc_ok = c->tc_ok && make_map(c, c->v_cache, &c->vmap);
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
       c->spec_units_max = 4 * (int64_t)sms;
+      c->sms = sms;
+    }
   }
   *out = c;
   return GP_OK;
@@ -1352,14 +1358,20 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
     for (int r = 0; r < n && !overlap; ++r)
       for (int j = 0; j < reqs[r].num_pages && !overlap; ++j)
         overlap = c->pending_pages.count(reqs[r].block_table[j]) != 0;
-  if (overlap) GP_CUDA(c, cudaStreamWaitEvent(c->stream, c->ev_done, 0));
   const int G = g.num_q_heads / g.num_kv_heads;
+  // The tensor-core kernel takes bf16 caches with d = 128 and G = 2 or 4
+  // (AUTO and TENSOR_CORE); the CUDA-core kernel everything else.
+  const bool tc = c->attn_tc_ok && c->scan_kernel != GP_SCAN_CUDA_CORE && gp::attention_tc_shape(g.head_dim, G);
+  if (c->scan_kernel == GP_SCAN_TENSOR_CORE && !tc)
+    return fail(c, GP_ERR_UNSUPPORTED, "the tensor-core attention kernel cannot take this cache or shape");
+  if (overlap) GP_CUDA(c, cudaStreamWaitEvent(c->stream, c->ev_done, 0));
   const int maxp = g.max_pages_per_req;
   const int Hkv = g.num_kv_heads;
   // Splits over the attended pages: about `chunk` pages per CTA, so that the
-  // call fills roughly six waves of two CTAs per SM (measured on a 64-request
-  // decode step: 2, 3, 6, 12 waves gave 69.5, 71.6, 74.0, 73.3 % of HBM); longest requests first,
-  // so that the largest CTAs start first.
+  // call fills a few waves of the kernel's resident CTAs (one per SM for the
+  // tensor-core kernel, two for the CUDA-core one, which measured 69.5, 71.6,
+  // 74.0, 73.3 % of HBM with 2, 3, 6, 12 waves on a 64-request decode step);
+  // longest requests first, so that the largest CTAs start first.
   std::vector<int> npg(n), order(n), nsp(n);
   long long total_pages = 0;
   for (int r = 0; r < n; ++r) {
@@ -1368,7 +1380,7 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
     order[r] = r;
   }
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return npg[x] > npg[y]; });
-  const long long target_ctas = 6LL * 2 * 152;
+  const long long target_ctas = tc ? 6LL * c->sms : 6LL * 2 * c->sms;
   const long long chunk = std::max(1LL, (total_pages * Hkv + target_ctas - 1) / target_ctas);
   long long n_ctas = 0;
   for (int r = 0; r < n; ++r) {
@@ -1402,6 +1414,11 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   char* base = static_cast<char*>(c->attn.p);
   GP_CUDA(c, cudaMemsetAsync(base + tick_off, 0, sizeof(unsigned) * (size_t)n * g.num_kv_heads, c->stream));
   gp::AttnArgs a{};
+  a.tc = tc ? 1 : 0;
+  if (tc) {
+    a.kmap = c->kmap;
+    a.vmap = c->vmap;
+  }
   a.k_cache = c->k_cache;
   a.v_cache = c->v_cache;
   a.kv_f32 = g.kv_dtype == GP_DTYPE_F32;

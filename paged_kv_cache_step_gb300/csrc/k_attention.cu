@@ -381,6 +381,7 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t s) {
 
 cudaError_t launch_decode_attention(const AttnArgs& a, cudaStream_t s) {
   if (a.n == 0) return cudaSuccess;
+  if (a.tc) return launch_decode_attention_tc(a, s);
   if (a.n_ctas < a.n * a.Hkv) return cudaErrorInvalidValue;
   const bool f32 = a.kv_f32 != 0;
   if (a.D == 128 && a.G == 4) return f32 ? launch_t<128, 4, true>(a, s) : launch_t<128, 4, false>(a, s);

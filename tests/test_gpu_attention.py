@@ -29,9 +29,16 @@ pytestmark = pytest.mark.gpu
 PAGE = 256
 SHAPES = {
     "bf16_g4_d128": ModelShape(2, 8, 2, 128, "bf16", "bf16", 5.0e5),
+    "bf16_g2_d128": ModelShape(2, 4, 2, 128, "bf16", "bf16", 5.0e5),
     "bf16_g2_d64": ModelShape(2, 4, 2, 64, "bf16", "bf16", 1.0e4),
     "f32_g4_d128": ModelShape(2, 8, 2, 128, "f32", "f32", 5.0e5),
 }
+# the kernels each shape runs on: the tensor-core kernel (forced, so that a
+# shape it cannot take fails instead of falling back) where it applies, and
+# the CUDA-core kernel everywhere
+KERNELS = {"tensor_core": gp.GP_SCAN_TENSOR_CORE, "cuda_core": gp.GP_SCAN_CUDA_CORE}
+CASES = [(s, k) for s in sorted(SHAPES) for k in sorted(KERNELS)
+         if k == "cuda_core" or (SHAPES[s].kv_dtype == "bf16" and SHAPES[s].head_dim == 128)]
 
 
 def _oracle_attention(q_pre, keys, values, pos, theta):
@@ -41,13 +48,14 @@ def _oracle_attention(q_pre, keys, values, pos, theta):
     return a @ values, a
 
 
-@pytest.mark.parametrize("shape_name", sorted(SHAPES))
-def test_decode_attention_matches_oracle(shape_name):
+@pytest.mark.parametrize("shape_name,kernel", CASES)
+def test_decode_attention_matches_oracle(shape_name, kernel):
     sh = SHAPES[shape_name]
     sizes = [1, 3, 33, 5]
     w = synth.make_workload("custom", device="cuda", shape=sh, sizes=sizes, seed_xor=41)
     run = hz.EngineRun(w)
     try:
+        gp.gp_set_scan_kernel(run.ctx, KERNELS[kernel])
         run.feed_history()
         n = len(sizes)
         ntok = [PAGE, 3 * PAGE - 100, 1, 0]
@@ -169,15 +177,18 @@ def test_theorem31_bound_after_compress_and_hold():
         run.close()
 
 
-def test_decode_attention_multi_page_splits():
-    """Enough pages that a split spans several pages (the host gives each CTA
-    about total_pages * Hkv / 912 pages) and the 64-split cap applies to the
-    longest request; ragged token counts end inside a stage."""
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_decode_attention_multi_page_splits(kernel):
+    """Enough pages that a split spans several pages (the host aims at six
+    waves of the kernel's resident CTAs: 912 CTAs for the tensor-core kernel,
+    1824 for the CUDA-core one) and the 64-split cap applies to the longest
+    request; ragged token counts end inside a tile or stage."""
     sh = SHAPES["bf16_g4_d128"]
-    sizes = [160, 150, 130, 97, 40, 5]  # 582 pages x 2 KV heads: about 2 pages per CTA
+    sizes = [160, 150, 130, 97, 40, 5]  # 582 pages x 2 KV heads: one or two pages per CTA
     w = synth.make_workload("custom", device="cuda", shape=sh, sizes=sizes, seed_xor=44)
     run = hz.EngineRun(w)
     try:
+        gp.gp_set_scan_kernel(run.ctx, KERNELS[kernel])
         run.feed_history()
         n, G, layer = len(sizes), sh.group, 0
         ntok = [160 * PAGE, 150 * PAGE - 77, 130 * PAGE - 1, 97 * PAGE - 255, 40 * PAGE - 128, 5 * PAGE - 130]
