@@ -1367,11 +1367,15 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   if (overlap) GP_CUDA(c, cudaStreamWaitEvent(c->stream, c->ev_done, 0));
   const int maxp = g.max_pages_per_req;
   const int Hkv = g.num_kv_heads;
-  // Splits over the attended pages: about `chunk` pages per CTA, so that the
-  // call fills a few waves of the kernel's resident CTAs (one per SM for the
-  // tensor-core kernel, two for the CUDA-core one, which measured 69.5, 71.6,
-  // 74.0, 73.3 % of HBM with 2, 3, 6, 12 waves on a 64-request decode step);
-  // longest requests first, so that the largest CTAs start first.
+  // Splits over the attended pages: about `chunk` pages per CTA, longest
+  // requests first so that the largest CTAs start first.  The tensor-core
+  // kernel (one CTA per SM) aims at one wave: a CTA's start (query, first
+  // tiles) and end (partials) are not hidden behind another CTA's copies, so
+  // fewer, longer CTAs win while the longest-first order keeps the SMs busy
+  // (64-request decode step: 1, 2, 3, 6, 12 waves gave 93.5, 92.7, 94.2,
+  // 91.4, 87.4 % of HBM; 16 requests of 128 pages: 89.0, 86.4, 86.0, 83.7 %
+  // for 1, 2, 3, 6).  The CUDA-core kernel (two CTAs per SM) aims at six
+  // waves (2, 3, 6, 12 gave 69.5, 71.6, 74.0, 73.3 % on the 64-request step).
   std::vector<int> npg(n), order(n), nsp(n);
   long long total_pages = 0;
   for (int r = 0; r < n; ++r) {
@@ -1380,7 +1384,7 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
     order[r] = r;
   }
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return npg[x] > npg[y]; });
-  const long long target_ctas = tc ? 6LL * c->sms : 6LL * 2 * c->sms;
+  const long long target_ctas = tc ? (long long)c->sms : 6LL * 2 * c->sms;
   const long long chunk = std::max(1LL, (total_pages * Hkv + target_ctas - 1) / target_ctas);
   long long n_ctas = 0;
   for (int r = 0; r < n; ++r) {

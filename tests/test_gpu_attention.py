@@ -179,12 +179,12 @@ def test_theorem31_bound_after_compress_and_hold():
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
 def test_decode_attention_multi_page_splits(kernel):
-    """Enough pages that a split spans several pages (the host aims at six
-    waves of the kernel's resident CTAs: 912 CTAs for the tensor-core kernel,
-    1824 for the CUDA-core one) and the 64-split cap applies to the longest
-    request; ragged token counts end inside a tile or stage."""
+    """Enough pages that a split spans several pages (the host aims at one
+    wave of the tensor-core kernel, 152 CTAs, or six of the CUDA-core one,
+    1824 CTAs) and, on the CUDA-core kernel, the 64-split cap applies to the
+    longest request; ragged token counts end inside a tile or stage."""
     sh = SHAPES["bf16_g4_d128"]
-    sizes = [160, 150, 130, 97, 40, 5]  # 582 pages x 2 KV heads: one or two pages per CTA
+    sizes = [160, 150, 130, 97, 40, 5]  # 582 pages x 2 KV heads: 1 or 2 pages per CUDA-core CTA, 8 per tensor-core one
     w = synth.make_workload("custom", device="cuda", shape=sh, sizes=sizes, seed_xor=44)
     run = hz.EngineRun(w)
     try:
