@@ -156,6 +156,19 @@ inline DemandPlan demand_plan(int P, bool tc_ok) {
 }
 
 // ---- decode attention with the summary update fused in (one layer) -------
+// One work item of the tensor-core kernel, built by the host: the split
+// `split` (of nsp) of request r's attended pages, for KV head h.
+struct AttnItem {
+  int32_t r, h, split, nsp;
+  int32_t part_first;  // the first partial of (r, h); this item's is part_first + split
+  int32_t p0;          // first attended page of the split
+  int32_t T;           // tiles of 128 keys (0: no attended token)
+  int32_t ntok;        // tokens the request attends to
+  int32_t bt_off, slot;
+  int64_t pos;
+};
+static_assert(sizeof(AttnItem) == 48, "three 16-byte loads per item");
+
 struct AttnArgs {
   CUtensorMap kmap, vmap;  // K and V caches as [rows][D] bf16, box 64 x 128, 128-byte swizzle
   int tc;                  // 1: the tensor-core kernel (bf16 caches, D = 128, G = 2 or 4)
@@ -176,11 +189,14 @@ struct AttnArgs {
   float* out;              // [n][Hq][D]
   float* part;             // split partials [n_ctas][G][D + 2], those of (r, h) together
   unsigned* tickets;       // [n][Hkv], zero before the launch
-  const int32_t* split_base;  // [n + 1] first CTA of each request, in `order`
+  const int32_t* split_base;  // [n + 1] first work item of each request, in `order`
   const int32_t* order;    // [n] requests, longest first; request order[i] has
-                           // (split_base[i+1] - split_base[i]) / Hkv splits, CTA
-                           // split_base[i] + split * Hkv + h
-  int n, n_ctas;
+                           // (split_base[i+1] - split_base[i]) / Hkv splits, work
+                           // item split_base[i] + split * Hkv + h
+  int n, n_ctas;           // n_ctas: work items (request, KV head, split); the
+                           // CUDA-core kernel runs one CTA per item
+  int grid;                // tensor-core kernel: persistent CTAs (<= n_ctas)
+  const AttnItem* items;   // tensor-core kernel: [n_ctas] work items, in the order above
   int* err;
 };
 cudaError_t launch_decode_attention(const AttnArgs& a, cudaStream_t s);

@@ -553,13 +553,15 @@ struct Staged {
   int32_t* work;
   int32_t* part_base;
   int32_t* sel;  // requests of a demand call that get a speculative selection
+  void* extra;   // a call's own table (decode attention: its work items)
   size_t bytes;
-  size_t off_bt, off_bt_new, off_work, off_pb, off_sel;
+  size_t off_bt, off_bt_new, off_work, off_pb, off_sel, off_extra;
 };
 
-// Pinned layout [DevReq n][bt n*maxP][bt_new n*maxP][work n][part_base n+1],
-// mirrored in `dev` (the engine's upload buffer unless another is given).
-gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s, DevBuf* dev = nullptr) {
+// Pinned layout [DevReq n][bt n*maxP][bt_new n*maxP][work n][part_base n+1]
+// [sel n][extra bytes], mirrored in `dev` (the engine's upload buffer unless
+// another is given).
+gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s, DevBuf* dev = nullptr, size_t extra = 0) {
   s->dev = dev ? dev : &c->upload;
   const int maxp = c->cfg.max_pages_per_req;
   size_t o = 0;
@@ -570,6 +572,7 @@ gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s, DevBuf* dev = nullpt
   s->off_work = take(sizeof(int32_t) * n);
   s->off_pb = take(sizeof(int32_t) * (n + 1));
   s->off_sel = take(sizeof(int32_t) * n);
+  s->off_extra = take(extra);
   s->bytes = o;
   gp_status st = ensure_pinned(c, o);
   if (st != GP_OK) return st;
@@ -582,6 +585,7 @@ gp_status stage(gp_ctx* c, int n, bool with_new, Staged* s, DevBuf* dev = nullpt
   s->work = reinterpret_cast<int32_t*>(p + s->off_work);
   s->part_base = reinterpret_cast<int32_t*>(p + s->off_pb);
   s->sel = reinterpret_cast<int32_t*>(p + s->off_sel);
+  s->extra = p + s->off_extra;
   return GP_OK;
 }
 
@@ -1367,15 +1371,16 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   if (overlap) GP_CUDA(c, cudaStreamWaitEvent(c->stream, c->ev_done, 0));
   const int maxp = g.max_pages_per_req;
   const int Hkv = g.num_kv_heads;
-  // Splits over the attended pages: about `chunk` pages per CTA, longest
-  // requests first so that the largest CTAs start first.  The tensor-core
-  // kernel (one CTA per SM) aims at one wave: a CTA's start (query, first
-  // tiles) and end (partials) are not hidden behind another CTA's copies, so
-  // fewer, longer CTAs win while the longest-first order keeps the SMs busy
-  // (64-request decode step: 1, 2, 3, 6, 12 waves gave 93.5, 92.7, 94.2,
-  // 91.4, 87.4 % of HBM; 16 requests of 128 pages: 89.0, 86.4, 86.0, 83.7 %
-  // for 1, 2, 3, 6).  The CUDA-core kernel (two CTAs per SM) aims at six
-  // waves (2, 3, 6, 12 gave 69.5, 71.6, 74.0, 73.3 % on the 64-request step).
+  // Work items: splits of about `chunk` attended pages per (request, KV
+  // head), longest requests first.  The tensor-core kernel is persistent
+  // (one CTA per SM walks its share of the items, prefetching the next
+  // item's tiles) and aims at about one item per SM: each item adds a
+  // ticket and, for the last split of a (request, KV head), a merge, so more
+  // items cost more than their balance gains (items per SM 1, 2, 4, 8: 97.4,
+  // 86.3, 97.9, 93.2 % of HBM on a 64-request decode step; 92.3, 89.4,
+  // 88.6, 89.1 % on 16 requests of 128 pages).  The CUDA-core kernel runs one
+  // CTA per item, two per SM, and aims at six waves (2, 3, 6, 12 gave 69.5,
+  // 71.6, 74.0, 73.3 % on the 64-request step).
   std::vector<int> npg(n), order(n), nsp(n);
   long long total_pages = 0;
   for (int r = 0; r < n; ++r) {
@@ -1395,11 +1400,36 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   const size_t tick_off = (part_floats * sizeof(float) + 255) & ~size_t(255);
   if ((st = ensure(c, c->attn, tick_off + sizeof(unsigned) * (size_t)n * Hkv)) != GP_OK) return st;
   Staged s{};
-  if ((st = stage(c, n, false, &s, &c->upload_attn)) != GP_OK) return st;
+  if ((st = stage(c, n, false, &s, &c->upload_attn, tc ? sizeof(gp::AttnItem) * (size_t)n_ctas : 0)) != GP_OK)
+    return st;
   s.part_base[0] = 0;
   for (int i = 0; i < n; ++i) {
     s.sel[i] = order[i];
     s.part_base[i + 1] = s.part_base[i] + nsp[order[i]] * Hkv;
+  }
+  if (tc) {
+    // the tensor-core kernel's work items, in the same order: request order[i],
+    // then item split * Hkv + h of it
+    gp::AttnItem* it = static_cast<gp::AttnItem*>(s.extra);
+    for (int i = 0; i < n; ++i) {
+      const int r = order[i], ns = nsp[r];
+      for (int local = 0; local < ns * Hkv; ++local, ++it) {
+        const int h = local % Hkv, split = local / Hkv;
+        const int p0 = (int)((long long)split * npg[r] / ns), p1 = (int)((long long)(split + 1) * npg[r] / ns);
+        const int span = std::min(num_tokens[r] - p0 * kPage, (p1 - p0) * kPage);
+        it->r = r;
+        it->h = h;
+        it->split = split;
+        it->nsp = ns;
+        it->part_first = s.part_base[i] + h * ns;
+        it->p0 = p0;
+        it->T = span > 0 ? (span + 127) / 128 : 0;
+        it->ntok = num_tokens[r];
+        it->bt_off = r * maxp;
+        it->slot = reqs[r].slot;
+        it->pos = reqs[r].pos;
+      }
+    }
   }
   for (int r = 0; r < n; ++r) {
     gp::DevReq& d = s.reqs[r];
@@ -1450,6 +1480,8 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   a.order = dev_at<int32_t>(s, s.off_sel);
   a.n = n;
   a.n_ctas = (int)n_ctas;
+  a.grid = (int)std::min<long long>(n_ctas, c->sms);
+  a.items = tc ? dev_at<gp::AttnItem>(s, s.off_extra) : nullptr;
   a.err = c->err_dev;
   return timed_launch(c, GP_KERNEL_ATTENTION, "decode_attention",
                       [&] { return gp::launch_decode_attention(a, c->stream); });

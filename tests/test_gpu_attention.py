@@ -179,10 +179,11 @@ def test_theorem31_bound_after_compress_and_hold():
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
 def test_decode_attention_multi_page_splits(kernel):
-    """Enough pages that a split spans several pages (the host aims at one
-    wave of the tensor-core kernel, 152 CTAs, or six of the CUDA-core one,
-    1824 CTAs) and, on the CUDA-core kernel, the 64-split cap applies to the
-    longest request; ragged token counts end inside a tile or stage."""
+    """Enough pages that a split spans several pages (the host aims at about
+    one work item per SM for the persistent tensor-core kernel, and at six
+    waves of two CTAs per SM, 1824 CTAs, for the CUDA-core one, where the
+    64-split cap applies to the longest request); ragged token counts end
+    inside a tile or stage."""
     sh = SHAPES["bf16_g4_d128"]
     sizes = [160, 150, 130, 97, 40, 5]  # 582 pages x 2 KV heads: 1 or 2 pages per CUDA-core CTA, 8 per tensor-core one
     w = synth.make_workload("custom", device="cuda", shape=sh, sizes=sizes, seed_xor=44)
@@ -208,5 +209,91 @@ def test_decode_attention_multi_page_splits(kernel):
                 tol = 1e-4 * np.abs(vals).max() + 1e-5 * np.abs(ref)
                 assert np.all(np.abs(got - ref) <= tol), \
                     f"request {r} head {h}: error {np.abs(got - ref).max()}"
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_unattended_slots_do_not_reach_the_output(kernel):
+    """The slots past num_tokens in a request's last attended page may hold
+    any bits (the caller's cache): filled here with NaN and +-inf in K and V,
+    they must change nothing -- their weight is 0, and 0 x inf must not
+    reach the output through the weighted sum.  The output buffer starts 4
+    bytes into its allocation, so the 16-byte stores of the merge must not
+    be taken for granted either."""
+    sh = SHAPES["bf16_g4_d128"]
+    sizes = [3, 2, 1]
+    w = synth.make_workload("custom", device="cuda", shape=sh, sizes=sizes, seed_xor=45)
+    run = hz.EngineRun(w)
+    try:
+        gp.gp_set_scan_kernel(run.ctx, KERNELS[kernel])
+        run.feed_history()
+        n, G, layer = len(sizes), sh.group, 1
+        ntok = [2 * PAGE + 77, PAGE + 1, 130]
+        for req, t in zip(run.reqs, ntok):
+            pg, off = req.pages[t // PAGE], t % PAGE
+            w.k_cache[:, pg, :, off:] = float("nan")
+            w.v_cache[:, pg, :, off::2] = float("inf")
+            w.v_cache[:, pg, :, off + 1::2] = float("-inf")
+            w.v_cache[:, pg, :, off::3] = float("nan")
+        q = torch.randn(n, sh.num_q_heads, sh.head_dim, device="cuda").to(torch.bfloat16)
+        first = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        flat = torch.full((n * sh.num_q_heads * sh.head_dim + 1,), float("nan"), device="cuda")
+        out = flat[1:].view(n, sh.num_q_heads, sh.head_dim)
+        assert out.data_ptr() % 16 == 4
+        gp.gp_decode_attention(run.ctx, layer, run.reqs, ntok, q, first, out)
+        torch.cuda.synchronize()
+        assert torch.isnan(flat[0])  # nothing written before the buffer
+        out = out.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(out))
+        qn = q.double().cpu().numpy()
+        for r, req in enumerate(run.reqs):
+            for h in range(sh.num_kv_heads):
+                keys = hz.unit_keys_dev(w.k_cache, req.pages, layer, h)[:ntok[r]]
+                vals = hz.unit_keys_dev(w.v_cache, req.pages, layer, h)[:ntok[r]]
+                assert np.all(np.isfinite(keys)) and np.all(np.isfinite(vals))
+                ref, _ = _oracle_attention(qn[r, h * G:(h + 1) * G], keys, vals, req.pos, sh.rope_theta)
+                got = out[r, h * G:(h + 1) * G]
+                tol = 1e-4 * np.abs(vals).max() + 1e-5 * np.abs(ref)
+                assert np.all(np.abs(got - ref) <= tol), f"request {r} head {h}: error {np.abs(got - ref).max()}"
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_decode_attention_many_requests(kernel):
+    """More work items than SMs: the persistent tensor-core kernel's CTAs take
+    several items each (the second round in reverse order), among them empty
+    ones (no attended token), one-token ones, and the splits of a long
+    request; every output against the oracle."""
+    sh = SHAPES["bf16_g4_d128"]
+    rng = np.random.default_rng(46)
+    sizes = [int(x) for x in rng.integers(1, 4, size=95)] + [40]
+    w = synth.make_workload("custom", device="cuda", shape=sh, sizes=sizes, seed_xor=46)
+    run = hz.EngineRun(w)
+    try:
+        gp.gp_set_scan_kernel(run.ctx, KERNELS[kernel])
+        run.feed_history()
+        n, G, layer = len(sizes), sh.group, 1
+        ntok = [int(rng.integers(0, p * PAGE + 1)) for p in sizes]
+        ntok[0], ntok[1], ntok[-1] = 0, 1, 40 * PAGE - 3
+        q = torch.randn(n, sh.num_q_heads, sh.head_dim, device="cuda").to(torch.bfloat16)
+        first = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        out = torch.full((n, sh.num_q_heads, sh.head_dim), float("nan"), device="cuda")
+        gp.gp_decode_attention(run.ctx, layer, run.reqs, ntok, q, first, out)
+        torch.cuda.synchronize()
+        out = out.cpu().numpy().astype(np.float64)
+        qn = q.double().cpu().numpy()
+        for r, req in enumerate(run.reqs):
+            for h in range(sh.num_kv_heads):
+                got = out[r, h * G:(h + 1) * G]
+                if ntok[r] == 0:
+                    assert np.all(got == 0.0)
+                    continue
+                keys = hz.unit_keys_dev(w.k_cache, req.pages, layer, h)[:ntok[r]]
+                vals = hz.unit_keys_dev(w.v_cache, req.pages, layer, h)[:ntok[r]]
+                ref, _ = _oracle_attention(qn[r, h * G:(h + 1) * G], keys, vals, req.pos, sh.rope_theta)
+                tol = 1e-4 * np.abs(vals).max() + 1e-5 * np.abs(ref)
+                assert np.all(np.abs(got - ref) <= tol), f"request {r} head {h}: error {np.abs(got - ref).max()}"
     finally:
         run.close()
