@@ -359,8 +359,13 @@ gp_status gp_compact_kv(gp_ctx* ctx, int32_t n, gp_request* reqs,
  *   softmax(z), out[r][g] = sum_i a_i v_i.
  * q_dev: device [n][Hq][d] in q_dtype; first_dev: device uint8 [n];
  * num_tokens: HOST int32 [n], 0 <= num_tokens[r] <= num_pages * 256 (0 gives
- * a zero output); out_dev: device fp32 [n][Hq][d].  Requests need not be at
- * a boundary.  With a compaction pending on the side stream (see
+ * a zero output); the cache slots past num_tokens[r] may hold any bits, NaN
+ * and inf included: they do not reach the output.  out_dev: device fp32
+ * [n][Hq][d], 4-byte aligned.  Requests need not be at a boundary.  bf16
+ * caches with d = 128 and 2 or 4 query heads per KV head run on the
+ * tensor-core kernel, everything else (or everything, under
+ * gp_set_scan_kernel(CUDA_CORE)) on the CUDA-core one; both give the same
+ * results within fp32 tolerances.  With a compaction pending on the side stream (see
  * gp_set_compaction_stream), the call makes the engine stream wait for it
  * only if one of its requests holds a page that compaction reads or writes;
  * otherwise the attention runs concurrently with it (App. E.3).

@@ -157,6 +157,28 @@ __global__ void __launch_bounds__(256) k_prep_queries(PrepArgs a) {
     a.zero32[i] = 0u;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_zero64; i += gridDim.x * blockDim.x) a.zero64[i] = 0ull;
   const DevReq rq = a.reqs[r];
+  const int g = hb * 8 + warp;
+  const int slot = rq.slot;
+  const bool live = g < a.Hq && slot >= 0 && slot < a.M;
+  // The warp's loads -- the query row and both summary rows -- leave
+  // together, before the angles are computed, so the block waits on memory
+  // once.
+  float qv[PER], vs[2][PER];
+  if (live) {
+    const size_t qoff = (((size_t)l * a.n + r) * a.Hq + g) * D;
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const int i = lane + 32 * m;
+      qv[m] = a.q_f32 ? static_cast<const float*>(a.q)[qoff + i]
+                      : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[qoff + i]);
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const double* row = a.pool + (((size_t)l * a.M + slot) * 2 + x) * ((size_t)a.Hq * D) + (size_t)g * D;
+#pragma unroll
+      for (int m = 0; m < PER; ++m) vs[x][m] = (float)row[lane + 32 * m];
+    }
+  }
   if (threadIdx.x < D / 2) {
     const double ang = (double)rq.pos * a.inv_freq[threadIdx.x];
     const double k = rint(ang * 0.15915494309189535);                  // 1 / (2 pi)
@@ -168,24 +190,16 @@ __global__ void __launch_bounds__(256) k_prep_queries(PrepArgs a) {
     sn_s[threadIdx.x] = sn;
   }
   __syncthreads();
-  const int g = hb * 8 + warp;
   if (g >= a.Hq) return;
-  const int slot = rq.slot;
   const int G = a.Hq / a.Hkv;
   const int h = g / G, gi = g % G;
-  if (slot < 0 || slot >= a.M) {
+  if (!live) {
     if (lane == 0) atomicOr(a.err, ERR_BAD_SLOT);
     return;
   }
-  const size_t qoff = (((size_t)l * a.n + r) * a.Hq + g) * D;
   float sq = 0.f;
 #pragma unroll
-  for (int m = 0; m < PER; ++m) {
-    const int i = lane + 32 * m;
-    const float v = a.q_f32 ? static_cast<const float*>(a.q)[qoff + i]
-                            : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[qoff + i]);
-    sq = fmaf(v, v, sq);
-  }
+  for (int m = 0; m < PER; ++m) sq = fmaf(qv[m], qv[m], sq);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
   const float rms_q = sqrtf(sq / D);
@@ -193,15 +207,12 @@ __global__ void __launch_bounds__(256) k_prep_queries(PrepArgs a) {
   const int ROWS = 2 * G;
   const int NB = (3 * ROWS + 15) / 16 * 16;
   unsigned char* bq = a.bq ? a.bq + (((size_t)r * a.L + l) * a.Hkv + h) * bq_bytes(D, G) : nullptr;
+#pragma unroll
   for (int x = 0; x < 2; ++x) {
-    const double* row = a.pool + (((size_t)l * a.M + slot) * 2 + x) * ((size_t)a.Hq * D) + (size_t)g * D;
-    float v[PER];
+    const float* v = vs[x];
     float sv = 0.f;
 #pragma unroll
-    for (int m = 0; m < PER; ++m) {
-      v[m] = (float)row[lane + 32 * m];
-      sv = fmaf(v[m], v[m], sv);
-    }
+    for (int m = 0; m < PER; ++m) sv = fmaf(v[m], v[m], sv);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
     const float rms_v = sqrtf(sv / D);
