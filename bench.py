@@ -60,7 +60,7 @@ def _peaks():
 
 KERNEL_OF = {"boundary_demand": "k_demand_tc", "compress_hold": "k_compress"}
 # the sources each kernel is built from (its capture is void once they change)
-KERNEL_SOURCES = {"k_demand_tc": ["k_demand_tc.cu", "demand_common.cuh", "gp_kernels.h"],
+KERNEL_SOURCES = {"k_demand_tc": ["k_demand_tc.cu", "demand_common.cuh", "tc_ptx.cuh", "gp_kernels.h"],
                   "k_compress": ["k_compress.cu", "gp_kernels.h"]}
 
 
