@@ -157,11 +157,12 @@ inline DemandPlan demand_plan(int P, bool tc_ok) {
 
 // ---- decode attention with the summary update fused in (one layer) -------
 // One work item of the tensor-core kernel, built by the host: the split
-// `split` (of nsp) of request r's attended pages, for KV head h.
+// `split` (of nsp) of request r's attended pages, for KV head h, pages
+// [p0, p0 + ceil(T / 2)) of its block table.
 struct AttnItem {
   int32_t r, h, split, nsp;
   int32_t part_first;  // the first partial of (r, h); this item's is part_first + split
-  int32_t p0;          // first attended page of the split
+  int32_t p0;          // first page of the split
   int32_t T;           // tiles of 128 keys (0: no attended token)
   int32_t ntok;        // tokens the request attends to
   int32_t bt_off, slot;
@@ -196,7 +197,9 @@ struct AttnArgs {
   int n, n_ctas;           // n_ctas: work items (request, KV head, split); the
                            // CUDA-core kernel runs one CTA per item
   int grid;                // tensor-core kernel: persistent CTAs (<= n_ctas)
-  const AttnItem* items;   // tensor-core kernel: [n_ctas] work items, in the order above
+  const AttnItem* items;   // tensor-core kernel: [n_ctas] work items, those of CTA c at
+  const int32_t* cta_begin;//   [cta_begin[c], cta_begin[c + 1]) ([grid + 1]); a pair's
+                           //   items are consecutive, its partials part_first + split
   int* err;
 };
 cudaError_t launch_decode_attention(const AttnArgs& a, cudaStream_t s);

@@ -1371,36 +1371,85 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   if (overlap) GP_CUDA(c, cudaStreamWaitEvent(c->stream, c->ev_done, 0));
   const int maxp = g.max_pages_per_req;
   const int Hkv = g.num_kv_heads;
-  // Work items: splits of about `chunk` attended pages per (request, KV
-  // head), longest requests first.  The tensor-core kernel is persistent
-  // (one CTA per SM walks its share of the items, prefetching the next
-  // item's tiles) and aims at about one item per SM: each item adds a
-  // ticket and, for the last split of a (request, KV head), a merge, so more
-  // items cost more than their balance gains (items per SM 1, 2, 4, 8: 97.4,
-  // 86.3, 97.9, 93.2 % of HBM on a 64-request decode step; 92.3, 89.4,
-  // 88.6, 89.1 % on 16 requests of 128 pages).  The CUDA-core kernel runs one
-  // CTA per item, two per SM, and aims at six waves (2, 3, 6, 12 gave 69.5,
-  // 71.6, 74.0, 73.3 % on the 64-request step).
   std::vector<int> npg(n), order(n), nsp(n);
   long long total_pages = 0;
+  int max_npg = 0;
   for (int r = 0; r < n; ++r) {
     npg[r] = (num_tokens[r] + kPage - 1) / kPage;
     total_pages += npg[r];
+    max_npg = std::max(max_npg, npg[r]);
     order[r] = r;
   }
+  // Work of the tensor-core kernel (persistent, one CTA per SM): every
+  // (request, KV head) pair's attended pages laid end to end and cut into
+  // one even range of W pages per SM; a CTA takes the items of its range --
+  // whole pairs, and at most two pieces of pairs it shares with its
+  // neighbours, whose partials the last piece to finish merges.  W is large
+  // enough that no pair has more than 64 pieces.  A
+  // pair with no attended token still gets an item (its summary update and
+  // zero output).  Even ranges balance equal pairs that a per-pair split
+  // cannot (16 requests of 128 pages over 152 SMs: 90.1 % of HBM with one
+  // item per SM of whole or halved pairs).
+  std::vector<gp::AttnItem> items;
+  std::vector<int32_t> cta_begin;
+  if (tc) {
+    const long long total = total_pages * Hkv;
+    // a pair's first piece can be a single page at the end of a range: then
+    // W >= (max_npg - 1) / 63 keeps every pair within 64 pieces
+    const long long W = std::max({1LL, (total + c->sms - 1) / c->sms, (long long)(max_npg + 61) / 63});
+    int cta = 0;
+    long long room = W;  // pages left in the current CTA's range
+    cta_begin.push_back(0);
+    for (int r = 0; r < n; ++r)
+      for (int h = 0; h < Hkv; ++h) {
+        const int first = (int)items.size();
+        int p0 = 0, split = 0;
+        do {
+          if (room == 0 && npg[r] > p0) {  // the range is full: the next CTA's range starts here
+            ++cta;
+            cta_begin.push_back((int32_t)items.size());
+            room = W;
+          }
+          const int take = (int)std::min<long long>(npg[r] - p0, room);
+          const int span = std::min(num_tokens[r] - p0 * kPage, take * kPage);
+          gp::AttnItem it{};
+          it.r = r;
+          it.h = h;
+          it.split = split++;
+          it.part_first = first;
+          it.p0 = p0;
+          it.T = span > 0 ? (span + 127) / 128 : 0;
+          it.ntok = num_tokens[r];
+          it.bt_off = r * maxp;
+          it.slot = reqs[r].slot;
+          it.pos = reqs[r].pos;
+          items.push_back(it);
+          p0 += take;
+          room -= take;
+        } while (p0 < npg[r]);
+        for (size_t k = first; k < items.size(); ++k) items[k].nsp = split;
+      }
+    cta_begin.push_back((int32_t)items.size());
+  }
+  // The CUDA-core kernel runs one CTA per item: splits of about `chunk`
+  // attended pages per pair, longest requests first, for about six waves of
+  // two CTAs per SM (2, 3, 6, 12 waves gave 69.5, 71.6, 74.0, 73.3 % of HBM
+  // on a 64-request decode step).
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return npg[x] > npg[y]; });
-  const long long target_ctas = tc ? (long long)c->sms : 6LL * 2 * c->sms;
+  const long long target_ctas = 6LL * 2 * c->sms;
   const long long chunk = std::max(1LL, (total_pages * Hkv + target_ctas - 1) / target_ctas);
   long long n_ctas = 0;
   for (int r = 0; r < n; ++r) {
     nsp[r] = (int)std::max(1LL, std::min(64LL, (npg[r] + chunk - 1) / chunk));
     n_ctas += (long long)nsp[r] * Hkv;
   }
+  if (tc) n_ctas = (long long)items.size();
   const size_t part_floats = (size_t)n_ctas * G * (g.head_dim + 2);
   const size_t tick_off = (part_floats * sizeof(float) + 255) & ~size_t(255);
   if ((st = ensure(c, c->attn, tick_off + sizeof(unsigned) * (size_t)n * Hkv)) != GP_OK) return st;
+  const size_t items_bytes = sizeof(gp::AttnItem) * items.size();
   Staged s{};
-  if ((st = stage(c, n, false, &s, &c->upload_attn, tc ? sizeof(gp::AttnItem) * (size_t)n_ctas : 0)) != GP_OK)
+  if ((st = stage(c, n, false, &s, &c->upload_attn, items_bytes + sizeof(int32_t) * cta_begin.size())) != GP_OK)
     return st;
   s.part_base[0] = 0;
   for (int i = 0; i < n; ++i) {
@@ -1408,28 +1457,8 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
     s.part_base[i + 1] = s.part_base[i] + nsp[order[i]] * Hkv;
   }
   if (tc) {
-    // the tensor-core kernel's work items, in the same order: request order[i],
-    // then item split * Hkv + h of it
-    gp::AttnItem* it = static_cast<gp::AttnItem*>(s.extra);
-    for (int i = 0; i < n; ++i) {
-      const int r = order[i], ns = nsp[r];
-      for (int local = 0; local < ns * Hkv; ++local, ++it) {
-        const int h = local % Hkv, split = local / Hkv;
-        const int p0 = (int)((long long)split * npg[r] / ns), p1 = (int)((long long)(split + 1) * npg[r] / ns);
-        const int span = std::min(num_tokens[r] - p0 * kPage, (p1 - p0) * kPage);
-        it->r = r;
-        it->h = h;
-        it->split = split;
-        it->nsp = ns;
-        it->part_first = s.part_base[i] + h * ns;
-        it->p0 = p0;
-        it->T = span > 0 ? (span + 127) / 128 : 0;
-        it->ntok = num_tokens[r];
-        it->bt_off = r * maxp;
-        it->slot = reqs[r].slot;
-        it->pos = reqs[r].pos;
-      }
-    }
+    std::memcpy(s.extra, items.data(), items_bytes);
+    std::memcpy(static_cast<char*>(s.extra) + items_bytes, cta_begin.data(), sizeof(int32_t) * cta_begin.size());
   }
   for (int r = 0; r < n; ++r) {
     gp::DevReq& d = s.reqs[r];
@@ -1480,8 +1509,9 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   a.order = dev_at<int32_t>(s, s.off_sel);
   a.n = n;
   a.n_ctas = (int)n_ctas;
-  a.grid = (int)std::min<long long>(n_ctas, c->sms);
+  a.grid = tc ? (int)cta_begin.size() - 1 : 0;
   a.items = tc ? dev_at<gp::AttnItem>(s, s.off_extra) : nullptr;
+  a.cta_begin = tc ? dev_at<int32_t>(s, s.off_extra + items_bytes) : nullptr;
   a.err = c->err_dev;
   return timed_launch(c, GP_KERNEL_ATTENTION, "decode_attention",
                       [&] { return gp::launch_decode_attention(a, c->stream); });

@@ -8,12 +8,13 @@
 // (k_attention.cu): an item is (request, KV head, split of the request's
 // attended pages); the split-0 item updates the G heads' summaries (Eq. 6,
 // App. E.1); each item writes (max, sum, G x d) partials and the last item
-// of a (request, KV head) to finish merges them.  Here the grid is
-// persistent -- one CTA per SM takes items k * grid + cta (every other
-// round in reverse, so that the longest-first order spreads evenly) -- and
-// every role runs on into the next item, so the copies of the next split
-// stream while this one finishes.  Within an item the keys are taken in
-// tiles of 128:
+// of a (request, KV head) to finish merges them (a pair with one item
+// writes its output directly).  Here the grid is persistent: the host lays
+// all pairs' attended pages end to end, cuts them into one even range per
+// SM, and gives each CTA the items of its range (whole pairs, and at most
+// two pieces of pairs shared with its neighbours); every role runs on into
+// the next item, so the copies of the next split stream while this one
+// finishes.  Within an item the keys are taken in tiles of 128:
 //   S   = K q~^T   M = 128 keys, N = 16, K = d: the G rotated, scaled query
 //                  rows, each split into three bf16 parts h1 + h2 + h3 that
 //                  carry its fp32 value (so K . q~ is computed to fp32
@@ -282,31 +283,25 @@ __global__ void __launch_bounds__(NT, 1) k_decode_attn_tc(const __grid_constant_
   auto endbar = [&](int e) { return mmadone + 8u * (uint32_t)(1 + 4 * NS + e); };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int cta = (int)blockIdx.x, grid = a.grid;
-  // Every role walks the same items: the k-th round's item of this CTA,
-  // with every other round reversed; the next item's record is loaded while
-  // f runs on this one.  Items whose slot is out of range are skipped (the
-  // query warps record the error).  f returns false to stop.
-  auto item_index = [&](int k) { return (k & 1) ? k * grid + grid - 1 - cta : k * grid + cta; };
+  const int cta = (int)blockIdx.x;
+  // Every role walks the same items, this CTA's list from the host; the
+  // next item's record is loaded while f runs on this one.  Items whose slot
+  // is out of range are skipped (the first query thread records the error).
+  // f returns false to stop.
+  const int i_begin = a.cta_begin[cta], i_end = a.cta_begin[cta + 1];
   auto for_items = [&](auto&& f) {
-    int k = 0;
-    while ((long long)k * grid < a.n_ctas && item_index(k) >= a.n_ctas) ++k;
-    if ((long long)k * grid >= a.n_ctas) return;
-    Item cur = load_item(a, item_index(k));
-    while (true) {
-      int kn = k + 1;
-      while ((long long)kn * grid < a.n_ctas && item_index(kn) >= a.n_ctas) ++kn;
-      const bool more = (long long)kn * grid < a.n_ctas;
+    if (i_begin >= i_end) return;
+    Item cur = load_item(a, i_begin);
+    for (int i = i_begin; i < i_end; ++i) {
+      const bool more = i + 1 < i_end;
       Item nxt;
-      if (more) nxt = load_item(a, item_index(kn));
+      if (more) nxt = load_item(a, i + 1);
       if (!cur.ok) {
-        if (tid == 32 * W_Q0) atomicOr(a.err, ERR_BAD_SLOT);  // reported once, by the first query thread
+        if (tid == 32 * W_Q0) atomicOr(a.err, ERR_BAD_SLOT);
       } else if (!f(cur.w)) {
         break;
       }
-      if (!more) break;
-      cur = nxt;
-      k = kn;
+      if (more) cur = nxt;
     }
   };
 
@@ -640,6 +635,15 @@ __global__ void __launch_bounds__(NT, 1) k_decode_attn_tc(const __grid_constant_
           den[gg] = fmaf(den[gg], rs[gg], ts[gg]);
           mx[gg] = tm[gg];
         }
+      }
+      if (it.nsp == 1) {
+        // the pair's only split: its output directly, no partial, ticket or merge
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg)
+          a.out[((size_t)it.r * a.Hq + it.h * G + gg) * D + d] = den[gg] > 0.f ? acc[gg] / den[gg] : 0.f;
+        if (it.T == 0)  // warp 8 alone (the other warps skipped the item): every d of the pair
+          for (int e = lane; e < G * D; e += 32) a.out[((size_t)it.r * a.Hq + it.h * G) * D + e] = 0.f;
+        return true;
       }
       // the item's partial: output of dimension d, and (warp 8) maxima and sums
       float* po = a.part + (size_t)(it.part_first + it.split) * kPartFloats<G>;

@@ -179,11 +179,12 @@ def test_theorem31_bound_after_compress_and_hold():
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
 def test_decode_attention_multi_page_splits(kernel):
-    """Enough pages that a split spans several pages (the host aims at about
-    one work item per SM for the persistent tensor-core kernel, and at six
-    waves of two CTAs per SM, 1824 CTAs, for the CUDA-core one, where the
-    64-split cap applies to the longest request); ragged token counts end
-    inside a tile or stage."""
+    """Enough pages that a split spans several pages (the persistent
+    tensor-core kernel cuts all pairs' pages into one even range per SM, so
+    the long requests' pairs are shared between CTAs; the CUDA-core kernel
+    aims at six waves of two CTAs per SM, 1824 CTAs, where the 64-split cap
+    applies to the longest request); ragged token counts end inside a tile
+    or stage."""
     sh = SHAPES["bf16_g4_d128"]
     sizes = [160, 150, 130, 97, 40, 5]  # 582 pages x 2 KV heads: 1 or 2 pages per CUDA-core CTA, 8 per tensor-core one
     w = synth.make_workload("custom", device="cuda", shape=sh, sizes=sizes, seed_xor=44)
@@ -262,10 +263,10 @@ def test_unattended_slots_do_not_reach_the_output(kernel):
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
 def test_decode_attention_many_requests(kernel):
-    """More work items than SMs: the persistent tensor-core kernel's CTAs take
-    several items each (the second round in reverse order), among them empty
-    ones (no attended token), one-token ones, and the splits of a long
-    request; every output against the oracle."""
+    """More pairs than SMs: the persistent tensor-core kernel's CTAs take
+    several items each -- whole pairs, pieces of pairs shared with the
+    neighbouring range, empty ones (no attended token), one-token ones, and
+    the pieces of a long request; every output against the oracle."""
     sh = SHAPES["bf16_g4_d128"]
     rng = np.random.default_rng(46)
     sizes = [int(x) for x in rng.integers(1, 4, size=95)] + [40]
