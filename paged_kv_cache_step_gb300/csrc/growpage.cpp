@@ -22,6 +22,7 @@
 #include <vector>
 
 #include "gp_internal.h"
+#include "attn_kernels.h"
 #include "gp_kernels.h"
 
 namespace {

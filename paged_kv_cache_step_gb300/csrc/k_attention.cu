@@ -29,6 +29,7 @@
 
 #include <cstdint>
 
+#include "attn_kernels.h"
 #include "gp_kernels.h"
 
 namespace gp {

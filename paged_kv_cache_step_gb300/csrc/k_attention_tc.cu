@@ -47,6 +47,7 @@
 
 #include <cstdint>
 
+#include "attn_kernels.h"
 #include "gp_kernels.h"
 #include "tc_ptx.cuh"
 
