@@ -4,17 +4,17 @@
 // Sec. 4.1, where the decode attention kernel updates the query summaries
 // as a side effect, for one layer of a decode step.
 //
-// The work items and the outputs are those of the CUDA-core kernel
-// (k_attention.cu): an item is (request, KV head, split of the request's
-// attended pages); the split-0 item updates the G heads' summaries (Eq. 6,
-// App. E.1); each item writes (max, sum, G x d) partials and the last item
-// of a (request, KV head) to finish merges them (a pair with one item
-// writes its output directly).  Here the grid is persistent: the host lays
-// all pairs' attended pages end to end, cuts them into one even range per
-// SM, and gives each CTA the items of its range (whole pairs, and at most
-// two pieces of pairs shared with its neighbours); every role runs on into
-// the next item, so the copies of the next split stream while this one
-// finishes.  Within an item the keys are taken in tiles of 128:
+// The outputs are those of the CUDA-core kernel (k_attention.cu); the work
+// is split differently.  The grid is persistent, one CTA per SM: the host
+// lays every (request, KV head) pair's attended pages end to end, cuts them
+// into one even range per SM, and gives each CTA the items of its range --
+// whole pairs, and at most two pieces of pairs it shares with its
+// neighbours.  The first piece of a pair updates the G heads' summaries
+// (Eq. 6, App. E.1); a pair in one piece writes its output directly, the
+// pieces of a shared pair write (max, sum, G x d) partials and the last of
+// them to finish merges them.  Every role runs on into the next item, so the
+// copies of the next piece stream while this one finishes.  Within an item
+// the keys are taken in tiles of 128:
 //   S   = K q~^T   M = 128 keys, N = 16, K = d: the G rotated, scaled query
 //                  rows, each split into three bf16 parts h1 + h2 + h3 that
 //                  carry its fp32 value (so K . q~ is computed to fp32
