@@ -125,3 +125,38 @@ def test_fused_attention_update_gives_the_same_bits():
     finally:
         gp.gp_destroy(ctxa)
         gp.gp_destroy(ctxb)
+
+
+def test_summary_update_full_size_sampled():
+    """The batch workload's size: 64 requests of the Llama-8B shape (32
+    layers, 32 query heads, d = 128; a 134 MB pool, larger than L2), one
+    first step and two updates, 20,000 sampled elements of each summary
+    checked against the exactly rounded value."""
+    L8, HQ8, D8, n = 32, 32, 128, 64
+    k = torch.zeros(L8, 2, 8, 256, D8, dtype=torch.bfloat16, device="cuda")
+    cfg = gp.gp_config_default(num_layers=L8, num_q_heads=HQ8, num_kv_heads=8, head_dim=D8, kv_dtype=0, q_dtype=0,
+                               max_slots=n, num_pages=2, max_pages_per_req=2, rope_theta=5e5)
+    ctx = gp.gp_create(cfg, k, torch.zeros_like(k), None)
+    g = torch.Generator().manual_seed(13)
+    rng = np.random.default_rng(13)
+    try:
+        slots = [gp.gp_slot_acquire(ctx) for _ in range(n)]
+        sl = torch.tensor(slots, dtype=torch.int32, device="cuda")
+        first = torch.ones(n, dtype=torch.uint8, device="cuda")
+        q = torch.randn(L8, n, HQ8, D8, generator=g).to(torch.bfloat16)
+        gp.gp_update_summaries(ctx, n, sl, q.cuda(), first)
+        for step in range(2):
+            old = np.stack([gp.gp_read_summaries(ctx, s, L8, HQ8, D8) for s in slots], axis=1)
+            q = (torch.randn(L8, n, HQ8, D8, generator=g) * (1 + step)).to(torch.bfloat16)
+            gp.gp_update_summaries(ctx, n, sl, q.cuda(), torch.zeros_like(first))
+            got = np.stack([gp.gp_read_summaries(ctx, s, L8, HQ8, D8) for s in slots], axis=1)
+            qd = q.double().numpy()
+            for x, beta in enumerate(BETA):
+                fb, w = Fraction(beta), 1.0 - beta
+                idx = rng.integers(0, qd.size, size=20000)
+                o, gx, qq = old[:, :, x].reshape(-1), got[:, :, x].reshape(-1), qd.reshape(-1)
+                for i in idx:
+                    want = float(fb * Fraction(float(o[i])) + Fraction(w * float(qq[i])))
+                    assert gx[i] == want, f"step {step} summary {x} element {i}: {gx[i]!r} != {want!r}"
+    finally:
+        gp.gp_destroy(ctx)
