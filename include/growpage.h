@@ -426,6 +426,20 @@ gp_status gp_read_summaries(gp_ctx* ctx, int32_t slot, double* out);
  * text names the error bits), GP_OK otherwise.  The error word is cleared. */
 gp_status gp_synchronize(gp_ctx* ctx);
 
+/* gp_debug_attention_plan: the work split gp_decode_attention gives the
+ * tensor-core attention kernel for n requests attending to num_tokens[r]
+ * tokens on a device of `sms` SMs, computed on the host without launching
+ * anything (also on a host-only context).  Every (request, KV head) pair's
+ * attended pages are laid end to end and cut into one even range per SM;
+ * each range's pieces are one CTA's items.  items_out: host int32
+ * [max_items][8], per item (request, KV head, piece, pieces of the pair,
+ * first page, tiles of 128 keys, first item of the pair, CTA), items of a
+ * CTA consecutive and CTAs in order.  *n_items, *n_ctas: the counts (set
+ * also when max_items is too small, which returns GP_ERR_INVALID).  Host
+ * only. */
+gp_status gp_debug_attention_plan(gp_ctx* ctx, int32_t n, const int32_t* num_tokens, int32_t sms,
+                                  int32_t max_items, int32_t* items_out, int32_t* n_items, int32_t* n_ctas);
+
 /* ---- test hooks -------------------------------------------------------------
  * gp_debug_set_wait_limit: the limit, in SM clock cycles, of the bounded copy
  * waits of later launches of `kernel` (GP_KERNEL_COMPRESS: the compaction;

@@ -42,6 +42,7 @@ EXPORTS = [
     "gp_debug_demand_k", "gp_debug_entropy",
     "gp_debug_scores", "gp_debug_probs", "gp_debug_keep_mask", "gp_read_summaries",
     "gp_set_scan_kernel", "gp_set_timing", "gp_kernel_time", "gp_reset_timing", "gp_stats",
+    "gp_debug_attention_plan",
     "gp_set_compaction_stream", "gp_wait_compaction", "gp_decode_attention",
     "gp_synchronize", "gp_debug_set_wait_limit", "gp_debug_fail_next_launch", "gp_set_selection_mode",
 ]
@@ -138,6 +139,7 @@ def load(build_if_missing: bool = True):
         "gp_debug_keep_mask": (I32, [P, I32, P]),
         "gp_read_summaries": (I32, [P, I32, P]),
         "gp_set_scan_kernel": (I32, [P, I32]),
+        "gp_debug_attention_plan": (I32, [P, I32, P, I32, I32, P, P, P]),
         "gp_set_timing": (I32, [P, I32]),
         "gp_kernel_time": (I32, [P, I32, C.POINTER(C.c_double), C.POINTER(I64)]),
         "gp_reset_timing": (I32, [P]),
@@ -394,6 +396,20 @@ def gp_read_summaries(ctx, slot: int, L: int, hq: int, d: int) -> np.ndarray:
     _check(ctx, load().gp_read_summaries(ctx, slot, out.ctypes.data))
     return out
 
+
+
+def gp_debug_attention_plan(ctx, num_tokens, sms: int) -> np.ndarray:
+    """The tensor-core attention kernel's work items for these token counts on
+    `sms` SMs (host only): int32 [items][8] rows (request, KV head, piece,
+    pieces, first page, tiles, first item of the pair, CTA)."""
+    nt = np.ascontiguousarray(np.asarray(num_tokens, dtype=np.int32))
+    n_items, n_ctas = C.c_int32(0), C.c_int32(0)
+    lib = load()
+    lib.gp_debug_attention_plan(ctx, len(nt), nt.ctypes.data, int(sms), 0, None, C.byref(n_items), C.byref(n_ctas))
+    out = np.zeros((max(n_items.value, 1), 8), dtype=np.int32)
+    _check(ctx, lib.gp_debug_attention_plan(ctx, len(nt), nt.ctypes.data, int(sms), out.shape[0], out.ctypes.data,
+                                            C.byref(n_items), C.byref(n_ctas)))
+    return out[:n_items.value]
 
 
 def gp_set_scan_kernel(ctx, kind: int):

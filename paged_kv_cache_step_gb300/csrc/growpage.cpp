@@ -303,6 +303,63 @@ bool make_map(gp_ctx* c, void* cache, CUtensorMap* map) {
   return r == CUDA_SUCCESS;
 }
 
+// Work of the tensor-core attention kernel (persistent, one CTA per SM):
+// every (request, KV head) pair's attended pages laid end to end and cut
+// into one even range of W pages per SM; a CTA takes the items of its range
+// -- whole pairs, and at most two pieces of pairs it shares with its
+// neighbours, whose partials the last piece to finish merges.  A pair's
+// first piece can be a single page at the end of a range, so W >= (longest
+// pair - 1) / 63 keeps every pair within 64 pieces.  A pair with no attended
+// token still gets an item (its summary update and zero output).  Even
+// ranges balance equal pairs that a per-pair split cannot (16 requests of
+// 128 pages over 152 SMs: 90.1 % of HBM with one item per SM of whole or
+// halved pairs).  Fills everything but bt_off, slot and pos; cta_begin gets
+// the first item of each CTA and the item count.
+void attention_plan(int n, const int32_t* num_tokens, int Hkv, int sms, std::vector<gp::AttnItem>& items,
+                    std::vector<int32_t>& cta_begin) {
+  items.clear();
+  cta_begin.clear();
+  long long total_pages = 0;
+  int max_npg = 0;
+  for (int r = 0; r < n; ++r) {
+    const int npg = (num_tokens[r] + kPage - 1) / kPage;
+    total_pages += npg;
+    max_npg = std::max(max_npg, npg);
+  }
+  const long long total = total_pages * Hkv;
+  const long long W = std::max({1LL, (total + sms - 1) / sms, (long long)(max_npg + 61) / 63});
+  long long room = W;  // pages left in the current CTA's range
+  cta_begin.push_back(0);
+  for (int r = 0; r < n; ++r) {
+    const int npg = (num_tokens[r] + kPage - 1) / kPage;
+    for (int h = 0; h < Hkv; ++h) {
+      const int first = (int)items.size();
+      int p0 = 0, split = 0;
+      do {
+        if (room == 0 && npg > p0) {  // the range is full: the next CTA's range starts here
+          cta_begin.push_back((int32_t)items.size());
+          room = W;
+        }
+        const int take = (int)std::min<long long>(npg - p0, room);
+        const int span = std::min(num_tokens[r] - p0 * kPage, take * kPage);
+        gp::AttnItem it{};
+        it.r = r;
+        it.h = h;
+        it.split = split++;
+        it.part_first = first;
+        it.p0 = p0;
+        it.T = span > 0 ? (span + 127) / 128 : 0;
+        it.ntok = num_tokens[r];
+        items.push_back(it);
+        p0 += take;
+        room -= take;
+      } while (p0 < npg);
+      for (size_t k = first; k < items.size(); ++k) items[k].nsp = split;
+    }
+  }
+  cta_begin.push_back((int32_t)items.size());
+}
+
 }  // namespace
 
 // The C linkage of every gp_* definition below comes from its declaration
@@ -1298,6 +1355,38 @@ gp_status gp_synchronize(gp_ctx* c) {
   return check_kernel_errors(c);  // synchronises the engine stream
 }
 
+gp_status gp_debug_attention_plan(gp_ctx* c, int32_t n, const int32_t* num_tokens, int32_t sms, int32_t max_items,
+                                  int32_t* items_out, int32_t* n_items, int32_t* n_ctas) {
+  if (!c) return GP_ERR_INVALID;
+  if (n < 0 || sms < 1 || max_items < 0 || !n_items || !n_ctas || (n > 0 && !num_tokens))
+    return fail(c, GP_ERR_INVALID, "gp_debug_attention_plan: bad arguments");
+  for (int r = 0; r < n; ++r)
+    if (num_tokens[r] < 0 || num_tokens[r] > c->cfg.max_pages_per_req * kPage)
+      return fail(c, GP_ERR_INVALID, "request %d: num_tokens %d outside [0, %d]", r, num_tokens[r],
+                  c->cfg.max_pages_per_req * kPage);
+  std::vector<gp::AttnItem> items;
+  std::vector<int32_t> cta_begin;
+  attention_plan(n, num_tokens, c->cfg.num_kv_heads, sms, items, cta_begin);
+  *n_items = (int32_t)items.size();
+  *n_ctas = (int32_t)cta_begin.size() - 1;
+  if ((int64_t)items.size() > max_items)
+    return fail(c, GP_ERR_INVALID, "gp_debug_attention_plan: %zu items, room for %d", items.size(), max_items);
+  for (int cta = 0; cta + 1 < (int)cta_begin.size(); ++cta)
+    for (int k = cta_begin[cta]; k < cta_begin[cta + 1]; ++k) {
+      const gp::AttnItem& it = items[k];
+      int32_t* o = items_out + (size_t)k * 8;
+      o[0] = it.r;
+      o[1] = it.h;
+      o[2] = it.split;
+      o[3] = it.nsp;
+      o[4] = it.p0;
+      o[5] = it.T;
+      o[6] = it.part_first;
+      o[7] = cta;
+    }
+  return GP_OK;
+}
+
 gp_status gp_debug_set_wait_limit(gp_ctx* c, int32_t kernel, int64_t cycles) {
   if (!c) return GP_ERR_INVALID;
   const long long v = cycles >= 0 ? (long long)cycles : gp::kDefaultWaitLimit;
@@ -1374,63 +1463,20 @@ gp_status gp_decode_attention(gp_ctx* c, int32_t layer, int32_t n, const gp_requ
   const int Hkv = g.num_kv_heads;
   std::vector<int> npg(n), order(n), nsp(n);
   long long total_pages = 0;
-  int max_npg = 0;
   for (int r = 0; r < n; ++r) {
     npg[r] = (num_tokens[r] + kPage - 1) / kPage;
     total_pages += npg[r];
-    max_npg = std::max(max_npg, npg[r]);
     order[r] = r;
   }
-  // Work of the tensor-core kernel (persistent, one CTA per SM): every
-  // (request, KV head) pair's attended pages laid end to end and cut into
-  // one even range of W pages per SM; a CTA takes the items of its range --
-  // whole pairs, and at most two pieces of pairs it shares with its
-  // neighbours, whose partials the last piece to finish merges.  W is large
-  // enough that no pair has more than 64 pieces.  A
-  // pair with no attended token still gets an item (its summary update and
-  // zero output).  Even ranges balance equal pairs that a per-pair split
-  // cannot (16 requests of 128 pages over 152 SMs: 90.1 % of HBM with one
-  // item per SM of whole or halved pairs).
   std::vector<gp::AttnItem> items;
   std::vector<int32_t> cta_begin;
   if (tc) {
-    const long long total = total_pages * Hkv;
-    // a pair's first piece can be a single page at the end of a range: then
-    // W >= (max_npg - 1) / 63 keeps every pair within 64 pieces
-    const long long W = std::max({1LL, (total + c->sms - 1) / c->sms, (long long)(max_npg + 61) / 63});
-    int cta = 0;
-    long long room = W;  // pages left in the current CTA's range
-    cta_begin.push_back(0);
-    for (int r = 0; r < n; ++r)
-      for (int h = 0; h < Hkv; ++h) {
-        const int first = (int)items.size();
-        int p0 = 0, split = 0;
-        do {
-          if (room == 0 && npg[r] > p0) {  // the range is full: the next CTA's range starts here
-            ++cta;
-            cta_begin.push_back((int32_t)items.size());
-            room = W;
-          }
-          const int take = (int)std::min<long long>(npg[r] - p0, room);
-          const int span = std::min(num_tokens[r] - p0 * kPage, take * kPage);
-          gp::AttnItem it{};
-          it.r = r;
-          it.h = h;
-          it.split = split++;
-          it.part_first = first;
-          it.p0 = p0;
-          it.T = span > 0 ? (span + 127) / 128 : 0;
-          it.ntok = num_tokens[r];
-          it.bt_off = r * maxp;
-          it.slot = reqs[r].slot;
-          it.pos = reqs[r].pos;
-          items.push_back(it);
-          p0 += take;
-          room -= take;
-        } while (p0 < npg[r]);
-        for (size_t k = first; k < items.size(); ++k) items[k].nsp = split;
-      }
-    cta_begin.push_back((int32_t)items.size());
+    attention_plan(n, num_tokens, Hkv, c->sms, items, cta_begin);
+    for (gp::AttnItem& it : items) {
+      it.bt_off = it.r * maxp;
+      it.slot = reqs[it.r].slot;
+      it.pos = reqs[it.r].pos;
+    }
   }
   // The CUDA-core kernel runs one CTA per item: splits of about `chunk`
   // attended pages per pair, longest requests first, for about six waves of
