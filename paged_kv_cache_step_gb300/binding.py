@@ -194,23 +194,61 @@ class Request:
         self.pos = int(pos)
 
     @property
+    def table(self):
+        return self._table
+
+    @table.setter
+    def table(self, t):
+        self._table = np.ascontiguousarray(t, dtype=np.int32)
+        self._bt = self._table.ctypes.data  # the C side reads and extends it in place
+
+    @property
     def pages(self):
         return self.table[:self.num_pages].tolist()
 
 
+# gp_request as a numpy record, so that a call's requests are marshalled one
+# field at a time instead of one ctypes attribute at a time
+_REQ_DTYPE = np.dtype({"names": ["slot", "num_pages", "block_table", "pos"],
+                       "formats": [np.int32, np.int32, np.uint64, np.int64],
+                       "offsets": [GpRequest.slot.offset, GpRequest.num_pages.offset,
+                                   GpRequest.block_table.offset, GpRequest.pos.offset],
+                       "itemsize": C.sizeof(GpRequest)})
+
+
 def _marshal(reqs):
-    arr = (GpRequest * max(1, len(reqs)))()
-    for i, r in enumerate(reqs):
-        arr[i].slot = r.slot
-        arr[i].num_pages = r.num_pages
-        arr[i].block_table = r.table.ctypes.data_as(C.POINTER(C.c_int32))
-        arr[i].pos = r.pos
+    n = len(reqs)
+    arr = (GpRequest * max(1, n))()
+    if n:
+        v = np.frombuffer(arr, dtype=_REQ_DTYPE, count=n)
+        v["slot"] = [r.slot for r in reqs]
+        v["num_pages"] = [r.num_pages for r in reqs]
+        v["block_table"] = [r._bt for r in reqs]
+        v["pos"] = [r.pos for r in reqs]
     return arr
 
 
 def _unmarshal(arr, reqs):
-    for i, r in enumerate(reqs):
-        r.num_pages = arr[i].num_pages
+    if reqs:
+        counts = np.frombuffer(arr, dtype=_REQ_DTYPE, count=len(reqs))["num_pages"].tolist()
+        for r, p in zip(reqs, counts):
+            r.num_pages = p
+
+
+class _Demands(list):
+    """gp_boundary_demand's results: gp_demand views into one ctypes array,
+    which gp_decide passes on as it is while the list is unchanged."""
+
+    def __init__(self, arr, n):
+        super().__init__(arr[i] for i in range(n))
+        self._arr = arr
+
+    def __setitem__(self, i, v):
+        self._arr = None
+        super().__setitem__(i, v)
+
+    def _whole(self, n):
+        return self._arr if self._arr is not None and len(self) == n else None
 
 
 # ---------------------------------------------------------------------------
@@ -281,7 +319,7 @@ def gp_boundary_demand(ctx, reqs, q_cur_dev):
     arr = _marshal(reqs)
     out = (GpDemand * max(1, len(reqs)))()
     _check(ctx, load().gp_boundary_demand(ctx, len(reqs), arr, _ptr(q_cur_dev), out))
-    return [out[i] for i in range(len(reqs))]
+    return _Demands(out, len(reqs))
 
 
 def gp_boundary_demand_noalloc(ctx, reqs, q_cur_dev, k_units=None):
@@ -295,7 +333,9 @@ def gp_boundary_demand_noalloc(ctx, reqs, q_cur_dev, k_units=None):
 
 def gp_decide(ctx, reqs, demand):
     arr = _marshal(reqs)
-    dem = (GpDemand * max(1, len(reqs)))(*demand)
+    dem = demand._whole(len(reqs)) if isinstance(demand, _Demands) else None
+    if dem is None:
+        dem = (GpDemand * max(1, len(reqs)))(*demand)
     out = (GpAction * max(1, len(reqs)))()
     _check(ctx, load().gp_decide(ctx, len(reqs), arr, dem, out))
     return [out[i] for i in range(len(reqs))]
