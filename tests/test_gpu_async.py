@@ -1,5 +1,8 @@
 """Asynchronous compaction on a side stream (App. E.3), through the C ABI.
 
+Also decode attention issued while the compaction is pending: over requests
+it does not touch (no wait) and over compacted ones (a wait on it).
+
 Two engines over identical synthetic caches run the same boundary event:
 one compacts on its own stream, the other on a side stream while summary
 updates of the next decode steps are issued on the engine stream.  After
@@ -150,3 +153,51 @@ def test_side_stream_compaction_with_a_shared_prefix_matches_oracle():
                                               og.gather_logical(got, req.pages, layer, h)[:n_live])
     finally:
         gp.gp_destroy(ctx)
+
+
+def test_decode_attention_beside_a_side_stream_compaction():
+    """App. E.3: while a Compress & Hold runs on the side stream, decode
+    attention over a request it does not touch runs without waiting for it,
+    and attention over a compacted request waits for it (its pages overlap);
+    both give exactly the outputs of the engine that compacted on its own
+    stream (the tensor-core attention kernel, summaries updated in passing)."""
+    side = torch.cuda.Stream()
+    (wa, ra), (wb, rb) = _engine(None), _engine(side)
+    try:
+        sh = wa.shape
+        q = wa.history[-1]
+        comp_a = [r for r in ra.reqs if r.num_pages >= 3]
+        comp_b = [r for r in rb.reqs if r.num_pages >= 3]
+        idle_a = [r for r in ra.reqs if r.num_pages < 3]
+        idle_b = [r for r in rb.reqs if r.num_pages < 3]
+        assert comp_a and idle_a
+        gp.gp_boundary_demand(ra.ctx, comp_a, q)
+        gp.gp_boundary_demand(rb.ctx, comp_b, q)
+        gp.gp_compress_hold(ra.ctx, comp_a)
+        gp.gp_compress_hold(rb.ctx, comp_b)   # on the side stream
+        qa = torch.randn(len(ra.reqs), sh.num_q_heads, sh.head_dim, generator=torch.Generator().manual_seed(9))
+        qa = qa.to(torch.bfloat16).cuda()
+        outs = []
+        for run, idle, comp in ((ra, idle_a, comp_a), (rb, idle_b, comp_b)):
+            o_idle = torch.empty(len(idle), sh.num_q_heads, sh.head_dim, device="cuda")
+            o_comp = torch.empty(len(comp), sh.num_q_heads, sh.head_dim, device="cuda")
+            nf_i = torch.zeros(len(idle), dtype=torch.uint8, device="cuda")
+            nf_c = torch.zeros(len(comp), dtype=torch.uint8, device="cuda")
+            for layer in range(sh.num_layers):
+                # the untouched requests first: no wait for the side stream
+                gp.gp_decode_attention(run.ctx, layer, idle, [x.num_pages * 256 for x in idle],
+                                       qa[:len(idle)].contiguous(), nf_i, o_idle)
+                gp.gp_decode_attention(run.ctx, layer, comp, [x.num_pages * 256 for x in comp],
+                                       qa[len(idle):len(idle) + len(comp)].contiguous(), nf_c, o_comp)
+            gp.gp_synchronize(run.ctx)
+            torch.cuda.synchronize()
+            outs.append((o_idle.cpu(), o_comp.cpu()))
+        assert torch.equal(outs[0][0], outs[1][0]), "attention beside the compaction differs"
+        assert torch.equal(outs[0][1], outs[1][1]), "attention after the compaction differs"
+        for x, y in zip(ra.reqs, rb.reqs):
+            sa = gp.gp_read_summaries(ra.ctx, x.slot, sh.num_layers, sh.num_q_heads, sh.head_dim)
+            sb = gp.gp_read_summaries(rb.ctx, y.slot, sh.num_layers, sh.num_q_heads, sh.head_dim)
+            assert np.array_equal(sa, sb)
+    finally:
+        ra.close()
+        rb.close()
