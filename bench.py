@@ -209,8 +209,12 @@ class Stream:
         self.fill = fill   # hole-fill compaction (order-destroying variant) instead of the stable one
 
     def _query(self):
+        # drawn on the engine stream, which reads it: a tensor that the
+        # caching allocator hands out on one stream and another stream reads
+        # can be overwritten by the next allocation before the read is done
         kind = (self.t // PHASE) % 2 == 0      # concentrated phases first
-        return synth.query_step(self.w, [kind])
+        with torch.cuda.stream(self.torch_stream):
+            return synth.query_step(self.w, [kind])
 
     def _update(self, q):
         with torch.cuda.stream(self.torch_stream):
@@ -365,7 +369,9 @@ def run_gpu(args, world, rank, local):
         dev_q = torch.empty_like(s._query(), device=device)
         e2e_times = []
         for _ in range(args.steps):
-            hq = s._query().cpu().pin_memory()
+            q = s._query()
+            torch.cuda.synchronize()
+            hq = q.cpu().pin_memory()
             torch.cuda.synchronize()
             ev0 = torch.cuda.Event(enable_timing=True)
             ev1 = torch.cuda.Event(enable_timing=True)
@@ -561,7 +567,9 @@ class Batch:
         self.t += 1
 
     def query(self):
-        return synth.query_step(self.w, synth.batch_kinds(self.w, self.t))
+        # drawn on the engine stream, which reads it (see Stream._query)
+        with torch.cuda.stream(self.stream):
+            return synth.query_step(self.w, synth.batch_kinds(self.w, self.t))
 
     def decode(self, count: int):
         """Non-boundary decode steps: summary updates only."""
@@ -651,10 +659,10 @@ def measure_overlap_batch(args, device, extra):
             if grown:
                 reqs = [b.reqs[i] for i in grown]
                 ntok = [(r.num_pages - 1) * PAGE for r in reqs]
-                qa = torch.randn(sh.num_layers, len(reqs), sh.num_q_heads, sh.head_dim,
-                                 device=device).to(torch.bfloat16)
-                out = torch.empty(len(reqs), sh.num_q_heads, sh.head_dim, device=device)
-                b.stream.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(b.stream):
+                    qa = torch.randn(sh.num_layers, len(reqs), sh.num_q_heads, sh.head_dim,
+                                     device=device).to(torch.bfloat16)
+                    out = torch.empty(len(reqs), sh.num_q_heads, sh.head_dim, device=device)
                 for layer in range(sh.num_layers):
                     gp.gp_decode_attention(b.ctx, layer, reqs, ntok, qa[layer], first[:len(reqs)], out)
             gp.gp_wait_compaction(b.ctx, b.stream)
@@ -796,7 +804,9 @@ def run_batch(args, world, rank, local):
         dev_q = None
         e2e_times = []
         for _ in range(args.steps):
-            hq = b.query().cpu().pin_memory()
+            q = b.query()
+            torch.cuda.synchronize()
+            hq = q.cpu().pin_memory()
             if dev_q is None:
                 dev_q = torch.empty(hq.shape, dtype=hq.dtype, device=device)
             torch.cuda.synchronize()
