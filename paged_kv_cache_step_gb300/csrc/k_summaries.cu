@@ -39,11 +39,9 @@ __device__ __forceinline__ double widen_exact(float f) {
 // integer significand, 0 < w) and a bf16 query with bit pattern qb, by
 // integer operations: the significands' product has 60 or 61 bits and is
 // rounded to 53 (to nearest, ties to even), which is exactly what the fp64
-// multiply returns.  GB300 issues fp64 arithmetic at a small fraction of its
-// integer rate, and the EMA would otherwise spend four fp64 operations per
-// element; this leaves the two fused multiply-adds.  False (and the caller
-// multiplies in fp64) for a subnormal, infinite or NaN q, or a product
-// outside the normal range.
+// multiply returns.  False for a subnormal, infinite or NaN q, or a product
+// outside the normal range.  k_ema_update uses it to build, per block, the
+// products for the 128 bf16 significands, off GB300's narrow fp64 pipe.
 __device__ __forceinline__ bool mul_w_bf16(unsigned long long mw, int ew, unsigned qb, double& out) {
   const unsigned eq = (qb >> 7) & 0xffu, sq = (qb >> 15) & 1u;
   if (eq == 0u) {
@@ -72,17 +70,48 @@ __device__ __forceinline__ bool mul_w_bf16(unsigned long long mw, int ew, unsign
   return true;
 }
 
+// The fp64 multiply for the queries the table does not cover (zero,
+// subnormal, infinite or NaN bf16, or fp32 queries).  A function of its own
+// so that the compiler keeps it behind a branch: if-converted into the main
+// path it would issue two fp64 multiplies for every element.
+__device__ __noinline__ double mul_fp64(double w, double q) { return w * q; }
+
 // grid (ceil(Hq D / 1024), n, L), 256 threads: thread t of block (c, r, l)
 // owns elements [4 (256 c + t), +4) of the (layer l, request r) row.
 // (mws, ews), (mwl, ewl): 1 - beta_s and 1 - beta_l as significand and
-// biased exponent, for mul_w_bf16.
+// biased exponent.  tab: both are at least 2^-896, so that every product
+// with a normal bf16 query is a normal double.
+//
+// (1 - beta) q for a normal bf16 query q = (-1)^s (1 + f/128) 2^(e - 127)
+// is RN((1 - beta)(1 + f/128)) with e - 127 added to its exponent and s put
+// in its sign bit: scaling by a power of two is exact while the result
+// stays normal.  The block first forms the 128 rounded products of each
+// weight with 1 + f/128, with integer operations, in shared memory; each
+// element then takes one 16-byte shared load and two integer adds, and
+// only the two fused multiply-adds run on the fp64 pipe.
 __global__ void __launch_bounds__(256) k_ema_update(EmaArgs a, unsigned long long mws, int ews,
-                                                    unsigned long long mwl, int ewl) {
+                                                    unsigned long long mwl, int ewl, int tab) {
+  // {low word, high word - (127 << 20)} of both products, per fraction f
+  __shared__ uint4 wq[128];
   const int r = blockIdx.y, l = blockIdx.z;
   const int row = a.Hq * a.D;
   const int e0 = (blockIdx.x * 256 + threadIdx.x) * 4;
   const int slot = a.slots[r];
   const bool first = a.first[r] != 0;  // loaded beside the slot, not after it
+  if (threadIdx.x < 128) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (tab) {
+      double ps, pl;
+      mul_w_bf16(mws, ews, 0x3f80u | threadIdx.x, ps);  // q = 1 + f/128
+      mul_w_bf16(mwl, ewl, 0x3f80u | threadIdx.x, pl);
+      const unsigned long long bs = (unsigned long long)__double_as_longlong(ps);
+      const unsigned long long bl = (unsigned long long)__double_as_longlong(pl);
+      v = make_uint4((unsigned)bs, (unsigned)(bs >> 32) - (127u << 20), (unsigned)bl,
+                     (unsigned)(bl >> 32) - (127u << 20));
+    }
+    wq[threadIdx.x] = v;
+  }
+  __syncthreads();
   if (slot < 0 || slot >= a.M) {
     if (blockIdx.x == 0 && l == 0 && threadIdx.x == 0) atomicOr(a.err, ERR_BAD_SLOT);
     return;
@@ -103,34 +132,42 @@ __global__ void __launch_bounds__(256) k_ema_update(EmaArgs a, unsigned long lon
 #pragma unroll
     for (int i = 0; i < 4; ++i) qf[i] = __uint_as_float(qb[i] << 16);
   }
-  double q[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) q[i] = widen_exact(qf[i]);
   double2* row_s = reinterpret_cast<double2*>(a.pool + ((size_t)l * a.M + slot) * 2 * row + e0);
   double2* row_l = reinterpret_cast<double2*>(reinterpret_cast<double*>(row_s) + row);
   // the old summaries are loaded whatever `first` says, so that their loads
   // leave with the query's instead of waiting for the flag
   const double2 os0 = __ldcs(row_s), os1 = __ldcs(row_s + 1);
   const double2 ol0 = __ldcs(row_l), ol1 = __ldcs(row_l + 1);
-  double2 s0, s1, l0, l1;
+  const double os[4] = {os0.x, os0.y, os1.x, os1.y}, ol[4] = {ol0.x, ol0.y, ol1.x, ol1.y};
+  double ns[4], nl[4];
+  bool other = a.q_f32 || !tab;  // a query the table does not cover
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const unsigned e7 = qb[i] & 0x7f80u;
+    other |= e7 == 0u || e7 == 0x7f80u;
+  }
   if (first) {
-    s0 = make_double2(q[0], q[1]);
-    s1 = make_double2(q[2], q[3]);
-    l0 = s0;
-    l1 = s1;
-  } else {
-    const double ws = 1.0 - a.beta_s, wl = 1.0 - a.beta_l;
-    double cs[4], cl[4];  // (1 - beta) q, rounded once as an fp64 multiply would
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ns[i] = nl[i] = widen_exact(qf[i]);
+  } else if (!other) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      if (a.q_f32 || !mul_w_bf16(mws, ews, qb[i], cs[i])) cs[i] = ws * q[i];
-      if (a.q_f32 || !mul_w_bf16(mwl, ewl, qb[i], cl[i])) cl[i] = wl * q[i];
+      const uint4 t = wq[qb[i] & 0x7fu];
+      const unsigned adj = ((qb[i] & 0x7f80u) << 13) | ((qb[i] & 0x8000u) << 16);  // (e << 20) | (s << 31)
+      ns[i] = fma(a.beta_s, os[i], __hiloint2double((int)(t.y + adj), (int)t.x));
+      nl[i] = fma(a.beta_l, ol[i], __hiloint2double((int)(t.w + adj), (int)t.z));
     }
-    s0 = make_double2(fma(a.beta_s, os0.x, cs[0]), fma(a.beta_s, os0.y, cs[1]));
-    s1 = make_double2(fma(a.beta_s, os1.x, cs[2]), fma(a.beta_s, os1.y, cs[3]));
-    l0 = make_double2(fma(a.beta_l, ol0.x, cl[0]), fma(a.beta_l, ol0.y, cl[1]));
-    l1 = make_double2(fma(a.beta_l, ol1.x, cl[2]), fma(a.beta_l, ol1.y, cl[3]));
+  } else {
+    const double ws = 1.0 - a.beta_s, wl = 1.0 - a.beta_l;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const double q = widen_exact(qf[i]);
+      ns[i] = fma(a.beta_s, os[i], mul_fp64(ws, q));
+      nl[i] = fma(a.beta_l, ol[i], mul_fp64(wl, q));
+    }
   }
+  const double2 s0 = make_double2(ns[0], ns[1]), s1 = make_double2(ns[2], ns[3]);
+  const double2 l0 = make_double2(nl[0], nl[1]), l1 = make_double2(nl[2], nl[3]);
   __stcs(row_s, s0);
   __stcs(row_s + 1, s1);
   __stcs(row_l, l0);
@@ -278,7 +315,8 @@ cudaError_t launch_ema(const EmaArgs& a, cudaStream_t s) {
   split(1.0 - a.beta_s, mws, ews);
   split(1.0 - a.beta_l, mwl, ewl);
   if (ews == 0 || ewl == 0) return cudaErrorInvalidValue;
-  k_ema_update<<<dim3((row + 1023) / 1024, a.n, a.L), 256, 0, s>>>(a, mws, ews, mwl, ewl);
+  const int tab = ews >= 127 && ewl >= 127;  // both weights at least 2^-896
+  k_ema_update<<<dim3((row + 1023) / 1024, a.n, a.L), 256, 0, s>>>(a, mws, ews, mwl, ewl, tab);
   return cudaGetLastError();
 }
 
