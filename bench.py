@@ -217,9 +217,9 @@ class Stream:
             return synth.query_step(self.w, [kind])
 
     def _update(self, q):
-        with torch.cuda.stream(self.torch_stream):
-            self.gp.gp_update_summaries(self.ctx, 1, self.slots, q,
-                                        self.notfirst if self.started else self.first)
+        # the engine launches on its own stream, which draws q
+        self.gp.gp_update_summaries(self.ctx, 1, self.slots, q,
+                                    self.notfirst if self.started else self.first)
         self.started = True
         self.t += 1
 
@@ -560,10 +560,11 @@ class Batch:
             self._update(q)
 
     def _update(self, q):
+        # after the refills, which run on the current stream; the engine
+        # launches on its own stream
         self.stream.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(self.stream):
-            self.gp.gp_update_summaries(self.ctx, self.w.n, self.slots, q,
-                                        self.first if self.t == 0 else self.notfirst)
+        self.gp.gp_update_summaries(self.ctx, self.w.n, self.slots, q,
+                                    self.first if self.t == 0 else self.notfirst)
         self.t += 1
 
     def query(self):

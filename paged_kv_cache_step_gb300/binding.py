@@ -13,6 +13,7 @@ device memory and streams.
 from __future__ import annotations
 
 import ctypes as C
+import struct
 import os
 from dataclasses import dataclass
 
@@ -216,20 +217,28 @@ _REQ_DTYPE = np.dtype({"names": ["slot", "num_pages", "block_table", "pos"],
                        "itemsize": C.sizeof(GpRequest)})
 
 
+# gp_request packed field by field: {int32 slot, int32 num_pages, pointer
+# block_table, int64 pos}, checked against the ctypes layout at import.
+_REQ_PACK = struct.Struct("=iiQq")
+assert (_REQ_PACK.size == C.sizeof(GpRequest) and GpRequest.slot.offset == 0 and GpRequest.num_pages.offset == 4
+        and GpRequest.block_table.offset == 8 and GpRequest.pos.offset == 16), "gp_request layout"
+_NUM_PAGES = struct.Struct("=i")
+
+
 def _marshal(reqs):
-    n = len(reqs)
-    arr = (GpRequest * max(1, n))()
-    if n:
-        v = np.frombuffer(arr, dtype=_REQ_DTYPE, count=n)
-        v["slot"] = [r.slot for r in reqs]
-        v["num_pages"] = [r.num_pages for r in reqs]
-        v["block_table"] = [r._bt for r in reqs]
-        v["pos"] = [r.pos for r in reqs]
+    arr = (GpRequest * max(1, len(reqs)))()
+    pack, size = _REQ_PACK.pack_into, _REQ_PACK.size
+    for i, r in enumerate(reqs):
+        pack(arr, i * size, r.slot, r.num_pages, r._bt, r.pos)
     return arr
 
 
 def _unmarshal(arr, reqs):
-    if reqs:
+    if len(reqs) <= 8:
+        get, size = _NUM_PAGES.unpack_from, _REQ_PACK.size
+        for i, r in enumerate(reqs):
+            r.num_pages = get(arr, i * size + 4)[0]
+    else:
         counts = np.frombuffer(arr, dtype=_REQ_DTYPE, count=len(reqs))["num_pages"].tolist()
         for r, p in zip(reqs, counts):
             r.num_pages = p

@@ -97,6 +97,8 @@ struct gp_ctx {
   void* pinned = nullptr;
   size_t pinned_cap = 0;
   cudaEvent_t pinned_free = nullptr;  // recorded after the last async use of `pinned`
+  void* readback = nullptr;           // pinned: a demand call's sums and error word
+  size_t readback_cap = 0;
   // asynchronous compaction: a side stream, the event the side stream waits
   // for (engine stream state), and the event of the last compaction there
   cudaStream_t cstream = nullptr;
@@ -166,6 +168,20 @@ gp_status ensure_pinned(gp_ctx* c, size_t bytes) {
   c->pinned_cap = 0;
   GP_CUDA(c, cudaHostAlloc(&c->pinned, cap, cudaHostAllocDefault));
   c->pinned_cap = cap;
+  return GP_OK;
+}
+
+// The pinned readback buffer; a demand call reads it only after
+// synchronising the stream, so no copy into it is still in flight here.
+gp_status ensure_readback(gp_ctx* c, size_t bytes) {
+  if (bytes <= c->readback_cap) return GP_OK;
+  size_t cap = std::max<size_t>(std::max(bytes, c->readback_cap * 2), 4096);
+  cap = (cap + 4095) & ~size_t(4095);
+  if (c->readback) GP_CUDA(c, cudaFreeHost(c->readback));
+  c->readback = nullptr;
+  c->readback_cap = 0;
+  GP_CUDA(c, cudaHostAlloc(&c->readback, cap, cudaHostAllocDefault));
+  c->readback_cap = cap;
   return GP_OK;
 }
 
@@ -240,10 +256,18 @@ gp_status need_device(gp_ctx* c) {
 // Read and clear the kernels' error word (synchronises the stream).  A word
 // holding only ERR_TIMEOUT (bounded waits gave up) is GP_ERR_TIMEOUT; any
 // failed device-side check makes it GP_ERR_INVALID.
+gp_status kernel_error_status(gp_ctx* c, int e);
+
 gp_status check_kernel_errors(gp_ctx* c) {
   int e = 0;
   GP_CUDA(c, cudaMemcpyAsync(&e, c->err_dev, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
   GP_CUDA(c, cudaStreamSynchronize(c->stream));
+  return kernel_error_status(c, e);
+}
+
+// The status of an error word already read (the stream synchronised); a
+// non-zero word is cleared on the device.
+gp_status kernel_error_status(gp_ctx* c, int e) {
   if (e) {
     GP_CUDA(c, cudaMemsetAsync(c->err_dev, 0, sizeof(int), c->stream));
     GP_CUDA(c, cudaStreamSynchronize(c->stream));
@@ -498,6 +522,7 @@ gp_status gp_destroy(gp_ctx* c) {
     if (c->pool) cudaFree(c->pool);
     if (c->err_dev) cudaFree(c->err_dev);
     if (c->pinned) cudaFreeHost(c->pinned);
+    if (c->readback) cudaFreeHost(c->readback);
     if (c->pinned_free) cudaEventDestroy(c->pinned_free);
     for (auto& t : c->timed) {
       cudaEventDestroy(t.start);
@@ -892,11 +917,16 @@ gp_status gp_boundary_demand(gp_ctx* c, int32_t n, const gp_request* reqs, const
     GP_CUDA(c, cudaMemcpyAsync(eff.data(), c->ent.p, sizeof(double) * eff.size(), cudaMemcpyDeviceToHost,
                                c->stream));
   }
-  std::vector<unsigned long long> sums((size_t)n * 2);
-  GP_CUDA(c, cudaMemcpyAsync(sums.data(), c->ksum.p, sizeof(unsigned long long) * sums.size(),
-                             cudaMemcpyDeviceToHost, c->stream));
-  st = check_kernel_errors(c);  // synchronises
-  if (st != GP_OK) return st;
+  // the sums and the error word in one pinned buffer, read after one
+  // synchronisation
+  const size_t sum_bytes = sizeof(unsigned long long) * (size_t)n * 2;
+  if ((st = ensure_readback(c, sum_bytes + 16)) != GP_OK) return st;
+  const unsigned long long* sums = static_cast<const unsigned long long*>(c->readback);
+  int* err_host = reinterpret_cast<int*>(static_cast<char*>(c->readback) + sum_bytes);
+  GP_CUDA(c, cudaMemcpyAsync(c->readback, c->ksum.p, sum_bytes, cudaMemcpyDeviceToHost, c->stream));
+  GP_CUDA(c, cudaMemcpyAsync(err_host, c->err_dev, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+  GP_CUDA(c, cudaStreamSynchronize(c->stream));
+  if ((st = kernel_error_status(c, *err_host)) != GP_OK) return st;
 
   c->last_demand.assign(n, DemandRec{});
   for (int r = 0; r < n; ++r) {
