@@ -2,8 +2,9 @@
 initialisation) element by element against its exactly rounded value.
 
 The kernel evaluates Eq. 6 in fp64 as one fused multiply-add per element,
-qbar <- RN(beta * qbar + c) with c = RN((1 - beta) * q) (the product taken by
-integer operations, the multiply-add on the fp64 pipe).  Each new value is
+qbar <- RN(beta * qbar + c) with c = RN((1 - beta) * q) (the product read from
+a per-block table of rounded products, or an fp64 multiply for the queries
+the table does not cover; the multiply-add on the fp64 pipe).  Each new value is
 checked against the nearest double (ties to even) of the exact rational
 beta * old + c, computed with fractions.Fraction, so the check rests on
 IEEE 754's rounding rule alone.  The queries span magnitudes 2^-30 .. 2^30,
@@ -96,6 +97,59 @@ def test_summary_update_is_one_correctly_rounded_fma():
             bad = np.flatnonzero(got.view(np.int64) != want.view(np.int64))
             assert bad.size == 0, (f"step {step}: {bad.size} elements differ, first at {bad[0]}: "
                                    f"got {got.reshape(-1)[bad[0]]!r} want {want.reshape(-1)[bad[0]]!r}")
+    finally:
+        gp.gp_destroy(ctx)
+
+
+def _edge_queries(g, n):
+    """bf16 queries at the edges of the format: subnormals (which the kernel
+    multiplies in fp64 instead of taking its product table), the smallest and
+    largest normal exponents, and ordinary values beside them."""
+    bits = torch.randint(0x0080, 0x7f80, (L, n, HQ, D), generator=g, dtype=torch.int32)
+    kind = torch.randint(0, 5, (L, n, HQ, D), generator=g)
+    bits = torch.where(kind == 0, torch.randint(1, 0x80, bits.shape, generator=g, dtype=torch.int32), bits)  # subnormal
+    bits = torch.where(kind == 1, 0x0080 + torch.randint(0, 0x80, bits.shape, generator=g, dtype=torch.int32), bits)
+    bits = torch.where(kind == 2, 0x7f00 + torch.randint(0, 0x80, bits.shape, generator=g, dtype=torch.int32), bits)
+    sign = torch.randint(0, 2, bits.shape, generator=g, dtype=torch.int32) << 15
+    return (bits | sign).to(torch.int16).view(torch.bfloat16)
+
+
+def test_summary_update_edge_queries():
+    """Subnormal and extreme-exponent bf16 queries take the same correctly
+    rounded update; an infinite or NaN query gives the IEEE 754 result."""
+    n = 2
+    ctx, _, _, slots = _ctx(n)
+    g = torch.Generator().manual_seed(23)
+    sl = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    first = torch.ones(n, dtype=torch.uint8, device="cuda")
+    nfirst = torch.zeros_like(first)
+    try:
+        gp.gp_update_summaries(ctx, n, sl, _queries(g, n).cuda(), first)
+        for step in range(2):
+            old = _read(ctx, slots)
+            q = _edge_queries(g, n)
+            gp.gp_update_summaries(ctx, n, sl, q.cuda(), nfirst)
+            got = _read(ctx, slots)
+            want = _rounded_update(old, q.double().numpy())
+            bad = np.flatnonzero(got.view(np.int64) != want.view(np.int64))
+            assert bad.size == 0, (f"step {step}: {bad.size} elements differ, first at {bad[0]}: "
+                                   f"got {got.reshape(-1)[bad[0]]!r} want {want.reshape(-1)[bad[0]]!r}")
+        # non-finite queries on a few elements of otherwise ordinary rows
+        old = _read(ctx, slots)
+        q = _queries(g, n).double()
+        special = torch.zeros(q.shape, dtype=torch.bool)
+        special[0, 0, 0, :3] = True
+        q[0, 0, 0, 0], q[0, 0, 0, 1], q[0, 0, 0, 2] = float("inf"), float("-inf"), float("nan")
+        gp.gp_update_summaries(ctx, n, sl, q.to(torch.bfloat16).cuda(), nfirst)
+        got = _read(ctx, slots)
+        qd = q.to(torch.bfloat16).double().numpy()
+        for x in range(2):
+            assert got[0, 0, x, 0, 0] == np.inf and got[0, 0, x, 0, 1] == -np.inf
+            assert np.isnan(got[0, 0, x, 0, 2])
+        qd_f = np.where(special.numpy(), 0.0, qd)
+        want = _rounded_update(old, qd_f)
+        mask = np.broadcast_to(~special.numpy()[:, :, None], got.shape)
+        assert np.array_equal(got.view(np.int64)[mask], want.view(np.int64)[mask])
     finally:
         gp.gp_destroy(ctx)
 
