@@ -246,6 +246,28 @@ def test_host_only_context_refuses_device_calls():
         gp.gp_destroy(ctx)
 
 
+@pytest.mark.parametrize("n", [1, 5, 20])
+def test_request_marshalling_matches_the_c_struct(n):
+    """The binding packs gp_request fields with struct; read back through the
+    ctypes field descriptors they are the requests' own values, and
+    num_pages written by the C side comes back to each request (both
+    read-back paths: up to 8 requests and more)."""
+    import ctypes as C
+    from paged_kv_cache_step_gb300 import binding as bd
+    rng = np.random.default_rng(n)
+    reqs = [gp.Request(int(rng.integers(0, 512)), list(rng.integers(0, 1000, int(rng.integers(1, 9)))),
+                       int(rng.integers(0, 1 << 40)), 16) for _ in range(n)]
+    arr = bd._marshal(reqs)
+    for i, r in enumerate(reqs):
+        assert arr[i].slot == r.slot and arr[i].num_pages == r.num_pages and arr[i].pos == r.pos
+        assert C.cast(arr[i].block_table, C.c_void_p).value == r.table.ctypes.data
+        assert arr[i].block_table[r.num_pages - 1] == r.pages[-1]
+    for i in range(n):
+        arr[i].num_pages = i + 1
+    bd._unmarshal(arr, reqs)
+    assert [r.num_pages for r in reqs] == list(range(1, n + 1))
+
+
 def test_mask_pack_roundtrip():
     rng = np.random.default_rng(2)
     keep = rng.random((3, 512)) < 0.5
